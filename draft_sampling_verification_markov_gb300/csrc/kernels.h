@@ -1,0 +1,75 @@
+// kernels.h -- host-side launchers of the libspecmarkov kernels (internal to the library).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace spec {
+
+// Number of vocabulary columns per partial of the Markov producers (one epilogue half-tile).
+constexpr int kMarkovSeg = 64;
+// Number of vocabulary columns per partial of the rank-0 streaming producer.
+constexpr int kStreamSeg = 8192;
+
+// Per-row outputs of a select pass.
+struct SelectOut {
+  int kind;              // 0: draft proposal at position k, 1: final token of rejection verify
+  int32_t* tokens;       // kind 0: draft_tokens [R, gamma]; kind 1: out_tokens [R, gamma+1]
+  float* logp;           // kind 0, optional
+  float* stats;          // kind 0, optional
+  int32_t* next_anchor;  // kind 1, optional
+  const float* uni;      // uniforms, indexed row * uni_stride + uni_offset
+  int uni_stride, uni_offset;
+  int greedy;
+};
+
+void launch_stream_partials(const RowJob& j, int dtype, int seg, int nseg, bool vec, bool sum,
+                            bool argmax, float* pm, float* ps, int* pi, int grid,
+                            cudaStream_t s);
+void launch_ffma_partials(const RowJob& j, int udt, int wdt, int nseg, bool argmax, float* pm,
+                          float* ps, int* pi, int grid, cudaStream_t s);
+void launch_select(const RowJob& j, int udt, int wdt, int seg, int nseg, const float* pm,
+                   const float* ps, const int* pi, const SelectOut& o, cudaStream_t s);
+void launch_finalize_stats(int rows, int nseg, const float* pm, const float* ps, float* stats,
+                           const int32_t* lengths, int rows_per_req, uint32_t* status,
+                           cudaStream_t s);
+void launch_greedy_scan(int R, int gamma, int V, int nseg, const float* pm, const int* pi,
+                        const int32_t* tokens, const int32_t* lengths, int32_t* accept_len,
+                        int32_t* out_tokens, int32_t* next_anchor, uint32_t* status,
+                        cudaStream_t s);
+void launch_accept(int dtype, int R, int gamma, int V, float scale, const void* T,
+                   const float* tstats, const int32_t* tokens, const float* dlogp,
+                   const float* u_accept, const int32_t* lengths, int32_t* final_n,
+                   int32_t* final_kind, int32_t* accept_len, int32_t* out_tokens,
+                   uint32_t* status, cudaStream_t s);
+void launch_tv_finalize(int R, int gamma, int nseg, const float* ps, float* conf, float* survival,
+                        cudaStream_t s);
+cudaError_t launch_schedule(const float* survival, const double* sps, int Bmax, int R, int gamma,
+                            int32_t* lengths, int32_t* B_out, double* theta_out, uint32_t* status,
+                            cudaStream_t s);
+size_t schedule_smem_bytes(int R, int gamma);
+
+// tcgen05 Markov producer (markov_tc.cu). Returns false when the shape is not supported
+// (the caller then uses the CUDA-core producer).
+bool markov_tc_supported(int udt, int wdt, int rank, int V, const void* U, const void* T,
+                         const void* W1, const void* W2);
+cudaError_t launch_markov_tc(const RowJob& j, float* pm, float* ps, int* pi, bool argmax,
+                             cudaStream_t s);
+
+int num_sms();
+
+// Tracing hooks around every launch (api.cu): count the launch and record the attached begin /
+// end events of its kernel class on the launch stream.
+void trace_begin(int kclass, cudaStream_t s);
+void trace_end(int kclass, cudaStream_t s);
+
+struct TraceScope {
+  int kclass;
+  cudaStream_t s;
+  TraceScope(int k, cudaStream_t st) : kclass(k), s(st) { trace_begin(k, st); }
+  ~TraceScope() { trace_end(kclass, s); }
+};
+
+}  // namespace spec

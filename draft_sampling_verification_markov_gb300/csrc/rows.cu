@@ -1,0 +1,691 @@
+// rows.cu -- streaming row reductions, the generic (CUDA-core) Markov producer, and the
+// select / verify / finalize consumers of libspecmarkov.
+//
+// Producers reduce every (row, segment) of a pass to a partial:
+//   stream_partials_kernel   rank-0 rows (no Markov bias): a pure HBM stream of 16-byte loads;
+//   markov_ffma_partials     rows with a Markov bias computed on CUDA cores in the canonical
+//                            fp32 order (fp32 weights, and every shape the tcgen05 kernel does
+//                            not take).
+// Consumers:
+//   select_kernel            per row: combine partials, then greedy argmax or the inverse-CDF
+//                            draw (recomputing only the crossing segment);
+//   finalize_stats_kernel    per row (m, log Z);
+//   greedy_scan_kernel       per request longest-prefix match + bonus;
+//   accept_kernel            per request rejection-sampling acceptance scan;
+//   tv_finalize_kernel       per request c* and the survival product.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace spec {
+
+// ------------------------------------------------------------------------------ logits
+
+// Draft logit z_d(v) of a row (DSpark sections 3-4): (U + W1[prev] . W2[v]) * scale, the bias
+// in the canonical fp32 chain acc = fma(W1[prev][i], W2[v][i], acc), i ascending.
+template <int UDT, int WDT>
+__device__ __forceinline__ float draft_logit(const RowJob& j, const RowInfo& ri, int v) {
+  float acc = 0.0f;
+  if (j.rank > 0) {
+    const size_t a = (size_t)ri.prev * j.rank, b = (size_t)v * j.rank;
+    for (int i = 0; i < j.rank; ++i)
+      acc = __fmaf_rn(ld_elem<WDT>(j.W1, a + i), ld_elem<WDT>(j.W2, b + i), acc);
+  }
+  const float s = __fadd_rn(ld_elem<UDT>(j.U, (size_t)ri.urow * j.V + v), acc);
+  return __fmul_rn(s, j.scale);
+}
+
+template <int DT>
+__device__ __forceinline__ float target_logit(const RowJob& j, const RowInfo& ri, int v) {
+  return __fmul_rn(ld_elem<DT>(j.T, (size_t)ri.trow * j.V + v), j.scale);
+}
+
+// Element value of a MODE_RESID / MODE_TV pass at column v.
+template <int UDT, int WDT, int MODE>
+__device__ __forceinline__ float pair_value(const RowJob& j, const RowInfo& ri, Norm dn, Norm tn,
+                                            int v) {
+  const float pt = prob_of(target_logit<UDT>(j, ri, v), tn);
+  if (MODE == MODE_RESID && !ri.resid) return pt;  // bonus row: q = p_t
+  const float pd = prob_of(draft_logit<UDT, WDT>(j, ri, v), dn);
+  if (MODE == MODE_RESID) return fmaxf(pt - pd, 0.0f);
+  return fminf(pt, pd);
+}
+
+__device__ __forceinline__ void row_norms(const RowJob& j, const RowInfo& ri, Norm& dn, Norm& tn) {
+  dn = {0.0f, 0.0f};
+  tn = {0.0f, 0.0f};
+  if (ri.trow >= 0 && j.tstats) tn = load_norm(j.tstats, ri.trow);
+  if (ri.urow >= 0 && j.dstats) dn = load_norm(j.dstats, ri.urow);
+}
+
+// ------------------------------------------------------------------------------ streaming producer
+
+// 8 consecutive elements starting at v (v % 8 == 0), vectorised when `vec`.
+template <int DT>
+__device__ __forceinline__ void load8(const void* base, size_t row_off, int v, int V, bool vec,
+                                      float (&x)[8]) {
+  if constexpr (DT == SPEC_BF16) {
+    const unsigned short* p = reinterpret_cast<const unsigned short*>(base) + row_off + v;
+    if (vec && v + 8 <= V) {
+      const uint4 q = ld_stream16(p);
+      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        x[2 * i] = __uint_as_float(w[i] << 16);
+        x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) x[i] = (v + i < V) ? bf16_to_f32(__ldg(p + i)) : -INFINITY;
+    }
+  } else {
+    const float* p = reinterpret_cast<const float*>(base) + row_off + v;
+    if (vec && v + 8 <= V) {
+      const uint4 q0 = ld_stream16(p), q1 = ld_stream16(p + 4);
+      x[0] = __uint_as_float(q0.x); x[1] = __uint_as_float(q0.y);
+      x[2] = __uint_as_float(q0.z); x[3] = __uint_as_float(q0.w);
+      x[4] = __uint_as_float(q1.x); x[5] = __uint_as_float(q1.y);
+      x[6] = __uint_as_float(q1.z); x[7] = __uint_as_float(q1.w);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) x[i] = (v + i < V) ? __ldg(p + i) : -INFINITY;
+    }
+  }
+}
+
+// Rank-0 rows. One block per (row, segment) unit, grid-stride. MODE_STATS reduces the row's
+// primary logits (U if the row has a draft side, else the target); SUM / ARGMAX select which
+// halves of the partial are needed. MODE_RESID / MODE_TV reduce the pair value.
+template <int DT, int MODE, bool SUM, bool ARGMAX>
+__global__ void __launch_bounds__(256) stream_partials_kernel(RowJob j, int seg, int nseg, bool vec,
+                                                              float* pm, float* ps, int* pi) {
+  const long long units = (long long)j.rows * nseg;
+  for (long long u = blockIdx.x; u < units; u += gridDim.x) {
+    const int row = (int)(u / nseg), sg = (int)(u % nseg);
+    const RowInfo ri = row_info(j, row);
+    const int v0 = sg * seg, v1 = min(j.V, v0 + seg);
+    const size_t out = (size_t)sg * j.rows + row;
+    if (!ri.active) {
+      if (threadIdx.x == 0) {
+        if (pm) pm[out] = -INFINITY;
+        if (ps) ps[out] = 0.0f;
+        if (pi) pi[out] = 0x7fffffff;
+      }
+      continue;
+    }
+    if constexpr (MODE == MODE_STATS) {
+      const bool draft = ri.urow >= 0;
+      const void* src = draft ? j.U : j.T;
+      const size_t off = (size_t)(draft ? ri.urow : ri.trow) * j.V;
+      StatsAcc acc = stats_empty();
+      for (int v = v0 + threadIdx.x * 8; v < v1; v += blockDim.x * 8) {
+        float x[8];
+        load8<DT>(src, off, v, v1, vec, x);
+        float g = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          x[i] = __fmul_rn(x[i], j.scale);
+          if (ARGMAX && x[i] > acc.m && x[i] > g) {  // first strict maximum in order
+            g = x[i];
+            acc.idx = v + i;
+          }
+          g = fmaxf(g, x[i]);
+        }
+        if (g > acc.m) {
+          if (SUM && acc.s != 0.0f) acc.s *= exp_shift(acc.m, g);
+          acc.m = g;
+        }
+        if (SUM && acc.m != -INFINITY) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc.s += exp_shift(x[i], acc.m);
+        }
+      }
+      acc = block_merge(acc);
+      if (threadIdx.x == 0) {
+        pm[out] = acc.m;
+        if (ps) ps[out] = acc.s;
+        if (pi) pi[out] = acc.idx;
+      }
+    } else {
+      Norm dn, tn;
+      row_norms(j, ri, dn, tn);
+      const bool pair = MODE == MODE_TV || ri.resid;
+      float acc = 0.0f;
+      for (int v = v0 + threadIdx.x * 8; v < v1; v += blockDim.x * 8) {
+        float xt[8], xd[8];
+        load8<DT>(j.T, (size_t)ri.trow * j.V, v, v1, vec, xt);
+        if (pair) load8<DT>(j.U, (size_t)ri.urow * j.V, v, v1, vec, xd);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (v + i >= v1) continue;
+          const float pt = prob_of(__fmul_rn(xt[i], j.scale), tn);
+          if (!pair) {
+            acc += pt;
+            continue;
+          }
+          const float pd = prob_of(__fmul_rn(xd[i], j.scale), dn);
+          acc += MODE == MODE_RESID ? fmaxf(pt - pd, 0.0f) : fminf(pt, pd);
+        }
+      }
+      acc = block_sum(acc);
+      if (threadIdx.x == 0) ps[out] = acc;
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------ generic Markov producer
+
+// One warp per (row, 64-column chunk); lane l handles columns c*64 + l and c*64 + 32 + l.
+template <int UDT, int WDT, int MODE, bool ARGMAX>
+__global__ void __launch_bounds__(256) markov_ffma_partials(RowJob j, int nseg, float* pm, float* ps,
+                                                            int* pi) {
+  const int lane = threadIdx.x & 31;
+  const long long units = (long long)j.rows * nseg;
+  const long long stride = (long long)gridDim.x * (blockDim.x >> 5);
+  for (long long u = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); u < units;
+       u += stride) {
+    const int row = (int)(u / nseg), c = (int)(u % nseg);
+    const RowInfo ri = row_info(j, row);
+    const size_t out = (size_t)c * j.rows + row;
+    if constexpr (MODE == MODE_STATS) {
+      StatsAcc acc = stats_empty();
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int v = c * 64 + h * 32 + lane;
+        if (v < j.V) {
+          const float z = draft_logit<UDT, WDT>(j, ri, v);
+          StatsAcc e = {z, 1.0f, v};
+          if (!(z > -INFINITY)) e = {-INFINITY, 0.0f, v};
+          acc = stats_merge(acc, e);
+        }
+      }
+      acc = warp_merge(acc);
+      if (lane == 0) {
+        pm[out] = acc.m;
+        ps[out] = acc.s;
+        if (ARGMAX) pi[out] = acc.idx;
+      }
+    } else {
+      Norm dn, tn;
+      row_norms(j, ri, dn, tn);
+      float acc = 0.0f;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int v = c * 64 + h * 32 + lane;
+        if (v < j.V) acc += pair_value<UDT, WDT, MODE>(j, ri, dn, tn, v);
+      }
+      acc = warp_sum(acc);
+      if (lane == 0) ps[out] = acc;
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------ select
+
+// Exclusive block scan of one double per thread (blockDim.x == 256); returns the exclusive
+// prefix and writes the block total.
+__device__ __forceinline__ double block_exscan_d(double x, double* total) {
+  __shared__ double sm[32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  double inc = x;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const double y = __shfl_up_sync(0xffffffffu, inc, off);
+    if (lane >= off) inc += y;
+  }
+  __syncthreads();
+  if (lane == 31) sm[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    double w = lane < nw ? sm[lane] : 0.0;
+    double wi = w;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const double y = __shfl_up_sync(0xffffffffu, wi, off);
+      if (lane >= off) wi += y;
+    }
+    if (lane < nw) sm[lane] = wi - w;  // exclusive warp offsets
+    if (lane == nw - 1) sm[31] = wi;
+  }
+  __syncthreads();
+  const double ex = sm[warp] + inc - x;
+  *total = sm[31];
+  __syncthreads();
+  return ex;
+}
+
+// One block (256 threads) per row.
+//   kind 0 (MODE_STATS partials): greedy argmax, or inverse-CDF draw from the softmax;
+//   kind 1 (MODE_RESID partials): inverse-CDF draw from the residual / bonus distribution.
+// The crossing segment is recomputed element by element; everything else uses the partials.
+template <int UDT, int WDT>
+__global__ void __launch_bounds__(256) select_kernel(RowJob j, int seg, int nseg, const float* pm,
+                                                     const float* ps, const int* pi,
+                                                     SelectOut o) {
+  __shared__ int sh_c;
+  __shared__ double sh_rem;
+  __shared__ float sh_M, sh_lz;
+  const int row = blockIdx.x;
+  if (row >= j.rows) return;
+  const RowInfo ri = row_info(j, row);
+  const int tid = threadIdx.x;
+  const int resid = o.kind == 1;
+
+  // 1. normaliser from the partials
+  float M = -INFINITY;
+  if (!resid) {
+    StatsAcc a = stats_empty();
+    for (int c = tid; c < nseg; c += blockDim.x) {
+      const size_t q = (size_t)c * j.rows + row;
+      a = stats_merge(a, {pm[q], ps[q], pi ? pi[q] : 0x7fffffff});
+    }
+    a = block_merge(a);
+    M = a.m;
+    if (o.greedy) {
+      // argmax from the partials' first maxima
+      if (tid == 0) {
+        int x = a.idx;
+        if (!(M > -INFINITY) || x < 0 || x >= j.V) {
+          atomicOr(j.status, SPEC_DEV_NONFINITE);
+          x = 0;
+        }
+        sh_c = x;
+      }
+    }
+  }
+  // run of segments owned by this thread
+  const int run = (nseg + blockDim.x - 1) / blockDim.x;
+  const int c0 = min(nseg, tid * run), c1 = min(nseg, c0 + run);
+  double local = 0.0;
+  for (int c = c0; c < c1; ++c) {
+    const size_t q = (size_t)c * j.rows + row;
+    local += resid ? (double)ps[q]
+                   : (ps[q] == 0.0f ? 0.0 : (double)ps[q] * (double)exp_shift(pm[q], M));
+  }
+  double Z;
+  const double before = block_exscan_d(local, &Z);
+  if (!resid && tid == 0) {
+    sh_M = M;
+    sh_lz = (float)log(Z);
+    if (!(Z > 0.0) || !isfinite(Z) || !(M > -INFINITY)) atomicOr(j.status, SPEC_DEV_NONFINITE);
+  }
+
+  int x;
+  if (!resid && o.greedy) {
+    __syncthreads();
+    x = sh_c;
+  } else {
+    // 2. crossing segment for t = u * Z
+    const double u = (double)o.uni[(size_t)row * o.uni_stride + o.uni_offset];
+    const double t = u * Z;
+    if (tid == 0) {
+      sh_c = -1;
+      sh_rem = 0.0;
+    }
+    __syncthreads();
+    if (before <= t && before + local > t) {
+      double cum = before;
+      int lastc = -1;
+      double lastw = 0.0;
+      for (int c = c0; c < c1; ++c) {
+        const size_t q = (size_t)c * j.rows + row;
+        const double w = resid ? (double)ps[q]
+                               : (ps[q] == 0.0f ? 0.0 : (double)ps[q] * (double)exp_shift(pm[q], M));
+        if (cum + w > t) {
+          lastc = c;
+          lastw = t - cum;
+          break;
+        }
+        if (w > 0.0) {
+          lastc = c;
+          lastw = 1e300;  // summation-order rounding: end of the last positive segment
+        }
+        cum += w;
+      }
+      sh_c = lastc;
+      sh_rem = lastw;
+    }
+    __syncthreads();
+    if (sh_c < 0) {
+      // rounding left no crossing: take the last segment with positive mass, at its end
+      if (tid == 0) {
+        int last = -1;
+        for (int c = nseg - 1; c >= 0 && last < 0; --c)
+          if (ps[(size_t)c * j.rows + row] > 0.0f) last = c;
+        if (last < 0) atomicOr(j.status, resid ? SPEC_DEV_EMPTY_RESIDUAL : SPEC_DEV_NONFINITE);
+        sh_c = last;
+        sh_rem = 1e300;
+      }
+      __syncthreads();
+    }
+    const int cstar = sh_c;
+    const double rem = sh_rem;
+    // 3. recompute the crossing segment and scan it in token order
+    Norm dn, tn;
+    if (resid) row_norms(j, ri, dn, tn);
+    const int v0 = max(cstar, 0) * seg, v1 = min(j.V, v0 + seg);
+    const int per = (seg + blockDim.x - 1) / blockDim.x;
+    const int e0 = min(v1, v0 + tid * per), e1 = min(v1, e0 + per);
+    float mine = 0.0f;
+    for (int v = e0; v < e1; ++v)
+      mine += resid ? pair_value<UDT, WDT, MODE_RESID>(j, ri, dn, tn, v)
+                    : exp_shift(draft_logit<UDT, WDT>(j, ri, v), M);
+    double segtot;
+    const double sbefore = block_exscan_d((double)mine, &segtot);
+    __shared__ int sh_x;
+    __shared__ int sh_last;
+    if (tid == 0) {
+      sh_x = -1;
+      sh_last = -1;
+    }
+    __syncthreads();
+    if (cstar >= 0) {
+      if (sbefore <= rem && sbefore + (double)mine > rem) {
+        double cum = sbefore;
+        for (int v = e0; v < e1; ++v) {
+          const float w = resid ? pair_value<UDT, WDT, MODE_RESID>(j, ri, dn, tn, v)
+                                : exp_shift(draft_logit<UDT, WDT>(j, ri, v), M);
+          if (cum + (double)w > rem) {
+            sh_x = v;
+            break;
+          }
+          cum += w;
+        }
+      }
+      // last positive element of the segment (fallback for a remainder past its end)
+      int lastp = -1;
+      for (int v = e1 - 1; v >= e0 && lastp < 0; --v) {
+        const float w = resid ? pair_value<UDT, WDT, MODE_RESID>(j, ri, dn, tn, v)
+                              : exp_shift(draft_logit<UDT, WDT>(j, ri, v), M);
+        if (w > 0.0f) lastp = v;
+      }
+      if (lastp >= 0) atomicMax(&sh_last, lastp);
+    }
+    __syncthreads();
+    x = sh_x >= 0 ? sh_x : sh_last;
+    if (x < 0) {
+      // no mass at all: emit a valid id (the proposed token at the rejected position for a
+      // residual, token 0 otherwise); the status word already records the fault
+      x = 0;
+      if (resid && ri.resid) {
+        const int n = j.final_n[row];
+        x = j.tokens[(size_t)row * j.gamma + n];
+        if (x < 0 || x >= j.V) x = 0;
+      }
+    }
+  }
+
+  // 4. outputs
+  if (tid == 0) {
+    if (!resid) {
+      const size_t q = (size_t)row * j.gamma + (j.k - 1);
+      o.tokens[q] = x;
+      if (o.logp) o.logp[q] = draft_logit<UDT, WDT>(j, ri, x) - sh_M - sh_lz;
+      if (o.stats) {
+        o.stats[2 * q] = sh_M;
+        o.stats[2 * q + 1] = sh_lz;
+      }
+    } else {
+      const int n = j.final_n[row];
+      o.tokens[(size_t)row * (j.gamma + 1) + n] = x;
+      if (o.next_anchor) o.next_anchor[row] = x;
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------ finalize / scans
+
+// (m, log Z) per row from MODE_STATS partials; one warp per row.
+__global__ void finalize_stats_kernel(int rows, int nseg, const float* pm, const float* ps,
+                                      float* stats, const int32_t* lengths, int rows_per_req,
+                                      uint32_t* status) {
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  if (lengths && (row % rows_per_req) > min(max(lengths[row / rows_per_req], 0), rows_per_req - 1))
+    return;  // row beyond the verified length: never read
+  float M = -INFINITY;
+  for (int c = lane; c < nseg; c += 32) M = fmaxf(M, pm[(size_t)c * rows + row]);
+  M = warp_max(M);
+  double Z = 0.0;
+  for (int c = lane; c < nseg; c += 32) {
+    const size_t q = (size_t)c * rows + row;
+    if (ps[q] != 0.0f) Z += (double)ps[q] * (double)exp_shift(pm[q], M);
+  }
+  Z = warp_sum_d(Z);
+  if (lane == 0) {
+    if (!(Z > 0.0) || !isfinite(Z) || !(M > -INFINITY)) atomicOr(status, SPEC_DEV_NONFINITE);
+    stats[2 * (size_t)row] = M;
+    stats[2 * (size_t)row + 1] = (float)log(Z);
+  }
+}
+
+// Greedy longest-prefix match + bonus, one thread per request, from target argmax partials.
+__global__ void greedy_scan_kernel(int R, int gamma, int V, int nseg, const float* pm,
+                                   const int* pi, const int32_t* tokens, const int32_t* lengths,
+                                   int32_t* accept_len, int32_t* out_tokens,
+                                   int32_t* next_anchor, uint32_t* status) {
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= R) return;
+  const int rows = R * (gamma + 1);
+  int l = gamma;
+  if (lengths) {
+    l = lengths[r];
+    if (l < 0 || l > gamma) {
+      atomicOr(status, SPEC_DEV_BAD_LENGTH);
+      l = l < 0 ? 0 : gamma;
+    }
+  }
+  int n = 0, y = 0;
+  for (int i = 0; i <= l; ++i) {
+    const int row = r * (gamma + 1) + i;
+    float best = -INFINITY;
+    int idx = -1;
+    for (int c = 0; c < nseg; ++c) {
+      const float m = pm[(size_t)c * rows + row];
+      if (m > best) {
+        best = m;
+        idx = pi[(size_t)c * rows + row];
+      }
+    }
+    if (idx < 0 || idx >= V) {
+      atomicOr(status, SPEC_DEV_NONFINITE);
+      idx = 0;
+    }
+    y = idx;
+    if (i == l || tokens[(size_t)r * gamma + i] != y) break;
+    n = i + 1;
+  }
+  accept_len[r] = n;
+  if (out_tokens) {
+    int32_t* o = out_tokens + (size_t)r * (gamma + 1);
+    for (int i = 0; i <= gamma; ++i) o[i] = i < n ? tokens[(size_t)r * gamma + i] : -1;
+    o[n] = y;
+  }
+  if (next_anchor) next_anchor[r] = y;
+}
+
+// Rejection-sampling acceptance scan, one thread per request. Accept x_k iff
+// u_accept * p_d(x_k) < p_t,k-1(x_k); records n_r and whether the final token is a residual
+// draw (rejection) or a bonus draw (all l accepted).
+template <int DT>
+__global__ void accept_kernel(int R, int gamma, int V, float scale, const void* T,
+                              const float* tstats, const int32_t* tokens, const float* dlogp,
+                              const float* u_accept, const int32_t* lengths, int32_t* final_n,
+                              int32_t* final_kind, int32_t* accept_len, int32_t* out_tokens,
+                              uint32_t* status) {
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= R) return;
+  int l = gamma;
+  if (lengths) {
+    l = lengths[r];
+    if (l < 0 || l > gamma) {
+      atomicOr(status, SPEC_DEV_BAD_LENGTH);
+      l = l < 0 ? 0 : gamma;
+    }
+  }
+  int n = 0;
+  for (int k = 1; k <= l; ++k) {
+    int x = tokens[(size_t)r * gamma + k - 1];
+    if (x < 0 || x >= V) {
+      atomicOr(status, SPEC_DEV_BAD_TOKEN);
+      break;  // an invalid proposal is rejected
+    }
+    const long long trow = (long long)r * (gamma + 1) + (k - 1);
+    const float t = __fmul_rn(ld_elem<DT>(T, (size_t)trow * V + x), scale);
+    const float pt = prob_of(t, load_norm(tstats, trow));
+    const float pd = fast_exp2(dlogp[(size_t)r * gamma + k - 1] * kLog2e);  // exp(log p_d)
+    if (!(u_accept[(size_t)r * gamma + k - 1] * pd < pt)) break;
+    n = k;
+  }
+  final_n[r] = n;
+  final_kind[r] = n < l ? 1 : 0;
+  accept_len[r] = n;
+  if (out_tokens) {
+    int32_t* o = out_tokens + (size_t)r * (gamma + 1);
+    for (int i = 0; i <= gamma; ++i) o[i] = i < n ? tokens[(size_t)r * gamma + i] : -1;
+  }
+}
+
+// c*_{r,k} = sum of the MODE_TV partials of row (r, k), clamped to [0, 1]; survival
+// a_{r,j} = fl32(a_{r,j-1} * c_{r,j}) in order. One warp per request.
+__global__ void tv_finalize_kernel(int R, int gamma, int nseg, const float* ps, float* conf,
+                                   float* survival) {
+  const int lane = threadIdx.x & 31;
+  const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (r >= R) return;
+  const int rows = R * gamma;
+  float a = 1.0f;
+  for (int k = 0; k < gamma; ++k) {
+    const int row = r * gamma + k;
+    double c = 0.0;
+    for (int s = lane; s < nseg; s += 32) c += (double)ps[(size_t)s * rows + row];
+    c = warp_sum_d(c);
+    if (lane == 0) {
+      float cf = (float)c;
+      cf = fminf(fmaxf(cf, 0.0f), 1.0f);
+      a = __fmul_rn(a, cf);
+      conf[row] = cf;
+      if (survival) survival[row] = a;
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------ launchers
+
+namespace {
+template <int DT, int MODE, bool SUM, bool ARGMAX>
+void launch_stream_t(const RowJob& j, int seg, int nseg, bool vec, float* pm, float* ps, int* pi,
+                     int grid, cudaStream_t s) {
+  stream_partials_kernel<DT, MODE, SUM, ARGMAX><<<grid, 256, 0, s>>>(j, seg, nseg, vec, pm, ps, pi);
+}
+
+template <int UDT, int WDT>
+void launch_ffma_t(const RowJob& j, int nseg, bool argmax, float* pm, float* ps, int* pi, int grid,
+                   cudaStream_t s) {
+  switch (j.mode) {
+    case MODE_STATS:
+      if (argmax)
+        markov_ffma_partials<UDT, WDT, MODE_STATS, true><<<grid, 256, 0, s>>>(j, nseg, pm, ps, pi);
+      else
+        markov_ffma_partials<UDT, WDT, MODE_STATS, false><<<grid, 256, 0, s>>>(j, nseg, pm, ps, pi);
+      break;
+    case MODE_RESID:
+      markov_ffma_partials<UDT, WDT, MODE_RESID, false><<<grid, 256, 0, s>>>(j, nseg, pm, ps, pi);
+      break;
+    default:
+      markov_ffma_partials<UDT, WDT, MODE_TV, false><<<grid, 256, 0, s>>>(j, nseg, pm, ps, pi);
+      break;
+  }
+}
+}  // namespace
+
+void launch_stream_partials(const RowJob& j, int dtype, int seg, int nseg, bool vec, bool sum,
+                            bool argmax, float* pm, float* ps, int* pi, int grid, cudaStream_t s) {
+  TraceScope ts(SPEC_KCLASS_STREAM, s);
+  if (dtype == SPEC_BF16) {
+    switch (j.mode) {
+      case MODE_STATS:
+        if (sum && argmax) launch_stream_t<SPEC_BF16, MODE_STATS, true, true>(j, seg, nseg, vec, pm, ps, pi, grid, s);
+        else if (sum) launch_stream_t<SPEC_BF16, MODE_STATS, true, false>(j, seg, nseg, vec, pm, ps, pi, grid, s);
+        else launch_stream_t<SPEC_BF16, MODE_STATS, false, true>(j, seg, nseg, vec, pm, ps, pi, grid, s);
+        break;
+      case MODE_RESID: launch_stream_t<SPEC_BF16, MODE_RESID, true, false>(j, seg, nseg, vec, pm, ps, pi, grid, s); break;
+      default: launch_stream_t<SPEC_BF16, MODE_TV, true, false>(j, seg, nseg, vec, pm, ps, pi, grid, s); break;
+    }
+  } else {
+    switch (j.mode) {
+      case MODE_STATS:
+        if (sum && argmax) launch_stream_t<SPEC_F32, MODE_STATS, true, true>(j, seg, nseg, vec, pm, ps, pi, grid, s);
+        else if (sum) launch_stream_t<SPEC_F32, MODE_STATS, true, false>(j, seg, nseg, vec, pm, ps, pi, grid, s);
+        else launch_stream_t<SPEC_F32, MODE_STATS, false, true>(j, seg, nseg, vec, pm, ps, pi, grid, s);
+        break;
+      case MODE_RESID: launch_stream_t<SPEC_F32, MODE_RESID, true, false>(j, seg, nseg, vec, pm, ps, pi, grid, s); break;
+      default: launch_stream_t<SPEC_F32, MODE_TV, true, false>(j, seg, nseg, vec, pm, ps, pi, grid, s); break;
+    }
+  }
+}
+
+void launch_ffma_partials(const RowJob& j, int udt, int wdt, int nseg, bool argmax, float* pm,
+                          float* ps, int* pi, int grid, cudaStream_t s) {
+  TraceScope ts(SPEC_KCLASS_MARKOV, s);
+  if (udt == SPEC_BF16 && wdt == SPEC_BF16) launch_ffma_t<SPEC_BF16, SPEC_BF16>(j, nseg, argmax, pm, ps, pi, grid, s);
+  else if (udt == SPEC_BF16) launch_ffma_t<SPEC_BF16, SPEC_F32>(j, nseg, argmax, pm, ps, pi, grid, s);
+  else if (wdt == SPEC_BF16) launch_ffma_t<SPEC_F32, SPEC_BF16>(j, nseg, argmax, pm, ps, pi, grid, s);
+  else launch_ffma_t<SPEC_F32, SPEC_F32>(j, nseg, argmax, pm, ps, pi, grid, s);
+}
+
+void launch_select(const RowJob& j, int udt, int wdt, int seg, int nseg, const float* pm,
+                   const float* ps, const int* pi, const SelectOut& o, cudaStream_t s) {
+  if (j.rows == 0) return;
+  TraceScope ts(SPEC_KCLASS_SELECT, s);
+  if (udt == SPEC_BF16 && wdt == SPEC_BF16) select_kernel<SPEC_BF16, SPEC_BF16><<<j.rows, 256, 0, s>>>(j, seg, nseg, pm, ps, pi, o);
+  else if (udt == SPEC_BF16) select_kernel<SPEC_BF16, SPEC_F32><<<j.rows, 256, 0, s>>>(j, seg, nseg, pm, ps, pi, o);
+  else if (wdt == SPEC_BF16) select_kernel<SPEC_F32, SPEC_BF16><<<j.rows, 256, 0, s>>>(j, seg, nseg, pm, ps, pi, o);
+  else select_kernel<SPEC_F32, SPEC_F32><<<j.rows, 256, 0, s>>>(j, seg, nseg, pm, ps, pi, o);
+}
+
+void launch_finalize_stats(int rows, int nseg, const float* pm, const float* ps, float* stats,
+                           const int32_t* lengths, int rows_per_req, uint32_t* status,
+                           cudaStream_t s) {
+  if (rows == 0) return;
+  TraceScope ts(SPEC_KCLASS_OTHER, s);
+  finalize_stats_kernel<<<(rows + 7) / 8, 256, 0, s>>>(rows, nseg, pm, ps, stats, lengths,
+                                                        rows_per_req, status);
+}
+
+void launch_greedy_scan(int R, int gamma, int V, int nseg, const float* pm, const int* pi,
+                        const int32_t* tokens, const int32_t* lengths, int32_t* accept_len,
+                        int32_t* out_tokens, int32_t* next_anchor, uint32_t* status,
+                        cudaStream_t s) {
+  TraceScope ts(SPEC_KCLASS_OTHER, s);
+  greedy_scan_kernel<<<(R + 127) / 128, 128, 0, s>>>(R, gamma, V, nseg, pm, pi, tokens, lengths,
+                                                     accept_len, out_tokens, next_anchor, status);
+}
+
+void launch_accept(int dtype, int R, int gamma, int V, float scale, const void* T,
+                   const float* tstats, const int32_t* tokens, const float* dlogp,
+                   const float* u_accept, const int32_t* lengths, int32_t* final_n,
+                   int32_t* final_kind, int32_t* accept_len, int32_t* out_tokens,
+                   uint32_t* status, cudaStream_t s) {
+  const int grid = (R + 127) / 128;
+  TraceScope ts(SPEC_KCLASS_OTHER, s);
+  if (dtype == SPEC_BF16)
+    accept_kernel<SPEC_BF16><<<grid, 128, 0, s>>>(R, gamma, V, scale, T, tstats, tokens, dlogp,
+                                                  u_accept, lengths, final_n, final_kind,
+                                                  accept_len, out_tokens, status);
+  else
+    accept_kernel<SPEC_F32><<<grid, 128, 0, s>>>(R, gamma, V, scale, T, tstats, tokens, dlogp,
+                                                 u_accept, lengths, final_n, final_kind,
+                                                 accept_len, out_tokens, status);
+}
+
+void launch_tv_finalize(int R, int gamma, int nseg, const float* ps, float* conf, float* survival,
+                        cudaStream_t s) {
+  TraceScope ts(SPEC_KCLASS_OTHER, s);
+  tv_finalize_kernel<<<(R + 7) / 8, 256, 0, s>>>(R, gamma, nseg, ps, conf, survival);
+}
+
+}  // namespace spec

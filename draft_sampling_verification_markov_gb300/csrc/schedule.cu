@@ -1,0 +1,199 @@
+// schedule.cu -- hardware-aware prefix scheduler ("[DeepSeek-6] DSpark", section 6).
+//
+// Maximise Theta = tau * SPS(B) over the verify lengths l_r, with B = sum(1 + l_r) and
+// tau = sum(1 + sum_{j<=l_r} a_{r,j}). Every candidate (r, j) is queued by a_{r,j} in decreasing
+// order (ties: r ascending, then j ascending); because a is non-increasing in j, every queue
+// prefix is prefix-closed per request, and for a fixed B = R + K the first K candidates give the
+// largest tau. Scanning K therefore finds the optimum.
+//
+// One CTA does everything in shared memory (R * gamma <= 16384 candidates):
+//   1. keys = (~bits(a) << 32) | (r * gamma + j - 1), sorted ascending by a bitonic network;
+//   2. q = round-half-even(a * 2^32) per sorted candidate, an exact uint64 inclusive scan S_K;
+//   3. Theta(K) = double(R * 2^32 + S_K) * sps[R + K], arg-max with the smallest K on ties;
+//   4. l_r = number of selected candidates of request r.
+// The integer prefix sums and the single IEEE multiply make the result independent of the
+// summation order, so it is bit-identical to any implementation of the same definition.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace spec {
+
+constexpr int kSchedThreads = 1024;
+
+__global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float* survival,
+                                                                 const double* sps, int Bmax,
+                                                                 int R, int gamma, int npow2,
+                                                                 int32_t* lengths, int32_t* B_out,
+                                                                 double* theta_out,
+                                                                 uint32_t* status) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  unsigned long long* key = reinterpret_cast<unsigned long long*>(smem);  // [npow2]
+  int* len = reinterpret_cast<int*>(key + npow2);                       // [R]
+  __shared__ unsigned long long warp_tot[32];
+  __shared__ double best_theta[32];
+  __shared__ int best_k[32];
+
+  const int n = R * gamma;
+  const int tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
+
+  // 1. keys
+  for (int i = tid; i < npow2; i += blockDim.x) {
+    unsigned long long k = ~0ull;
+    if (i < n) {
+      float a = survival[i];
+      if (!(a >= 0.0f && a <= 1.0f)) {  // NaN or out of range: flag and clamp
+        atomicOr(status, SPEC_DEV_NONFINITE);
+        a = a > 1.0f ? 1.0f : 0.0f;
+      }
+      uint32_t bits = __float_as_uint(a) & 0x7fffffffu;  // +0 and -0 alike
+      k = ((unsigned long long)(~bits) << 32) | (unsigned long long)i;
+    }
+    key[i] = k;
+  }
+  for (int r = tid; r < R; r += blockDim.x) len[r] = 0;
+  __syncthreads();
+
+  // bitonic sort, ascending
+  for (int size = 2; size <= npow2; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int t = tid; t < (npow2 >> 1); t += blockDim.x) {
+        const int lo = (t / stride) * stride * 2 + (t % stride);
+        const int hi = lo + stride;
+        const bool up = (lo & size) == 0;
+        const unsigned long long x = key[lo], y = key[hi];
+        if ((x > y) == up) {
+          key[lo] = y;
+          key[hi] = x;
+        }
+      }
+      __syncthreads();
+    }
+  }
+
+  // 2. fixed-point prefix sums over the sorted queue; thread t owns sorted slots
+  //    [t*per, (t+1)*per)
+  const int per = (n + blockDim.x - 1) / blockDim.x;
+  const int s0 = min(n, tid * per), s1 = min(n, s0 + per);
+  auto q_of = [&](int slot) -> unsigned long long {
+    const uint32_t bits = ~(uint32_t)(key[slot] >> 32);
+    const float a = __uint_as_float(bits);
+    return (unsigned long long)__double2ull_rn((double)a * 4294967296.0);
+  };
+  unsigned long long local = 0;
+  for (int s = s0; s < s1; ++s) local += q_of(s);
+  unsigned long long inc = local;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const unsigned long long y = __shfl_up_sync(0xffffffffu, inc, off);
+    if (lane >= off) inc += y;
+  }
+  if (lane == 31) warp_tot[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = blockDim.x >> 5;
+    unsigned long long w = lane < nw ? warp_tot[lane] : 0ull;
+    unsigned long long wi = w;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const unsigned long long y = __shfl_up_sync(0xffffffffu, wi, off);
+      if (lane >= off) wi += y;
+    }
+    if (lane < nw) warp_tot[lane] = wi - w;
+  }
+  __syncthreads();
+  unsigned long long S = warp_tot[warp] + inc - local;  // exclusive prefix of this thread
+
+  // 3. Theta(K) for K in [0, Kmax]; thread t evaluates K = slot + 1 for its slots (and K = 0)
+  const int Kmax = min(n, Bmax - R);
+  const unsigned long long base = (unsigned long long)R << 32;
+  double bt = -1.0;
+  int bk = 0x7fffffff;
+  if (tid == 0) {
+    bt = (double)base * sps[R];
+    bk = 0;
+  }
+  for (int s = s0; s < s1; ++s) {
+    S += q_of(s);
+    const int K = s + 1;
+    if (K > Kmax) break;
+    const double th = (double)(base + S) * sps[R + K];
+    if (th > bt) {  // slots ascend, so the first maximum in this run has the smallest K
+      bt = th;
+      bk = K;
+    }
+  }
+  // block arg-max: larger Theta wins, ties go to the smaller K
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const double ot = __shfl_xor_sync(0xffffffffu, bt, off);
+    const int ok = __shfl_xor_sync(0xffffffffu, bk, off);
+    if (ot > bt || (ot == bt && ok < bk)) {
+      bt = ot;
+      bk = ok;
+    }
+  }
+  if (lane == 0) {
+    best_theta[warp] = bt;
+    best_k[warp] = bk;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = blockDim.x >> 5;
+    bt = lane < nw ? best_theta[lane] : -1.0;
+    bk = lane < nw ? best_k[lane] : 0x7fffffff;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const double ot = __shfl_xor_sync(0xffffffffu, bt, off);
+      const int ok = __shfl_xor_sync(0xffffffffu, bk, off);
+      if (ot > bt || (ot == bt && ok < bk)) {
+        bt = ot;
+        bk = ok;
+      }
+    }
+    if (lane == 0) {
+      best_theta[0] = bt;
+      best_k[0] = bk;
+    }
+  }
+  __syncthreads();
+  const int Kstar = best_k[0];
+
+  // 4. lengths
+  for (int s = tid; s < Kstar; s += blockDim.x) {
+    const int idx = (int)(key[s] & 0xffffffffull);
+    atomicAdd(&len[idx / gamma], 1);
+  }
+  __syncthreads();
+  for (int r = tid; r < R; r += blockDim.x) lengths[r] = len[r];
+  if (tid == 0) {
+    *B_out = R + Kstar;
+    *theta_out = best_theta[0] / 4294967296.0;
+  }
+}
+
+size_t schedule_smem_bytes(int R, int gamma) {
+  int n = R * gamma, p = 1;
+  while (p < n) p <<= 1;
+  return (size_t)p * 8 + (size_t)R * 4;
+}
+
+cudaError_t launch_schedule(const float* survival, const double* sps, int Bmax, int R, int gamma,
+                            int32_t* lengths, int32_t* B_out, double* theta_out, uint32_t* status,
+                            cudaStream_t s) {
+  int n = R * gamma, p = 1;
+  while (p < n) p <<= 1;
+  if (p < 2) p = 2;
+  const size_t smem = (size_t)p * 8 + (size_t)R * 4;
+  cudaError_t e = cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  schedule_kernel<<<1, kSchedThreads, smem, s>>>(survival, sps, Bmax, R, gamma, p, lengths, B_out,
+                                                 theta_out, status);
+  return cudaGetLastError();
+}
+
+}  // namespace spec

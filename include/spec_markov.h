@@ -1,0 +1,264 @@
+/*
+ * spec_markov.h -- C ABI of libspecmarkov.so, the token-level hot path of speculative decoding
+ * on GB300 (sm_103a): draft proposal over the vocabulary, target verification, TV confidence
+ * with prefix survival, and the hardware-aware prefix scheduler.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every array argument is a DEVICE pointer owned by the caller; the library never allocates
+ *    device or host memory and never keeps a pointer after the call returns. Scalars are passed
+ *    by value; the few host outputs are named *_host below.
+ *  - Layouts are dense row-major (C-contiguous) with the shapes given per argument.
+ *    R = requests, gamma = proposed positions per request, V = vocabulary, rank = Markov rank.
+ *  - Logits and Markov weights are SPEC_F32 or SPEC_BF16. W1 is the Markov embedding [V, rank]
+ *    (row x is the low-rank code of previous token x); W2 is the Markov projection stored
+ *    [V, rank] (row v holds the rank weights that project onto token v, the weight layout of a
+ *    bias-free linear layer rank -> V).
+ *  - Temperature: one T scales draft and target logits alike, after the Markov bias is added;
+ *    the kernels multiply by the fp32 number 1.0f/T.
+ *  - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and the call returns without synchronising. No call does host I/O on the data.
+ *  - Scratch lives in the caller's workspace `ws` of `ws_bytes` bytes (device memory, 256-byte
+ *    aligned), sized by spec_workspace_bytes(). Initialise a workspace once with
+ *    spec_workspace_init() before its first use. Calls that share a workspace must not run
+ *    concurrently on different streams.
+ *  - Every entry point returns a spec_status. Arguments are validated on the host before any
+ *    launch; a failed validation launches nothing. SPEC_ERR_CUDA reports a launch error.
+ *  - Faults found on the device (a token id outside [0, V), a non-finite normaliser, a rejection
+ *    whose residual mass is zero) never trap: the kernels set bits in a status word inside the
+ *    workspace, read with spec_device_status(). Outputs of an affected request are still
+ *    written with valid token ids.
+ *
+ * Indexing (anchor-first window): x_0 is the anchor (the previous round's bonus token). Draft
+ * position k in [1, gamma] reads base-logit row U[r, k-1, :] and the Markov bias
+ * W1[x_{k-1}] . W2. Target row i in [0, gamma] scores the token that follows window position i,
+ * so x_k is checked against target row k-1 and row l is the bonus row when l tokens survive.
+ */
+#ifndef SPEC_MARKOV_H
+#define SPEC_MARKOV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SPEC_ABI_VERSION 1
+
+/* status codes */
+#define SPEC_OK 0
+#define SPEC_ERR_INVALID_ARG (-1)        /* null pointer, bad size, bad length, misalignment */
+#define SPEC_ERR_UNSUPPORTED_DTYPE (-2)  /* dtype code outside {SPEC_F32, SPEC_BF16} */
+#define SPEC_ERR_WORKSPACE_TOO_SMALL (-3)
+#define SPEC_ERR_CUDA (-4)               /* a CUDA runtime call or launch failed */
+#define SPEC_ERR_UNSUPPORTED (-6)        /* a combination this build does not implement */
+
+/* dtype codes */
+#define SPEC_F32 0
+#define SPEC_BF16 1
+
+/* op codes for spec_workspace_bytes */
+#define SPEC_OP_PROPOSE 0
+#define SPEC_OP_VERIFY_GREEDY 1
+#define SPEC_OP_VERIFY_REJECTION 2
+#define SPEC_OP_TV_CONFIDENCE 3
+#define SPEC_OP_SCHEDULE 4
+#define SPEC_OP_TARGET_STATS 5
+#define SPEC_OP_ALL 6 /* a workspace large enough for every op at this size */
+
+/* device status bits (spec_device_status) */
+#define SPEC_DEV_BAD_TOKEN 0x1u      /* an anchor or draft token outside [0, V) was read */
+#define SPEC_DEV_NONFINITE 0x2u      /* a row's softmax normaliser was NaN or infinite */
+#define SPEC_DEV_EMPTY_RESIDUAL 0x4u /* a rejection met zero residual mass (p_t == p_d) */
+#define SPEC_DEV_BAD_LENGTH 0x8u     /* a per-request length outside [0, gamma] */
+
+/* Largest R * gamma the prefix scheduler accepts (its sort runs in one CTA's shared memory). */
+#define SPEC_SCHEDULE_MAX_CANDIDATES 16384
+
+/*
+ * Workspace size in bytes for `op` at this problem size (SPEC_OP_ALL covers every op). The
+ * workspace is device memory owned by the caller, at least 256-byte aligned.
+ */
+size_t spec_workspace_bytes(int op, int R, int gamma, int V, int rank);
+
+/* Zero the workspace header (the device status word) on `stream`. Call once per workspace. */
+int spec_workspace_init(void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Copy the device status word of `ws` into *status_host (synchronises `stream`); if `clear`
+ * is non-zero the word is then reset to 0. Bits are the SPEC_DEV_* values.
+ */
+int spec_device_status(void* ws, size_t ws_bytes, void* stream, uint32_t* status_host,
+                       int clear);
+
+/* Static description of a status code. */
+const char* spec_status_string(int status);
+
+/* SPEC_ABI_VERSION of the loaded library. */
+int spec_abi_version(void);
+
+/*
+ * Draft proposal over the vocabulary.
+ * Defines: "[DeepSeek-6] DSpark", section 3 (semi-autoregressive head: per position,
+ *   p_k(v) = softmax_v(U_k(v) + B_k(v)), sampled left to right) and section 4 "Markov Head"
+ *   (B(x_{k-1}, .) = W1[x_{k-1}] W2, rank 256); with rank == 0 it is the MTP/NextN greedy
+ *   proposal of "Module deepseek_v4_mtp", Forward (draft = argmax(logits)).
+ * For k = 1..gamma (serially): s_k = U[r,k-1,:] + W1[x_{k-1}] . W2^T (x_0 = anchors[r]);
+ *   greedy (u_draft == NULL or temperature == 0): x_k = argmax_v s_k(v), ties to the lowest id;
+ *   sampling: x_k = the smallest v whose cumulative softmax(s_k / T) mass exceeds
+ *   u_draft[r,k-1] (inverse CDF in ascending token order).
+ * Arguments:
+ *   U            [R, gamma, V] draft base logits, dtype u_dtype.
+ *   W1, W2       [V, rank] each, dtype w_dtype (ignored when rank == 0).
+ *   rank         0 (no Markov head) or the Markov rank (1..1024).
+ *   anchors      [R] int32 x_0 (may be NULL when rank == 0).
+ *   u_draft      [R, gamma] fp32 uniforms in [0, 1), or NULL for greedy.
+ *   temperature  > 0 for sampling, 0 for greedy.
+ *   draft_tokens [R, gamma] int32 output.
+ *   draft_logp   [R, gamma] fp32 output log p_d(x_k) (optional, NULL to skip).
+ *   draft_stats  [R, gamma, 2] fp32 output (m, log Z) of softmax(s_k / T), with
+ *                p_d(v) = exp(s_k(v)/T - m - log Z); T = 1 when greedy (optional).
+ * fp32 weights use the canonical fp32 chain acc = fmaf(W1[x][i], W2[v][i], acc), i ascending,
+ * then s = U + acc in fp32, so greedy ids are reproducible bit for bit. bf16 weights with bf16
+ * logits, V % 8 == 0 and rank a multiple of 64 up to 256 run on the tcgen05 tensor cores.
+ */
+int spec_markov_propose(const void* U, int u_dtype, const void* W1, const void* W2, int w_dtype,
+                        int rank, const int32_t* anchors, const float* u_draft,
+                        float temperature, int R, int gamma, int V, int32_t* draft_tokens,
+                        float* draft_logp, float* draft_stats, void* ws, size_t ws_bytes,
+                        void* stream);
+
+/*
+ * Greedy verification with a bonus token.
+ * Defines: "DeepSeek-V4 MTP/NextN 怎样逐步生成候选", sections 三-四 (verify window
+ *   [bonus, d1..d_gamma]; all accepted -> gamma drafts + one new bonus; first mismatch -> one
+ *   target token) and "[DeepSeek-6] DSpark", section 1 (accept the longest legal prefix, then
+ *   emit one bonus token).
+ * With y_i = argmax target[r,i,:] (ties to the lowest id) and l = lengths[r] (gamma if NULL):
+ *   n = the largest i <= l with x_j == y_{j-1} for all j <= i; bonus = y_n.
+ * Arguments:
+ *   target       [R, gamma+1, V] target logits, dtype t_dtype.
+ *   draft_tokens [R, gamma] int32.
+ *   lengths      [R] int32 in [0, gamma], or NULL.
+ *   accept_len   [R] int32 output n.
+ *   out_tokens   [R, gamma+1] int32 output x_1..x_n, bonus, then -1 padding (optional).
+ *   next_anchor  [R] int32 output bonus (optional).
+ */
+int spec_verify_greedy(const void* target, int t_dtype, const int32_t* draft_tokens,
+                       const int32_t* lengths, int R, int gamma, int V, int32_t* accept_len,
+                       int32_t* out_tokens, int32_t* next_anchor, void* ws, size_t ws_bytes,
+                       void* stream);
+
+/*
+ * Softmax normalisers of target rows: stats[row] = (m, log Z) of softmax(target[row,:] / T).
+ * Defines: "[DeepSeek-6] DSpark", section 3 (the exact per-token probabilities that
+ *   rejection sampling needs) -- the p_t half of every probability used below.
+ * Arguments: target [rows, V] (rows = R * (gamma+1) for a verify window), stats [rows, 2] fp32.
+ */
+int spec_target_stats(const void* target, int t_dtype, float temperature, int rows, int V,
+                      float* stats, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Lossless rejection-sampling verification with a residual resample or a bonus token.
+ * Defines: named in "[DeepSeek-6] DSpark", sections 3 and 9 (exact draft probabilities make
+ *   rejection sampling lossless; acceptance is governed by p_d versus p_t); the rule itself is
+ *   standard speculative sampling: for k = 1..l accept x_k iff
+ *   u_accept[r,k-1] * p_d,k(x_k) < p_t,k-1(x_k) (i.e. with probability min(1, p_t/p_d));
+ *   at the first rejection k = n+1 the output token is the inverse-CDF draw with u_resid[r]
+ *   from norm(max(0, p_t,n - p_d,n+1)); if all l survive it is drawn from p_t,l.
+ * Arguments:
+ *   target       [R, gamma+1, V] and U [R, gamma, V], both dtype l_dtype.
+ *   W1, W2, rank, anchors: as spec_markov_propose (they rebuild p_d for the residual).
+ *   draft_tokens [R, gamma] int32 from spec_markov_propose.
+ *   draft_logp   [R, gamma] and draft_stats [R, gamma, 2] from the same propose call, at the
+ *                same temperature.
+ *   target_stats [R*(gamma+1), 2] from spec_target_stats at this temperature, or NULL to have
+ *                them computed here.
+ *   u_accept     [R, gamma] and u_resid [R] fp32 uniforms in [0, 1).
+ *   temperature  > 0.
+ *   lengths      [R] int32 in [0, gamma] (tokens to verify per request), or NULL for gamma.
+ *   accept_len, out_tokens, next_anchor: as spec_verify_greedy (the output token replaces the
+ *                greedy bonus).
+ */
+int spec_verify_rejection(const void* target, const void* U, int l_dtype, const void* W1,
+                          const void* W2, int w_dtype, int rank, const int32_t* anchors,
+                          const int32_t* draft_tokens, const float* draft_logp,
+                          const float* draft_stats, const float* target_stats,
+                          const float* u_accept, const float* u_resid, float temperature,
+                          const int32_t* lengths, int R, int gamma, int V, int32_t* accept_len,
+                          int32_t* out_tokens, int32_t* next_anchor, void* ws, size_t ws_bytes,
+                          void* stream);
+
+/*
+ * TV soft labels and prefix survival.
+ * Defines: "[DeepSeek-6] DSpark", section 5 (c*_k = 1 - 1/2 ||p_d,k - p_t,k||_1 over the
+ *   softmaxed draft and aligned target logits) and section 6 (a_{r,j} = prod_{i<=j} c_{r,i}).
+ * c*_{r,k} is evaluated as sum_v min(p_d,k(v), p_t,k-1(v)) (equal in exact arithmetic), with
+ * p_d,k conditioned on the proposed prefix; a_{r,j} is the sequential fp32 product over j.
+ * Arguments:
+ *   U [R, gamma, V], target [R, gamma+1, V] (dtype l_dtype); W1, W2, rank, anchors as propose.
+ *   draft_tokens [R, gamma]; draft_stats [R, gamma, 2] from propose at this temperature, or
+ *   NULL to recompute them; target_stats as spec_verify_rejection (or NULL).
+ *   conf [R, gamma] and survival [R, gamma] fp32 outputs (survival optional).
+ */
+int spec_tv_confidence(const void* U, const void* target, int l_dtype, const void* W1,
+                       const void* W2, int w_dtype, int rank, const int32_t* anchors,
+                       const int32_t* draft_tokens, const float* draft_stats,
+                       const float* target_stats, float temperature, int R, int gamma, int V,
+                       float* conf, float* survival, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Hardware-aware prefix scheduler.
+ * Defines: "[DeepSeek-6] DSpark", section 6: maximise Theta = tau * SPS(B) with
+ *   B = sum_r (1 + l_r) and tau = sum_r (1 + sum_{j<=l_r} a_{r,j}), queueing every candidate
+ *   (r, j) by a_{r,j} in decreasing order (prefix-closed because a is non-increasing in j).
+ * Candidates are ordered by (a desc, r asc, j asc); tau is carried in fixed point
+ * q = round-half-even(a * 2^32) so that the prefix sums are exact integers; for
+ * K = 0..min(R*gamma, Bmax-R): Theta(K) = double(R * 2^32 + S_K) * sps[R+K]; K* is the smallest
+ * K reaching the maximum and l_r counts the selected candidates of request r. The result is
+ * bit-identical to any implementation of the same definition.
+ * Arguments:
+ *   survival [R, gamma] fp32 in [0, 1], non-increasing in j.
+ *   sps      [Bmax+1] fp64 steps per second at batch size B (index B), finite and >= 0.
+ *   lengths  [R] int32 output; B_out [1] int32 output; theta_out [1] fp64 output
+ *            (tau * SPS(B) in natural units). All three are device pointers.
+ * Requires R * gamma <= SPEC_SCHEDULE_MAX_CANDIDATES and Bmax >= R.
+ */
+int spec_schedule_prefix(const float* survival, const double* sps, int Bmax, int R, int gamma,
+                         int32_t* lengths, int32_t* B_out, double* theta_out, void* ws,
+                         size_t ws_bytes, void* stream);
+
+/*
+ * Tracing (no counterpart on the pages; instrumentation of this library).
+ * Kernel classes: SPEC_KCLASS_MARKOV (the Markov producer: tensor-core GEMM fused with the
+ * softmax / residual / TV epilogue, or its CUDA-core form), SPEC_KCLASS_STREAM (rank-0 streaming
+ * row reductions), SPEC_KCLASS_SELECT (per-row select / sample), SPEC_KCLASS_OTHER (scans,
+ * finalisers, the scheduler).
+ */
+#define SPEC_KCLASS_MARKOV 0
+#define SPEC_KCLASS_STREAM 1
+#define SPEC_KCLASS_SELECT 2
+#define SPEC_KCLASS_OTHER 3
+#define SPEC_KCLASS_COUNT 4
+
+/* Number of kernels this process has launched through the library (all classes). */
+unsigned long long spec_launch_count(void);
+
+/*
+ * Attach caller-created CUDA events (cudaEvent_t handles created with timing enabled) to one
+ * kernel class: the i-th launch of that class after this call records begin_events[i] before
+ * and end_events[i] after itself on the launch stream, for i < capacity. Pass capacity 0 to
+ * detach. The events stay owned by the caller. Process-global state; not thread-safe.
+ */
+int spec_trace_events(int kclass, void* const* begin_events, void* const* end_events,
+                      int capacity);
+
+/* Launches of `kclass` recorded into the attached events since spec_trace_events. */
+int spec_trace_count(int kclass);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_MARKOV_H */
