@@ -1,0 +1,425 @@
+#!/usr/bin/env python
+"""Benchmark of the speculative-decoding hot path on GB300.
+
+Workload (N=1): DSpark Markov sampling + lossless rejection verification, R=256 requests,
+gamma=7 proposed positions, V=129280, Markov rank 256, bf16 logits and weights, T=1.
+One step = the whole hot path over one batch: gamma serial Markov proposal positions
+(tensor-core bias GEMM fused with softmax partials, then inverse-CDF sampling), the target
+softmax normalisers, the acceptance scan, and the residual / bonus draw.
+
+Metric: draft + verify logit rows per second, rows = R*gamma + R*(gamma+1) = 3840 per step.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (plain C, fp64) on a bounded sample of the same workload.
+For N > 1 (torchrun, one rank per GPU) every rank runs its own replica (weak scaling, no
+collective on the data path); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "draft+verify logit rows/s at V=129280, R=256 (HBM GB/s, % of peak)"
+UNIT = "rows/s"
+WORKLOAD = dict(R=256, gamma=7, V=129280, rank=256, temperature=1.0, seed=1003)
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--e2e-steps", type=int, default=20)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def config_dict(extra=None):
+    c = {"workload": "markov_rejection: Markov-head sampling + rejection verify, R=256 gamma=7 "
+                     "V=129280 rank=256 bf16 T=1",
+         "R": WORKLOAD["R"], "gamma": WORKLOAD["gamma"], "V": WORKLOAD["V"],
+         "rank": WORKLOAD["rank"], "temperature": WORKLOAD["temperature"],
+         "storage_dtype": "bf16",
+         "rows_per_step": WORKLOAD["R"] * (2 * WORKLOAD["gamma"] + 1),
+         "l2": "inputs larger than L2 (1.06 GB of logits per step vs 129 MB L2)"}
+    if extra:
+        c.update(extra)
+    return c
+
+
+def algorithmic_bytes_per_step():
+    """What one step must touch: U and the target read once, W2 read once, W1 row gathers."""
+    R, g, V, r = (WORKLOAD[k] for k in ("R", "gamma", "V", "rank"))
+    return 2 * (R * g * V + R * (g + 1) * V + V * r + R * g * r)
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50", "-i", str(self.index)], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 6:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0, t1):
+        win = [p for t, p in self.samples if t0 - 0.05 <= t <= t1 + 0.05]
+        if not win and self.samples:
+            mid = (t0 + t1) / 2
+            win = [min(self.samples, key=lambda s: abs(s[0] - mid))[1]]
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[0]) for p in win if num(p[0]) is not None]
+        mx = [num(p[1]) for p in win if num(p[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in win for i in range(4) if p[2 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(win)}
+
+
+# ----------------------------------------------------------------------------- profile traffic
+
+def recorded_traffic(kernel_class):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu summary
+    (profiles/traffic.json), or None if absent or taken on a different kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        rec = json.load(open(path)).get(kernel_class)
+    except (OSError, ValueError):
+        return None
+    if not rec:
+        return None
+    src = os.path.join(ROOT, rec.get("source", ""))
+    if not os.path.exists(src):
+        return None
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    if h != rec.get("source_sha256_16"):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------------------- CPU baseline
+
+def cpu_baseline_run(wl_host, n_req):
+    """Time the oracle (propose + rejection verify) on the first n_req requests."""
+    import oracle
+    sl = lambda t: None if t is None else t[:n_req]
+    t0 = time.perf_counter()
+    ref = oracle.markov_propose(sl(wl_host["U"]), wl_host["W1"], wl_host["W2"],
+                                sl(wl_host["anchors"]), sl(wl_host["u_draft"]),
+                                WORKLOAD["temperature"])
+    oracle.verify_rejection(sl(wl_host["target"]), sl(wl_host["U"]), wl_host["W1"],
+                            wl_host["W2"], sl(wl_host["anchors"]), ref["tokens"],
+                            sl(wl_host["u_accept"]), sl(wl_host["u_resid"]),
+                            WORKLOAD["temperature"])
+    dt = time.perf_counter() - t0
+    rows = n_req * (2 * WORKLOAD["gamma"] + 1)
+    return rows / dt, dt
+
+
+def host_sample(n_req, device):
+    """The first n_req requests of the workload, drawn on `device`, copied to host."""
+    from draft_sampling_verification_markov_gb300 import workloads
+    wl = workloads.markov_rejection(device, R=WORKLOAD["R"], gamma=WORKLOAD["gamma"],
+                                    V=WORKLOAD["V"], rank=WORKLOAD["rank"], seed=WORKLOAD["seed"],
+                                    temperature=WORKLOAD["temperature"])
+    out = {}
+    for k, v in wl.tensors().items():
+        out[k] = v[:n_req].cpu() if k not in ("W1", "W2") else v.cpu()
+    del wl
+    return out
+
+
+def run_reference(args):
+    """--impl reference: the CPU oracle, timed on the host cores, on a bounded sample."""
+    rank, world, local = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    threads = oracle.num_threads()
+    n_req = max(1, min(WORKLOAD["R"], threads))
+    wl = host_sample(n_req, "cpu")
+    for _ in range(args.warmup):
+        cpu_baseline_run(wl, n_req)
+    times = []
+    for _ in range(args.steps):
+        times.append(cpu_baseline_run(wl, n_req)[1])
+    total = sum(times)
+    rows = n_req * (2 * WORKLOAD["gamma"] + 1) * args.steps
+    value = rows / total
+    sample = (f"{n_req} of {WORKLOAD['R']} requests per step (all {WORKLOAD['gamma']} positions, "
+              f"full V), CPU-drawn inputs of the same shapes and distributions")
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": config_dict({"sample_requests_per_step": n_req}),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": min(threads, n_req),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    import torch
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from draft_sampling_verification_markov_gb300 import spec, workloads
+
+    W = WORKLOAD
+    wl = workloads.markov_rejection("cuda", R=W["R"], gamma=W["gamma"], V=W["V"], rank=W["rank"],
+                                    seed=W["seed"] + 100 * rank, temperature=W["temperature"])
+    R, g, V = W["R"], W["gamma"], W["V"]
+    T = W["temperature"]
+    stream = torch.cuda.Stream(device=dev)
+    ws = spec.Workspace(device=dev)
+    for op in range(6):
+        ws.for_op(op, R, g, V, W["rank"], stream)
+    toks = torch.empty(R, g, dtype=torch.int32, device=dev)
+    logp = torch.empty(R, g, dtype=torch.float32, device=dev)
+    dstats = torch.empty(R, g, 2, dtype=torch.float32, device=dev)
+    tstats = torch.empty(R * (g + 1), 2, dtype=torch.float32, device=dev)
+    n_acc = torch.empty(R, dtype=torch.int32, device=dev)
+    out = torch.empty(R, g + 1, dtype=torch.int32, device=dev)
+    nxt = torch.empty(R, dtype=torch.int32, device=dev)
+
+    def step(U, target, anchors, u_draft, u_acc, u_res):
+        spec.spec_markov_propose(U, wl.W1, wl.W2, anchors, u_draft, T, draft_tokens=toks,
+                                 draft_logp=logp, draft_stats=dstats, workspace=ws, stream=stream)
+        spec.spec_target_stats(target, T, stats=tstats, workspace=ws, stream=stream)
+        spec.spec_verify_rejection(target, U, wl.W1, wl.W2, anchors, toks, logp, dstats, u_acc,
+                                   u_res, T, target_stats=tstats, accept_len=n_acc,
+                                   out_tokens=out, next_anchor=nxt, workspace=ws, stream=stream)
+
+    inputs = (wl.U, wl.target, wl.anchors, wl.u_draft, wl.u_accept, wl.u_resid)
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            step(*inputs)
+    torch.cuda.synchronize()
+    assert ws.status() == 0, "device status word set during warm-up"
+
+    # live per-class kernel timing over the timed region (caller-owned events on `stream`)
+    # launches per step and class: Markov producer g+1, streaming rows 1, select g+1, other 2
+    caps = {0: (g + 1) * args.steps, 1: args.steps, 2: (g + 1) * args.steps, 3: 2 * args.steps}
+    ev = {}
+    for kc in range(4):
+        cap = caps[kc]
+        b = [torch.cuda.Event(enable_timing=True) for _ in range(cap)]
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(cap)]
+        for x in b + e:
+            x.record(stream)                      # materialise the CUDA event handles
+        ev[kc] = (b, e)
+    torch.cuda.synchronize()
+    import ctypes
+    keep = []
+    for kc, (b, e) in ev.items():
+        cap = caps[kc]
+        bh = (ctypes.c_void_p * cap)(*[x.cuda_event for x in b])
+        eh = (ctypes.c_void_p * cap)(*[x.cuda_event for x in e])
+        keep.append((bh, eh))
+        assert spec.lib().spec_trace_events(kc, bh, eh, cap) == 0
+    launches0 = spec.lib().spec_launch_count()
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    w0 = time.time()
+    t_start.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(args.steps):
+            step(*inputs)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    w1 = time.time()
+    if pg:
+        pg.barrier()
+    time.sleep(0.15)
+    sampler.stop()
+    launches = spec.lib().spec_launch_count() - launches0
+    counts = {kc: spec.lib().spec_trace_count(kc) for kc in range(4)}
+    for kc in range(4):
+        spec.lib().spec_trace_events(kc, None, None, 0)
+    ms = t_start.elapsed_time(t_end)
+    if pg:
+        t = torch.tensor([ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms = float(t.item())
+    assert ws.status() == 0, "device status word set during the timed region"
+    rows_per_step = R * (2 * g + 1)
+    value = rows_per_step * args.steps * world / (ms / 1e3)
+
+    # dominant kernel class by total device time over the timed region
+    totals = {}
+    for kc in range(4):
+        b, e = ev[kc]
+        d = [b[i].elapsed_time(e[i]) for i in range(counts[kc])]
+        totals[kc] = (sum(d), len(d))
+    dom = max(totals, key=lambda k: totals[k][0])
+    names = {0: "markov_producer", 1: "stream_rows", 2: "select", 3: "other"}
+    per_unit = algorithmic_bytes_per_step() / rows_per_step
+    units_per_launch = {0: R, 1: R * (g + 1), 2: R, 3: R}
+    dur_s = totals[dom][0] / max(totals[dom][1], 1) / 1e3
+    achieved = per_unit * units_per_launch[dom] / dur_s / 1e9
+    peaks = {}
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+        peak, peak_src = float(peaks["hbm_gbs"]), "measured"
+    except (OSError, ValueError, KeyError):
+        peak, peak_src = 6800.0, "fallback"
+    traffic = recorded_traffic(names[dom])
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": traffic, "kernel": names[dom],
+                "peak_source": peak_src,
+                "launch_ms": 1e3 * dur_s,
+                "step_hbm_frac": algorithmic_bytes_per_step() * args.steps / (ms / 1e3) / 1e9 / peak,
+                "class_ms_per_step": {names[k]: totals[k][0] / args.steps for k in totals}}
+
+    # end to end through the C ABI from pinned host buffers (weights stay resident)
+    e2e = None
+    if args.e2e_steps > 0:
+        host = [x.cpu().pin_memory() for x in inputs]
+        dbuf = [torch.empty_like(x) for x in inputs]
+        h_out = torch.empty(R, g + 1, dtype=torch.int32).pin_memory()
+        h_n = torch.empty(R, dtype=torch.int32).pin_memory()
+        h2d = sum(x.numel() * x.element_size() for x in host)
+        d2h = h_out.numel() * 4 + h_n.numel() * 4
+
+        def e2e_step():
+            for d, h in zip(dbuf, host):
+                d.copy_(h, non_blocking=True)
+            step(*dbuf)
+            h_out.copy_(out, non_blocking=True)
+            h_n.copy_(n_acc, non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                e2e_step()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if pg:
+            pg.barrier()
+        a.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(args.e2e_steps):
+                e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        e_ms = a.elapsed_time(b)
+        if pg:
+            t = torch.tensor([e_ms], device=dev)
+            pg.all_reduce(t, op=pg.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": rows_per_step * args.e2e_steps * world / (e_ms / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e_ms / args.e2e_steps}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        threads = oracle.num_threads()
+        n_req = max(1, min(R, 2 * threads))
+        wl_h = {k: (v[:n_req].cpu() if k not in ("W1", "W2") else v.cpu())
+                for k, v in wl.tensors().items()}
+        v_cpu, dt = cpu_baseline_run(wl_h, n_req)
+        cpu = {"value": v_cpu, "unit": UNIT, "cores": min(threads, n_req), "kind": "oracle",
+               "sample": f"{n_req} of {R} requests (all {g} positions, full V) of the same "
+                         f"seeded bytes, {dt:.1f} s"}
+
+    clocks = sampler.summary(w0, w1)
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f32", "data": "synthetic",
+                "config": config_dict({"parallelism": f"replicas x{world}"}),
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": int(launches), "clocks": clocks,
+                "tokens_per_s": float(n_acc.sum().item() + R) * args.steps * world / (ms / 1e3)}
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

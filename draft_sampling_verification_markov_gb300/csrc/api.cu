@@ -63,7 +63,7 @@ constexpr size_t kHeader = 256;
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 int cdiv(long long a, long long b) { return (int)((a + b - 1) / b); }
 
-int markov_nseg(int V) { return cdiv(V, kMarkovSeg); }
+int markov_nseg(int V) { return cdiv(V, kMarkovMinSeg); }
 int stream_nseg(int V) { return cdiv(V, kStreamSeg); }
 
 struct Layout {
@@ -163,14 +163,19 @@ int grid_for(long long units, int per_block) {
 }
 
 // Rows of a Markov (rank > 0) pass: tcgen05 producer when the shape allows, else CUDA cores.
-int markov_pass(const RowJob& j, int udt, int wdt, const Ws& w, bool argmax, cudaStream_t s) {
+// Reports the segment width of the partials it wrote.
+int markov_pass(const RowJob& j, int udt, int wdt, const Ws& w, bool argmax, cudaStream_t s,
+                int* seg, int* nseg) {
   if (markov_tc_supported(udt, wdt, j.rank, j.V, j.U, j.T, j.W1, j.W2)) {
+    *seg = markov_tc_seg(j.mode);
+    *nseg = cdiv(j.V, *seg);
     if (launch_markov_tc(j, w.pm, w.ps, w.pi, argmax, s) != cudaSuccess) return SPEC_ERR_CUDA;
     return SPEC_OK;
   }
-  const int nseg = markov_nseg(j.V);
-  launch_ffma_partials(j, udt, wdt, nseg, argmax, w.pm, w.ps, w.pi,
-                       grid_for((long long)j.rows * nseg, 8), s);
+  *seg = kMarkovSeg;
+  *nseg = cdiv(j.V, kMarkovSeg);
+  launch_ffma_partials(j, udt, wdt, *nseg, argmax, w.pm, w.ps, w.pi,
+                       grid_for((long long)j.rows * *nseg, 8), s);
   return SPEC_OK;
 }
 
@@ -320,9 +325,7 @@ int spec_markov_propose(const void* U, int u_dtype, const void* W1, const void* 
       launch_stream_partials(j, u_dtype, seg, nseg, vec, true, greedy, w.pm, w.ps, w.pi,
                              grid_for((long long)R * nseg, 1), s);
     } else {
-      seg = kMarkovSeg;
-      nseg = markov_nseg(V);
-      rc = markov_pass(j, u_dtype, wdt, w, greedy, s);
+      rc = markov_pass(j, u_dtype, wdt, w, greedy, s, &seg, &nseg);
       if (rc != SPEC_OK) return rc;
     }
     launch_select(j, u_dtype, wdt, seg, nseg, w.pm, w.ps, greedy ? w.pi : nullptr, o, s);
@@ -442,9 +445,7 @@ int spec_verify_rejection(const void* target, const void* U, int l_dtype, const 
     launch_stream_partials(j, l_dtype, seg, nseg, vec_ok(target, U, l_dtype, V), true, false,
                            w.pm, w.ps, w.pi, grid_for((long long)R * nseg, 1), s);
   } else {
-    seg = kMarkovSeg;
-    nseg = markov_nseg(V);
-    rc = markov_pass(j, l_dtype, wdt, w, false, s);
+    rc = markov_pass(j, l_dtype, wdt, w, false, s, &seg, &nseg);
     if (rc != SPEC_OK) return rc;
   }
   SelectOut o;
@@ -510,8 +511,8 @@ int spec_tv_confidence(const void* U, const void* target, int l_dtype, const voi
       launch_stream_partials(j, l_dtype, kStreamSeg, nseg, vec, true, false, w.pm, w.ps, w.pi,
                              grid_for((long long)j.rows * nseg, 1), s);
     } else {
-      nseg = markov_nseg(V);
-      rc = markov_pass(j, l_dtype, wdt, w, false, s);
+      int seg;
+      rc = markov_pass(j, l_dtype, wdt, w, false, s, &seg, &nseg);
       if (rc != SPEC_OK) return rc;
     }
     launch_finalize_stats(j.rows, nseg, w.pm, w.ps, w.dstats, nullptr, 1, w.status, s);
@@ -525,8 +526,8 @@ int spec_tv_confidence(const void* U, const void* target, int l_dtype, const voi
     launch_stream_partials(j, l_dtype, kStreamSeg, nseg, vec, true, false, w.pm, w.ps, w.pi,
                            grid_for((long long)j.rows * nseg, 1), s);
   } else {
-    nseg = markov_nseg(V);
-    rc = markov_pass(j, l_dtype, wdt, w, false, s);
+    int seg;
+    rc = markov_pass(j, l_dtype, wdt, w, false, s, &seg, &nseg);
     if (rc != SPEC_OK) return rc;
   }
   launch_tv_finalize(R, gamma, nseg, w.ps, conf, survival, s);

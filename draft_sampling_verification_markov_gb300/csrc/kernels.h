@@ -57,6 +57,10 @@ bool markov_tc_supported(int udt, int wdt, int rank, int V, const void* U, const
                          const void* W1, const void* W2);
 cudaError_t launch_markov_tc(const RowJob& j, float* pm, float* ps, int* pi, bool argmax,
                              cudaStream_t s);
+// Vocabulary columns per partial written by the tcgen05 producer in pass mode `mode`.
+int markov_tc_seg(int mode);
+// Smallest partial segment any Markov producer writes (sizes the workspace).
+constexpr int kMarkovMinSeg = 32;
 
 int num_sms();
 

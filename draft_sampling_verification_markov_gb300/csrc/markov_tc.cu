@@ -1,14 +1,751 @@
-// markov_tc.cu -- tcgen05 Markov producer (placeholder until the tensor-core kernel lands).
+// markov_tc.cu -- tcgen05 Markov producer: the rank-r bias GEMM W1[x_{k-1}] . W2^T on the
+// 5th-generation tensor cores, fused with the per-row epilogue of each pass ("[DeepSeek-6]
+// DSpark", section 4 "Markov Head": B(x_{k-1}, .) = W1[x_{k-1}] W2 added to the base logits,
+// section 3 softmax; section 5 TV label; the residual of rejection sampling).
+//
+// One tile = 128 rows (requests, TMEM lanes) x BN vocabulary columns, K = rank (<= 256).
+//   A  [128 x rank] bf16: the W1 rows of each row's previous token, gathered by the epilogue
+//      warps into shared memory in the 128-byte-swizzled K-major layout (once per row block).
+//   B  [BN x rank] bf16: W2 rows (W2 stored [V, rank], K-major) by TMA, kept in L2 with an
+//      evict-last policy (every row block and every draft position reads all of W2).
+//   D  [128 x BN] fp32 in tensor memory, two stages, read back with tcgen05.ld by the epilogue.
+//   U / T tiles: the base-logit (and target) rows of the same 128 rows x BN columns, by TMA
+//      with an evict-first policy (read once), or by per-row bulk copies when the rows of a
+//      tile are not equally spaced (the final rows of rejection verification).
+// Warp roles (320 threads, one CTA per SM, persistent over a contiguous range of tiles):
+//   warp 0      TMA producer;   warp 1  TMEM allocator + single-thread MMA issuer;
+//   warps 2..9  epilogue: warp w reads TMEM lanes 32*(w%4).. and column half (w-2)/4.
+// Epilogues (per row, per 64-column segment):
+//   MODE_STATS  z = (U + bias) * scale -> (max z, sum exp(z - max), first argmax);
+//   MODE_TV     sum min(p_d, p_t);    MODE_RESID  sum max(0, p_t - p_d) (p_t on bonus rows);
+//   these two write one partial per row and 32-column half (markov_tc_seg).
+// Every mbarrier wait is bounded (about a second); on expiry the CTA sets SPEC_DEV_TIMEOUT,
+// drains its own copies and MMAs, frees its tensor memory and returns.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
 #include "kernels.h"
 
 namespace spec {
+namespace tc {
 
-bool markov_tc_supported(int, int, int, int, const void*, const void*, const void*, const void*) {
-  return false;
+constexpr int kBM = 128;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = (2 + kEpiWarps) * 32;
+constexpr long long kSpinCycles = 4000000000LL;  // ~2 s at the maximum SM clock
+constexpr uint32_t kAtomBytes = kBM * 128;       // 128 rows x 128 B (64 bf16 of K)
+
+// BN = 128 (softmax partials, U only): A 64 KB + B 6 x 16 KB + U 2 x 32 KB = 224 KB.
+// BN = 64 (TV / residual, U and T): A 64 KB + B 6 x 8 KB + (U + T) 3 x 2 x 18 KB = 220 KB.
+template <int BN>
+struct Cfg {
+  static constexpr int kBStages = 6;
+  static constexpr int kUStages = BN == 128 ? 2 : 3;
+  static constexpr uint32_t kBStageBytes = BN * 128;
+  static constexpr uint32_t kRowPitch = BN * 2 + 16;  // gathered rows (pair modes only)
+  static constexpr uint32_t kTileBytes = BN == 128 ? kBM * BN * 2 : kBM * kRowPitch;
+};
+
+// ------------------------------------------------------------------------------ PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-cudaError_t launch_markov_tc(const RowJob&, float*, float*, int*, bool, cudaStream_t) {
-  return cudaErrorNotSupported;
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for the phase of `parity` to complete. Returns false if the CTA aborted or the
+// wait expired (then the abort flag and SPEC_DEV_TIMEOUT are set).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          uint32_t* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (clock64() - t0 > kSpinCycles) {
+      *abort = 1;
+      atomicOr(status, SPEC_DEV_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// Bounded wait that ignores the abort flag (used to drain copies already in flight).
+__device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity) && clock64() - t0 < kSpinCycles) {
+  }
+}
+
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1,
+                                            uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1,
+                                            int c2, uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)),
+      "l"(policy)
+      : "memory");
+}
+
+// Untiled bulk copy global -> shared (both 16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                          uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void fence_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) |
+         ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Instruction descriptor, kind::f16: bf16 A and B (both K-major), fp32 accumulate, M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+// 8 bf16 of a 16-byte word, unpacked to fp32 and added to x[0..7].
+__device__ __forceinline__ void add_bf16x8(uint4 w, float* x) {
+  const uint32_t a[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    x[2 * i] += __uint_as_float(a[i] << 16);
+    x[2 * i + 1] += __uint_as_float(a[i] & 0xffff0000u);
+  }
+}
+
+__device__ __forceinline__ void unpack_bf16x8(uint4 w, float* x) {
+  const uint32_t a[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    x[2 * i] = __uint_as_float(a[i] << 16);
+    x[2 * i + 1] = __uint_as_float(a[i] & 0xffff0000u);
+  }
+}
+
+// ------------------------------------------------------------------------------ tiles
+
+struct Tiles {
+  int n_mt, n_nt;  // row blocks and column tiles
+  int rb;          // row blocks per draft position (MAP_ALL_POS)
+};
+
+// Row m of the pass for lane row i of row block mt, and its request / position.
+struct TileRow {
+  int valid;
+  int r;
+  int k;      // draft position (1-based) of this row block (uniform modes)
+  int prow;   // partial row index in the pass
+};
+
+__device__ __forceinline__ TileRow tile_row(const RowJob& j, const Tiles& t, int mt, int i) {
+  TileRow o;
+  if (j.map == MAP_ALL_POS) {
+    o.k = mt / t.rb + 1;
+    o.r = (mt % t.rb) * kBM + i;
+    o.prow = o.r * j.gamma + (o.k - 1);
+  } else {
+    o.k = j.k;
+    o.r = mt * kBM + i;
+    o.prow = o.r;
+  }
+  o.valid = o.r < j.R;
+  return o;
+}
+
+// ------------------------------------------------------------------------------ kernel
+
+struct TcParams {
+  RowJob j;
+  Tiles t;
+  float* pm;
+  float* ps;
+  int* pi;
+};
+
+template <int BN, int MODE, bool ARGMAX, bool GATHER>
+__global__ void __launch_bounds__(kThreads, 1)
+    markov_tc_kernel(const __grid_constant__ CUtensorMap map_w2,
+                     const __grid_constant__ CUtensorMap map_u,
+                     const __grid_constant__ CUtensorMap map_t, const TcParams P) {
+  using C = Cfg<BN>;
+  constexpr int KB = C::kBStages, KU = C::kUStages;
+  constexpr bool kPair = MODE != MODE_STATS;  // needs target tiles
+  constexpr int kHalf = BN / 2;               // columns per epilogue warp
+
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const RowJob& j = P.j;
+  const int ka_n = j.rank / 64;
+  unsigned char* sA = smem;                                         // ka_n atoms
+  unsigned char* sB = sA + 4 * kAtomBytes;                          // KB stages
+  unsigned char* sU = sB + KB * C::kBStageBytes;                    // KU stages
+  unsigned char* sT = sU + KU * C::kTileBytes;                      // KU stages (pair modes)
+  unsigned char* tail = sT + (kPair ? KU * C::kTileBytes : 0);
+  uint64_t* b_full = reinterpret_cast<uint64_t*>(tail);
+  uint64_t* b_empty = b_full + KB;
+  uint64_t* u_full = b_empty + KB;
+  uint64_t* u_empty = u_full + KU;
+  uint64_t* acc_full = u_empty + KU;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* a_full = acc_empty + 2;
+  uint64_t* a_empty = a_full + 1;
+  uint64_t* drain = a_empty + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint32_t* status = j.status;
+
+  // contiguous range of tiles for this CTA
+  const long long total = (long long)P.t.n_mt * P.t.n_nt;
+  const long long t_begin = total * blockIdx.x / gridDim.x;
+  const long long t_end = total * (blockIdx.x + 1) / gridDim.x;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < KB; ++s) {
+      mbar_init(&b_full[s], 1);
+      mbar_init(&b_empty[s], 1);
+    }
+    for (int s = 0; s < KU; ++s) {
+      mbar_init(&u_full[s], 1);
+      mbar_init(&u_empty[s], kEpiWarps);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&acc_full[s], 1);
+      mbar_init(&acc_empty[s], kEpiWarps);
+    }
+    mbar_init(a_full, kEpiWarps);
+    mbar_init(a_empty, 1);
+    mbar_init(drain, 1);
+    *abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(2 * BN < 32 ? 32 : 2 * BN)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    const uint64_t pol_keep = policy_evict_last(), pol_stream = policy_evict_first();
+    int bs = 0, us = 0;
+    uint32_t bph = 0, uph = 0;
+    bool ok = true;
+    for (long long t = t_begin; t < t_end && ok; ++t) {
+      const int mt = (int)(t / P.t.n_nt), nt = (int)(t % P.t.n_nt);
+      const int n0 = nt * BN;
+      for (int ka = 0; ka < ka_n && ok; ++ka) {
+        ok = mbar_wait(&b_empty[bs], bph ^ 1, abort, status);
+        if (ok && lane == 0) {
+          mbar_arrive_expect_tx(&b_full[bs], C::kBStageBytes);
+          tma_load_2d(sB + bs * C::kBStageBytes, &map_w2, ka * 64, n0, &b_full[bs], pol_keep);
+        }
+        if (++bs == KB) { bs = 0; bph ^= 1; }
+      }
+      if (!ok) break;
+      ok = mbar_wait(&u_empty[us], uph ^ 1, abort, status);
+      if (!ok) break;
+      unsigned char* du = sU + us * C::kTileBytes;
+      unsigned char* dt = sT + us * C::kTileBytes;
+      if constexpr (!GATHER) {
+        if (lane == 0) {
+          const TileRow tr = tile_row(j, P.t, mt, 0);
+          const int r0 = tr.r, kk = tr.k - 1;
+          constexpr int nbox = BN / 64;
+          mbar_arrive_expect_tx(&u_full[us], (kPair ? 2u : 1u) * nbox * kAtomBytes);
+          for (int b = 0; b < nbox; ++b) {
+            tma_load_3d(du + b * kAtomBytes, &map_u, n0 + b * 64, kk, r0, &u_full[us], pol_stream);
+            if constexpr (kPair)
+              tma_load_3d(dt + b * kAtomBytes, &map_t, n0 + b * 64, kk, r0, &u_full[us],
+                          pol_stream);
+          }
+        }
+      } else {
+        // final rows of rejection verification: one bulk copy per row (and per tensor)
+        const uint32_t bytes = (uint32_t)min(BN, j.V - n0) * 2u;
+        uint32_t mine = 0;
+        for (int i = lane; i < kBM; i += 32) {
+          const int r = mt * kBM + i;
+          if (r < j.R) mine += j.final_kind[r] ? 2u * bytes : bytes;
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, off);
+        if (lane == 0) mbar_arrive_expect_tx(&u_full[us], mine);
+        __syncwarp();
+        for (int i = lane; i < kBM; i += 32) {
+          const int r = mt * kBM + i;
+          if (r >= j.R) continue;
+          const int n = j.final_n[r];
+          const unsigned short* trow = reinterpret_cast<const unsigned short*>(j.T) +
+                                       ((size_t)r * (j.gamma + 1) + n) * j.V + n0;
+          bulk_load(dt + i * C::kRowPitch, trow, bytes, &u_full[us], pol_stream);
+          if (j.final_kind[r]) {
+            const unsigned short* urow = reinterpret_cast<const unsigned short*>(j.U) +
+                                         ((size_t)r * j.gamma + n) * j.V + n0;
+            bulk_load(du + i * C::kRowPitch, urow, bytes, &u_full[us], pol_stream);
+          }
+        }
+      }
+      if (++us == KU) { us = 0; uph ^= 1; }
+    }
+    // drain: every issued copy lands before the CTA moves on
+    if (lane == 0) {
+      for (int s = 0; s < KB; ++s) mbar_drain(&b_full[s], (s < bs) ? bph : (bph ^ 1));
+      for (int s = 0; s < KU; ++s) mbar_drain(&u_full[s], (s < us) ? uph : (uph ^ 1));
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    constexpr uint32_t idesc = idesc_bf16(kBM, BN);
+    int bs = 0, as = 0;
+    uint32_t bph = 0, aph = 0;
+    uint32_t accph[2] = {0, 0};
+    bool ok = true;
+    int cur_mt = -1;
+    if (lane == 0) {
+      for (long long t = t_begin; t < t_end && ok; ++t) {
+        const int mt = (int)(t / P.t.n_nt);
+        if (mt != cur_mt) {
+          ok = mbar_wait(a_full, aph, abort, status);
+          aph ^= 1;
+          cur_mt = mt;
+          if (!ok) break;
+          tc_fence_after();
+        }
+        ok = mbar_wait(&acc_empty[as], accph[as] ^ 1, abort, status);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t d = tmem + as * BN;
+        for (int ka = 0; ka < ka_n && ok; ++ka) {
+          ok = mbar_wait(&b_full[bs], bph, abort, status);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(sA + ka * kAtomBytes);
+          const uint32_t b_base = smem_u32(sB + bs * C::kBStageBytes);
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            mma_bf16(d, sw128_desc(a_base + ks * 32), sw128_desc(b_base + ks * 32), idesc,
+                     (ka | ks) != 0);
+          mma_commit(&b_empty[bs]);
+          if (++bs == KB) { bs = 0; bph ^= 1; }
+        }
+        if (!ok) break;
+        mma_commit(&acc_full[as]);
+        accph[as] ^= 1;
+        as ^= 1;
+        const bool last_of_block = (t + 1 == t_end) || ((int)((t + 1) / P.t.n_nt) != mt);
+        if (last_of_block) mma_commit(a_empty);
+      }
+      // all MMAs issued by this thread complete before tensor memory is released
+      mma_commit(drain);
+      mbar_drain(drain, 0);
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------------------------------------------- epilogue
+    const int ew = warp - 2;
+    const int q = warp & 3;          // TMEM lane quarter
+    const int h = ew >> 2;           // column half
+    const int i = q * 32 + lane;     // row within the tile
+    const int et = threadIdx.x - 64; // 0..255
+    int as = 0, us = 0;
+    uint32_t accph[2] = {0, 0}, uph = 0, aeph = 0;
+    int cur_mt = -1;
+    bool ok = true;
+    float scale2 = j.scale * kLog2e;
+    (void)scale2;
+    for (long long t = t_begin; t < t_end && ok; ++t) {
+      const int mt = (int)(t / P.t.n_nt), nt = (int)(t % P.t.n_nt);
+      const int n0 = nt * BN;
+      if (mt != cur_mt) {
+        if (cur_mt >= 0) {
+          ok = mbar_wait(a_empty, aeph, abort, status);
+          aeph ^= 1;
+          if (!ok) break;
+        }
+        cur_mt = mt;
+        // gather A: row ii <- W1[prev(ii)] in the swizzled K-major layout
+        const int chunks = ka_n * 8;  // 16-byte chunks per row
+        for (int c = et; c < kBM * chunks; c += kEpiWarps * 32) {
+          const int ii = c / chunks, cc = c % chunks;
+          const int ka = cc >> 3, cw = cc & 7;
+          uint4 v = make_uint4(0, 0, 0, 0);
+          const TileRow tr = tile_row(j, P.t, mt, ii);
+          if (tr.valid) {
+            int prev;
+            if (j.map == MAP_FINAL) {
+              const int n = j.final_n[tr.r];
+              prev = n == 0 ? j.anchors[tr.r] : j.tokens[(size_t)tr.r * j.gamma + n - 1];
+            } else {
+              prev = tr.k == 1 ? j.anchors[tr.r] : j.tokens[(size_t)tr.r * j.gamma + tr.k - 2];
+            }
+            if (prev < 0 || prev >= j.V) {
+              atomicOr(status, SPEC_DEV_BAD_TOKEN);
+              prev = 0;
+            }
+            v = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const unsigned short*>(j.W1) +
+                                                     (size_t)prev * j.rank) +
+                      cc);
+          }
+          *reinterpret_cast<uint4*>(sA + ka * kAtomBytes + ii * 128 + ((cw ^ (ii & 7)) << 4)) = v;
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(a_full);
+      }
+      ok = mbar_wait(&acc_full[as], accph[as], abort, status);
+      if (!ok) break;
+      tc_fence_after();
+      ok = mbar_wait(&u_full[us], uph, abort, status);
+      if (!ok) break;
+
+      const TileRow tr = tile_row(j, P.t, mt, i);
+      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + as * BN + h * kHalf;
+      const uint32_t u_base = smem_u32(sU + us * C::kTileBytes);
+      const uint32_t t_base = smem_u32(sT + us * C::kTileBytes);
+      // address of 16-byte chunk c (8 columns) of this thread's row, tile-relative column
+      auto chunk_addr = [&](uint32_t base, int col) -> uint32_t {
+        if constexpr (GATHER) {
+          return base + i * C::kRowPitch + col * 2;
+        } else {
+          const int b = col >> 6, c = (col & 63) >> 3;
+          return base + b * kAtomBytes + i * 128 + ((c ^ (i & 7)) << 4);
+        }
+      };
+
+      if constexpr (MODE == MODE_STATS) {
+        StatsAcc acc = stats_empty();
+#pragma unroll
+        for (int ch = 0; ch < kHalf / 32; ++ch) {
+          float z[32];
+          tmem_ld32(taddr + ch * 32, z);
+          const int col0 = h * kHalf + ch * 32;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) add_bf16x8(lds128(chunk_addr(u_base, col0 + c * 8)), z + 8 * c);
+          float cm = -INFINITY;
+          int ci = 0x7fffffff;
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            z[e] *= j.scale;
+            if (n0 + col0 + e >= j.V) z[e] = -INFINITY;
+            if (ARGMAX && z[e] > cm) ci = n0 + col0 + e;
+            cm = fmaxf(cm, z[e]);
+          }
+          float cs = 0.0f;
+          if (cm > -INFINITY) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) cs += exp_shift(z[e], cm);
+          }
+          acc = stats_merge(acc, {cm, cs, ci});
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&acc_empty[as]);
+          mbar_arrive(&u_empty[us]);
+        }
+        if (tr.valid) {
+          const int cg = (n0 + h * kHalf) / 64;
+          const size_t o = (size_t)cg * j.rows + tr.prow;
+          if (n0 + h * kHalf < j.V) {
+            P.pm[o] = acc.m;
+            P.ps[o] = acc.s;
+            if (ARGMAX) P.pi[o] = acc.idx;
+          }
+        }
+      } else {
+        // pair modes: BN = 64, each warp half holds 32 columns
+        float b[32];
+        tmem_ld32(taddr, b);
+        const int col0 = h * kHalf;
+        Norm dn = {0.0f, 0.0f}, tn = {0.0f, 0.0f};
+        bool resid = true;
+        if (tr.valid) {
+          if constexpr (MODE == MODE_TV) {
+            tn = load_norm(j.tstats, (long long)tr.r * (j.gamma + 1) + (tr.k - 1));
+            dn = load_norm(j.dstats, (long long)tr.r * j.gamma + (tr.k - 1));
+          } else {
+            const int n = j.final_n[tr.r];
+            resid = j.final_kind[tr.r] != 0;
+            tn = load_norm(j.tstats, (long long)tr.r * (j.gamma + 1) + n);
+            if (resid) dn = load_norm(j.dstats, (long long)tr.r * j.gamma + n);
+          }
+        }
+        float sum = 0.0f;
+        if (tr.valid) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            float u[8], tv[8];
+            unpack_bf16x8(lds128(chunk_addr(t_base, col0 + c * 8)), tv);
+            if (resid) unpack_bf16x8(lds128(chunk_addr(u_base, col0 + c * 8)), u);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int v = n0 + col0 + c * 8 + e;
+              if (v >= j.V) continue;
+              const float pt = prob_of(tv[e] * j.scale, tn);
+              if (MODE == MODE_RESID && !resid) {
+                sum += pt;
+                continue;
+              }
+              const float pd = prob_of((u[e] + b[c * 8 + e]) * j.scale, dn);
+              sum += MODE == MODE_RESID ? fmaxf(pt - pd, 0.0f) : fminf(pt, pd);
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&acc_empty[as]);
+          mbar_arrive(&u_empty[us]);
+        }
+        // one partial per row and 32-column half
+        if (tr.valid && n0 + col0 < j.V) P.ps[(size_t)((n0 + col0) / 32) * j.rows + tr.prow] = sum;
+      }
+      if (++us == KU) { us = 0; uph ^= 1; }
+      accph[as] ^= 1;
+      as ^= 1;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(2 * BN < 32 ? 32 : 2 * BN)
+                 : "memory");
+  }
+}
+
+// ------------------------------------------------------------------------------ host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
+              const cuuint64_t* strides_bytes, const cuuint32_t* box) {
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims,
+                     strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN>
+size_t smem_bytes(bool pair) {
+  using C = Cfg<BN>;
+  return 1024 + 4 * kAtomBytes + C::kBStages * C::kBStageBytes +
+         (pair ? 2 : 1) * C::kUStages * C::kTileBytes + 512;
+}
+
+template <int BN, int MODE, bool ARGMAX, bool GATHER>
+cudaError_t launch_t(const TcParams& p, const CUtensorMap& w2, const CUtensorMap& u,
+                     const CUtensorMap& t, int grid, cudaStream_t s) {
+  const size_t smem = smem_bytes<BN>(MODE != MODE_STATS);
+  auto k = markov_tc_kernel<BN, MODE, ARGMAX, GATHER>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  k<<<grid, kThreads, smem, s>>>(w2, u, t, p);
+  return cudaGetLastError();
+}
+
+}  // namespace tc
+
+int markov_tc_seg(int mode) { return mode == MODE_STATS ? 64 : 32; }
+
+bool markov_tc_supported(int udt, int wdt, int rank, int V, const void* U, const void* T,
+                         const void* W1, const void* W2) {
+  auto al = [](const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
+  if (udt != SPEC_BF16 || wdt != SPEC_BF16) return false;
+  if (rank <= 0 || rank > 256 || rank % 64 != 0 || V % 8 != 0) return false;
+  if (!al(U) || !al(T) || !al(W1) || !al(W2)) return false;
+  int dev = 0, major = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
+    return false;
+  if (major < 10) return false;
+  return tc::encode_fn() != nullptr;
+}
+
+cudaError_t launch_markov_tc(const RowJob& j, float* pm, float* ps, int* pi, bool argmax,
+                             cudaStream_t s) {
+  using namespace tc;
+  TraceScope ts(SPEC_KCLASS_MARKOV, s);
+  const bool pair = j.mode != MODE_STATS;
+  const int BN = pair ? 64 : 128;
+  TcParams p;
+  p.j = j;
+  p.pm = pm;
+  p.ps = ps;
+  p.pi = pi;
+  const int rb = (j.R + kBM - 1) / kBM;
+  p.t.rb = rb;
+  p.t.n_mt = j.map == MAP_ALL_POS ? rb * j.gamma : rb;
+  p.t.n_nt = (j.V + BN - 1) / BN;
+  const long long total = (long long)p.t.n_mt * p.t.n_nt;
+  if (total == 0) return cudaSuccess;
+  const int grid = (int)(total < num_sms() ? total : num_sms());
+
+  CUtensorMap w2, u, t;
+  memset(&u, 0, sizeof u);
+  memset(&t, 0, sizeof t);
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)j.rank, (cuuint64_t)j.V};
+    const cuuint64_t str[1] = {(cuuint64_t)j.rank * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)BN};
+    if (!make_map(&w2, j.W2, 2, dims, str, box)) return cudaErrorInvalidValue;
+  }
+  const bool gather = j.map == MAP_FINAL;
+  if (!gather) {
+    const cuuint32_t box[3] = {64, 1, (cuuint32_t)kBM};
+    const cuuint64_t du[3] = {(cuuint64_t)j.V, (cuuint64_t)j.gamma, (cuuint64_t)j.R};
+    const cuuint64_t su[2] = {(cuuint64_t)j.V * 2, (cuuint64_t)j.V * 2 * j.gamma};
+    if (!make_map(&u, j.U, 3, du, su, box)) return cudaErrorInvalidValue;
+    if (pair) {
+      const cuuint64_t dt[3] = {(cuuint64_t)j.V, (cuuint64_t)j.gamma + 1, (cuuint64_t)j.R};
+      const cuuint64_t st[2] = {(cuuint64_t)j.V * 2, (cuuint64_t)j.V * 2 * (j.gamma + 1)};
+      if (!make_map(&t, j.T, 3, dt, st, box)) return cudaErrorInvalidValue;
+    }
+  }
+  if (j.mode == MODE_STATS) {
+    if (argmax) return launch_t<128, MODE_STATS, true, false>(p, w2, u, t, grid, s);
+    return launch_t<128, MODE_STATS, false, false>(p, w2, u, t, grid, s);
+  }
+  if (j.mode == MODE_TV) return launch_t<64, MODE_TV, false, false>(p, w2, u, t, grid, s);
+  return launch_t<64, MODE_RESID, false, true>(p, w2, u, t, grid, s);
 }
 
 }  // namespace spec

@@ -18,7 +18,8 @@ SPEC_OK = 0
 SPEC_F32, SPEC_BF16 = 0, 1
 (SPEC_OP_PROPOSE, SPEC_OP_VERIFY_GREEDY, SPEC_OP_VERIFY_REJECTION, SPEC_OP_TV_CONFIDENCE,
  SPEC_OP_SCHEDULE, SPEC_OP_TARGET_STATS, SPEC_OP_ALL) = range(7)
-SPEC_DEV_BAD_TOKEN, SPEC_DEV_NONFINITE, SPEC_DEV_EMPTY_RESIDUAL, SPEC_DEV_BAD_LENGTH = 1, 2, 4, 8
+(SPEC_DEV_BAD_TOKEN, SPEC_DEV_NONFINITE, SPEC_DEV_EMPTY_RESIDUAL, SPEC_DEV_BAD_LENGTH,
+ SPEC_DEV_TIMEOUT) = 1, 2, 4, 8, 16
 SPEC_SCHEDULE_MAX_CANDIDATES = 16384
 
 _lib = None
@@ -59,6 +60,11 @@ def lib():
         L.spec_tv_confidence.argtypes = [vp, vp, i, vp, vp, i, i, vp, vp, vp, vp, f, i, i, i, vp,
                                          vp, vp, sz, vp]
         L.spec_schedule_prefix.argtypes = [vp, vp, i, i, i, vp, vp, vp, vp, sz, vp]
+        L.spec_launch_count.restype = ctypes.c_ulonglong
+        L.spec_trace_events.argtypes = [i, vp, vp, i]
+        L.spec_trace_events.restype = i
+        L.spec_trace_count.argtypes = [i]
+        L.spec_trace_count.restype = i
         for name in ("spec_workspace_init", "spec_device_status", "spec_markov_propose",
                      "spec_verify_greedy", "spec_target_stats", "spec_verify_rejection",
                      "spec_tv_confidence", "spec_schedule_prefix"):

@@ -72,6 +72,7 @@ extern "C" {
 #define SPEC_DEV_NONFINITE 0x2u      /* a row's softmax normaliser was NaN or infinite */
 #define SPEC_DEV_EMPTY_RESIDUAL 0x4u /* a rejection met zero residual mass (p_t == p_d) */
 #define SPEC_DEV_BAD_LENGTH 0x8u     /* a per-request length outside [0, gamma] */
+#define SPEC_DEV_TIMEOUT 0x10u       /* a kernel's bounded wait expired; its outputs are invalid */
 
 /* Largest R * gamma the prefix scheduler accepts (its sort runs in one CTA's shared memory). */
 #define SPEC_SCHEDULE_MAX_CANDIDATES 16384

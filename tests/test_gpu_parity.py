@@ -252,3 +252,22 @@ def test_device_status_flags_nonfinite_logits(spec):
     assert ws.status() & spec.SPEC_DEV_NONFINITE
     t = toks.cpu()
     assert ((t >= 0) & (t < 512)).all()
+
+
+def test_greedy_bf16_markov_tensor_core(spec, ws):
+    """Greedy proposals with bf16 weights (tensor-core bias): ids match the oracle except where
+    the oracle's top-two score gap is below 1e-5 (the fp32 tensor-core accumulation order is
+    not the fp64 sum's); later positions of such a request are not compared."""
+    wl = W.markov_rejection("cpu", R=150, gamma=4, V=2056, rank=128, seed=31)
+    wl.W1 = (wl.W1.float() * 20).to(torch.bfloat16)     # make the bias matter
+    g = to_dev(wl, "cuda")
+    toks, logp, stats = spec.spec_markov_propose(g["U"], g["W1"], g["W2"], g["anchors"], None, 0.0,
+                                                 workspace=ws)
+    ref = oracle.markov_propose(wl.U, wl.W1, wl.W2, wl.anchors, None, 0.0)
+    gt = toks.cpu().numpy()
+    for r in range(wl.R):
+        for k in range(wl.gamma):
+            if gt[r, k] != ref["tokens"][r, k]:
+                assert ref["margin"][r, k] < 1e-5, (r, k, ref["margin"][r, k])
+                break
+    assert (gt == ref["tokens"]).all(axis=1).mean() > 0.95
