@@ -11,7 +11,7 @@ namespace spec {
 // Number of vocabulary columns per partial of the Markov producers (one epilogue half-tile).
 constexpr int kMarkovSeg = 64;
 // Number of vocabulary columns per partial of the rank-0 streaming producer.
-constexpr int kStreamSeg = 8192;
+constexpr int kStreamSeg = 32768;
 
 // Per-row outputs of a select pass.
 struct SelectOut {

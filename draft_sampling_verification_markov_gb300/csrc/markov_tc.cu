@@ -10,11 +10,13 @@
 //      evict-last policy (every row block and every draft position reads all of W2).
 //   D  [128 x BN] fp32 in tensor memory, two stages, read back with tcgen05.ld by the epilogue.
 //   U / T tiles: the base-logit (and target) rows of the same 128 rows x BN columns, by TMA
-//      with an evict-first policy (read once), or by per-row bulk copies when the rows of a
-//      tile are not equally spaced (the final rows of rejection verification).
-// Warp roles (320 threads, one CTA per SM, persistent over a contiguous range of tiles):
-//   warp 0      TMA producer;   warp 1  TMEM allocator + single-thread MMA issuer;
-//   warps 2..9  epilogue: warp w reads TMEM lanes 32*(w%4).. and column half (w-2)/4.
+//      with an evict-first policy (read once); when the rows of a tile are not equally spaced
+//      (the final rows of rejection verification) each epilogue thread loads its own row
+//      segment with 16-byte loads issued before it waits for the accumulator.
+// Warp roles (352 threads, one CTA per SM, persistent over a contiguous range of tiles):
+//   warp 0  W2 (B operand) TMA producer;  warp 1  TMEM allocator + single-thread MMA issuer;
+//   warp 2  U / T tile producer (decoupled from the B ring so logit rows stream ahead);
+//   warps 3..10  epilogue: warp w reads TMEM lanes 32*(w%4).. and column half (w-3)/4.
 // Epilogues (per row, per 64-column segment):
 //   MODE_STATS  z = (U + bias) * scale -> (max z, sum exp(z - max), first argmax);
 //   MODE_TV     sum min(p_d, p_t);    MODE_RESID  sum max(0, p_t - p_d) (p_t on bonus rows);
@@ -33,16 +35,17 @@ namespace tc {
 
 constexpr int kBM = 128;
 constexpr int kEpiWarps = 8;
-constexpr int kThreads = (2 + kEpiWarps) * 32;
+constexpr int kFirstEpi = 3;                       // warps 0..2: B producer, MMA, U/T producer
+constexpr int kThreads = (kFirstEpi + kEpiWarps) * 32;
 constexpr long long kSpinCycles = 4000000000LL;  // ~2 s at the maximum SM clock
 constexpr uint32_t kAtomBytes = kBM * 128;       // 128 rows x 128 B (64 bf16 of K)
 
-// BN = 128 (softmax partials, U only): A 64 KB + B 6 x 16 KB + U 2 x 32 KB = 224 KB.
+// BN = 128 (softmax partials, U only): A 64 KB + B 4 x 16 KB + U 3 x 32 KB = 224 KB.
 // BN = 64 (TV / residual, U and T): A 64 KB + B 6 x 8 KB + (U + T) 3 x 2 x 18 KB = 220 KB.
 template <int BN>
 struct Cfg {
-  static constexpr int kBStages = 6;
-  static constexpr int kUStages = BN == 128 ? 2 : 3;
+  static constexpr int kBStages = BN == 128 ? 4 : 6;
+  static constexpr int kUStages = 3;
   static constexpr uint32_t kBStageBytes = BN * 128;
   static constexpr uint32_t kRowPitch = BN * 2 + 16;  // gathered rows (pair modes only)
   static constexpr uint32_t kTileBytes = BN == 128 ? kBM * BN * 2 : kBM * kRowPitch;
@@ -135,16 +138,6 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
-// Untiled bulk copy global -> shared (both 16-byte aligned, size a multiple of 16).
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
-                                          uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
-      : "memory");
-}
-
 __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -202,6 +195,60 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 32 columns of this thread's TMEM lane, raw bits, without waiting (pair with tmem_wait_ld).
+__device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Packed pair arithmetic (two fp32 lanes per instruction).
+__device__ __forceinline__ unsigned long long pack2(float lo, float hi) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
+__device__ __forceinline__ void unpack2(unsigned long long v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ unsigned long long add2(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+__device__ __forceinline__ unsigned long long mul2(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b,
+                                                   unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
@@ -343,14 +390,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    // ---------------------------------------------------------------- TMA producer
-    const uint64_t pol_keep = policy_evict_last(), pol_stream = policy_evict_first();
-    int bs = 0, us = 0;
-    uint32_t bph = 0, uph = 0;
+    // ---------------------------------------------------------------- W2 (B) producer
+    const uint64_t pol_keep = policy_evict_last();
+    int bs = 0;
+    uint32_t bph = 0;
     bool ok = true;
     for (long long t = t_begin; t < t_end && ok; ++t) {
-      const int mt = (int)(t / P.t.n_nt), nt = (int)(t % P.t.n_nt);
-      const int n0 = nt * BN;
+      const int n0 = (int)(t % P.t.n_nt) * BN;
       for (int ka = 0; ka < ka_n && ok; ++ka) {
         ok = mbar_wait(&b_empty[bs], bph ^ 1, abort, status);
         if (ok && lane == 0) {
@@ -359,55 +405,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (++bs == KB) { bs = 0; bph ^= 1; }
       }
-      if (!ok) break;
+    }
+    // drain: every issued copy lands before the CTA moves on
+    if (lane == 0)
+      for (int s = 0; s < KB; ++s) mbar_drain(&b_full[s], (s < bs) ? bph : (bph ^ 1));
+  } else if (warp == 2) {
+    // ---------------------------------------------------------------- U / T producer
+    // (idle in gather mode: the epilogue loads the gathered final rows itself)
+    if constexpr (!GATHER) {
+    const uint64_t pol_stream = policy_evict_first();
+    int us = 0;
+    uint32_t uph = 0;
+    bool ok = true;
+    for (long long t = t_begin; t < t_end && ok; ++t) {
+      const int mt = (int)(t / P.t.n_nt), nt = (int)(t % P.t.n_nt);
+      const int n0 = nt * BN;
       ok = mbar_wait(&u_empty[us], uph ^ 1, abort, status);
       if (!ok) break;
       unsigned char* du = sU + us * C::kTileBytes;
       unsigned char* dt = sT + us * C::kTileBytes;
-      if constexpr (!GATHER) {
-        if (lane == 0) {
-          const TileRow tr = tile_row(j, P.t, mt, 0);
-          const int r0 = tr.r, kk = tr.k - 1;
-          constexpr int nbox = BN / 64;
-          mbar_arrive_expect_tx(&u_full[us], (kPair ? 2u : 1u) * nbox * kAtomBytes);
-          for (int b = 0; b < nbox; ++b) {
-            tma_load_3d(du + b * kAtomBytes, &map_u, n0 + b * 64, kk, r0, &u_full[us], pol_stream);
-            if constexpr (kPair)
-              tma_load_3d(dt + b * kAtomBytes, &map_t, n0 + b * 64, kk, r0, &u_full[us],
-                          pol_stream);
-          }
-        }
-      } else {
-        // final rows of rejection verification: one bulk copy per row (and per tensor)
-        const uint32_t bytes = (uint32_t)min(BN, j.V - n0) * 2u;
-        uint32_t mine = 0;
-        for (int i = lane; i < kBM; i += 32) {
-          const int r = mt * kBM + i;
-          if (r < j.R) mine += j.final_kind[r] ? 2u * bytes : bytes;
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, off);
-        if (lane == 0) mbar_arrive_expect_tx(&u_full[us], mine);
-        __syncwarp();
-        for (int i = lane; i < kBM; i += 32) {
-          const int r = mt * kBM + i;
-          if (r >= j.R) continue;
-          const int n = j.final_n[r];
-          const unsigned short* trow = reinterpret_cast<const unsigned short*>(j.T) +
-                                       ((size_t)r * (j.gamma + 1) + n) * j.V + n0;
-          bulk_load(dt + i * C::kRowPitch, trow, bytes, &u_full[us], pol_stream);
-          if (j.final_kind[r]) {
-            const unsigned short* urow = reinterpret_cast<const unsigned short*>(j.U) +
-                                         ((size_t)r * j.gamma + n) * j.V + n0;
-            bulk_load(du + i * C::kRowPitch, urow, bytes, &u_full[us], pol_stream);
-          }
+      if (lane == 0) {
+        const TileRow tr = tile_row(j, P.t, mt, 0);
+        const int r0 = tr.r, kk = tr.k - 1;
+        constexpr int nbox = BN / 64;
+        mbar_arrive_expect_tx(&u_full[us], (kPair ? 2u : 1u) * nbox * kAtomBytes);
+        for (int b = 0; b < nbox; ++b) {
+          tma_load_3d(du + b * kAtomBytes, &map_u, n0 + b * 64, kk, r0, &u_full[us], pol_stream);
+          if constexpr (kPair)
+            tma_load_3d(dt + b * kAtomBytes, &map_t, n0 + b * 64, kk, r0, &u_full[us],
+                        pol_stream);
         }
       }
       if (++us == KU) { us = 0; uph ^= 1; }
     }
-    // drain: every issued copy lands before the CTA moves on
-    if (lane == 0) {
-      for (int s = 0; s < KB; ++s) mbar_drain(&b_full[s], (s < bs) ? bph : (bph ^ 1));
+    if (lane == 0)
       for (int s = 0; s < KU; ++s) mbar_drain(&u_full[s], (s < us) ? uph : (uph ^ 1));
     }
   } else if (warp == 1) {
@@ -457,19 +488,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_drain(drain, 0);
     }
     __syncwarp();
-  } else {
+  } else if (warp >= kFirstEpi) {
     // ---------------------------------------------------------------- epilogue
-    const int ew = warp - 2;
-    const int q = warp & 3;          // TMEM lane quarter
-    const int h = ew >> 2;           // column half
-    const int i = q * 32 + lane;     // row within the tile
-    const int et = threadIdx.x - 64; // 0..255
+    const int ew = warp - kFirstEpi;
+    const int q = warp & 3;                       // TMEM lane quarter
+    const int h = ew >> 2;                        // column half
+    const int i = q * 32 + lane;                  // row within the tile
+    const int et = threadIdx.x - kFirstEpi * 32;  // 0..255
     int as = 0, us = 0;
     uint32_t accph[2] = {0, 0}, uph = 0, aeph = 0;
     int cur_mt = -1;
     bool ok = true;
-    float scale2 = j.scale * kLog2e;
-    (void)scale2;
     for (long long t = t_begin; t < t_end && ok; ++t) {
       const int mt = (int)(t / P.t.n_nt), nt = (int)(t % P.t.n_nt);
       const int n0 = nt * BN;
@@ -480,100 +509,143 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
         }
         cur_mt = mt;
-        // gather A: row ii <- W1[prev(ii)] in the swizzled K-major layout
+        // gather A: row ii <- W1[prev(ii)] in the swizzled K-major layout. All loads of a
+        // thread are issued before any store so that they overlap (up to 16 x 16 B).
         const int chunks = ka_n * 8;  // 16-byte chunks per row
-        for (int c = et; c < kBM * chunks; c += kEpiWarps * 32) {
-          const int ii = c / chunks, cc = c % chunks;
-          const int ka = cc >> 3, cw = cc & 7;
-          uint4 v = make_uint4(0, 0, 0, 0);
-          const TileRow tr = tile_row(j, P.t, mt, ii);
-          if (tr.valid) {
-            int prev;
-            if (j.map == MAP_FINAL) {
-              const int n = j.final_n[tr.r];
-              prev = n == 0 ? j.anchors[tr.r] : j.tokens[(size_t)tr.r * j.gamma + n - 1];
-            } else {
-              prev = tr.k == 1 ? j.anchors[tr.r] : j.tokens[(size_t)tr.r * j.gamma + tr.k - 2];
+        constexpr int kMaxPer = kBM * 32 / (kEpiWarps * 32);
+        uint4 v[kMaxPer];
+#pragma unroll
+        for (int it = 0; it < kMaxPer; ++it) {
+          const int c = et + it * kEpiWarps * 32;
+          v[it] = make_uint4(0, 0, 0, 0);
+          if (c < kBM * chunks) {
+            const int ii = c / chunks, cc = c % chunks;
+            const TileRow tr = tile_row(j, P.t, mt, ii);
+            if (tr.valid) {
+              int prev;
+              if (j.map == MAP_FINAL) {
+                const int n = j.final_n[tr.r];
+                prev = n == 0 ? j.anchors[tr.r] : j.tokens[(size_t)tr.r * j.gamma + n - 1];
+              } else {
+                prev = tr.k == 1 ? j.anchors[tr.r] : j.tokens[(size_t)tr.r * j.gamma + tr.k - 2];
+              }
+              if (prev < 0 || prev >= j.V) {
+                atomicOr(status, SPEC_DEV_BAD_TOKEN);
+                prev = 0;
+              }
+              v[it] = __ldg(reinterpret_cast<const uint4*>(
+                                reinterpret_cast<const unsigned short*>(j.W1) +
+                                (size_t)prev * j.rank) +
+                            cc);
             }
-            if (prev < 0 || prev >= j.V) {
-              atomicOr(status, SPEC_DEV_BAD_TOKEN);
-              prev = 0;
-            }
-            v = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const unsigned short*>(j.W1) +
-                                                     (size_t)prev * j.rank) +
-                      cc);
           }
-          *reinterpret_cast<uint4*>(sA + ka * kAtomBytes + ii * 128 + ((cw ^ (ii & 7)) << 4)) = v;
+        }
+#pragma unroll
+        for (int it = 0; it < kMaxPer; ++it) {
+          const int c = et + it * kEpiWarps * 32;
+          if (c < kBM * chunks) {
+            const int ii = c / chunks, cc = c % chunks;
+            const int ka = cc >> 3, cw = cc & 7;
+            *reinterpret_cast<uint4*>(sA + ka * kAtomBytes + ii * 128 + ((cw ^ (ii & 7)) << 4)) =
+                v[it];
+          }
         }
         fence_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(a_full);
       }
-      ok = mbar_wait(&acc_full[as], accph[as], abort, status);
-      if (!ok) break;
-      tc_fence_after();
-      ok = mbar_wait(&u_full[us], uph, abort, status);
-      if (!ok) break;
-
       const TileRow tr = tile_row(j, P.t, mt, i);
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + as * BN + h * kHalf;
-      const uint32_t u_base = smem_u32(sU + us * C::kTileBytes);
-      const uint32_t t_base = smem_u32(sT + us * C::kTileBytes);
-      // address of 16-byte chunk c (8 columns) of this thread's row, tile-relative column
-      auto chunk_addr = [&](uint32_t base, int col) -> uint32_t {
-        if constexpr (GATHER) {
-          return base + i * C::kRowPitch + col * 2;
-        } else {
-          const int b = col >> 6, c = (col & 63) >> 3;
-          return base + b * kAtomBytes + i * 128 + ((c ^ (i & 7)) << 4);
-        }
-      };
+      const int col0 = h * kHalf;  // first tile column of this warp
+      const bool tail = n0 + BN > j.V;
 
       if constexpr (MODE == MODE_STATS) {
-        StatsAcc acc = stats_empty();
+        ok = mbar_wait(&acc_full[as], accph[as], abort, status);
+        if (!ok) break;
+        tc_fence_after();
+        ok = mbar_wait(&u_full[us], uph, abort, status);
+        if (!ok) break;
+        // both TMEM reads and all shared-memory reads first, then release the stages
+        uint32_t braw[64];
+        tmem_ld32_async(taddr, braw);
+        tmem_ld32_async(taddr + 32, braw + 32);
+        const uint32_t u_base = smem_u32(sU + us * C::kTileBytes);
+        uint4 uw[8];
 #pragma unroll
-        for (int ch = 0; ch < kHalf / 32; ++ch) {
-          float z[32];
-          tmem_ld32(taddr + ch * 32, z);
-          const int col0 = h * kHalf + ch * 32;
-#pragma unroll
-          for (int c = 0; c < 4; ++c) add_bf16x8(lds128(chunk_addr(u_base, col0 + c * 8)), z + 8 * c);
-          float cm = -INFINITY;
-          int ci = 0x7fffffff;
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            z[e] *= j.scale;
-            if (n0 + col0 + e >= j.V) z[e] = -INFINITY;
-            if (ARGMAX && z[e] > cm) ci = n0 + col0 + e;
-            cm = fmaxf(cm, z[e]);
-          }
-          float cs = 0.0f;
-          if (cm > -INFINITY) {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) cs += exp_shift(z[e], cm);
-          }
-          acc = stats_merge(acc, {cm, cs, ci});
+        for (int c = 0; c < 8; ++c) {
+          const int cc = c, b = col0 >> 6;
+          uw[c] = lds128(u_base + b * kAtomBytes + i * 128 + ((cc ^ (i & 7)) << 4));
         }
+        tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(&acc_empty[as]);
           mbar_arrive(&u_empty[us]);
         }
-        if (tr.valid) {
-          const int cg = (n0 + h * kHalf) / 64;
-          const size_t o = (size_t)cg * j.rows + tr.prow;
-          if (n0 + h * kHalf < j.V) {
-            P.pm[o] = acc.m;
-            P.ps[o] = acc.s;
-            if (ARGMAX) P.pi[o] = acc.idx;
+        // z = (bias + U) * scale, two columns per instruction
+        const unsigned long long sc2 = pack2(j.scale, j.scale);
+        float z[64];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint32_t w[4] = {uw[c].x, uw[c].y, uw[c].z, uw[c].w};
+#pragma unroll
+          for (int p = 0; p < 4; ++p) {
+            const int e = 8 * c + 2 * p;
+            const unsigned long long u2 =
+                pack2(__uint_as_float(w[p] << 16), __uint_as_float(w[p] & 0xffff0000u));
+            const unsigned long long b2 =
+                pack2(__uint_as_float(braw[e]), __uint_as_float(braw[e + 1]));
+            unpack2(mul2(add2(b2, u2), sc2), z[e], z[e + 1]);
           }
         }
+        if (tail) {
+#pragma unroll
+          for (int e = 0; e < 64; ++e)
+            if (n0 + col0 + e >= j.V) z[e] = -INFINITY;
+        }
+        // maximum (3-input tree) and, for greedy, its first position
+        float t22[22];
+#pragma unroll
+        for (int e = 0; e < 21; ++e) t22[e] = max3(z[3 * e], z[3 * e + 1], z[3 * e + 2]);
+        t22[21] = z[63];
+        float t8[8];
+#pragma unroll
+        for (int e = 0; e < 7; ++e) t8[e] = max3(t22[3 * e], t22[3 * e + 1], t22[3 * e + 2]);
+        t8[7] = t22[21];
+        const float m = max3(max3(t8[0], t8[1], t8[2]), max3(t8[3], t8[4], t8[5]),
+                             fmaxf(t8[6], t8[7]));
+        int idx = 0x7fffffff;
+        if (ARGMAX) {
+#pragma unroll
+          for (int e = 63; e >= 0; --e)
+            if (z[e] == m) idx = n0 + col0 + e;
+        }
+        // sum of exp(z - m): 2^(fma(z, log2e, -fl(m log2e))) carries the common factor 2^delta
+        // (delta = the exact rounding error of m log2e), removed once per partial below
+        float s = 0.0f;
+        if (m > -INFINITY) {
+          const float nml = -(m * kLog2e);
+          const float delta = fmaf(m, kLog2e, nml);
+          const unsigned long long l2 = pack2(kLog2e, kLog2e), n2 = pack2(nml, nml);
+          float acc4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+          for (int e = 0; e < 64; e += 2) {
+            float a, b;
+            unpack2(fma2(pack2(z[e], z[e + 1]), l2, n2), a, b);
+            acc4[(e >> 1) & 3] += fast_exp2(a) + fast_exp2(b);
+          }
+          s = ((acc4[0] + acc4[1]) + (acc4[2] + acc4[3])) * (1.0f - delta * kLn2);
+        }
+        if (tr.valid && n0 + col0 < j.V) {
+          const size_t o = (size_t)((n0 + col0) / 64) * j.rows + tr.prow;
+          P.pm[o] = m;
+          P.ps[o] = s;
+          if (ARGMAX) P.pi[o] = idx;
+        }
+        if (++us == KU) { us = 0; uph ^= 1; }
       } else {
-        // pair modes: BN = 64, each warp half holds 32 columns
-        float b[32];
-        tmem_ld32(taddr, b);
-        const int col0 = h * kHalf;
+        // pair modes: BN = 64, each warp half holds 32 columns (4 chunks of 8)
         Norm dn = {0.0f, 0.0f}, tn = {0.0f, 0.0f};
         bool resid = true;
         if (tr.valid) {
@@ -587,17 +659,68 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (resid) dn = load_norm(j.dstats, (long long)tr.r * j.gamma + n);
           }
         }
+        const bool live = tr.valid && n0 + col0 < j.V;
+        uint4 tw[4], uw[4];
+        if constexpr (GATHER) {
+          // gathered final rows: this thread loads its own row segment (issued before the
+          // wait for the accumulator so that the loads overlap it)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            tw[c] = make_uint4(0, 0, 0, 0);
+            uw[c] = make_uint4(0, 0, 0, 0);
+          }
+          if (live) {
+            const int n = j.final_n[tr.r];
+            const uint4* trow = reinterpret_cast<const uint4*>(
+                reinterpret_cast<const unsigned short*>(j.T) +
+                ((size_t)tr.r * (j.gamma + 1) + n) * j.V + n0 + col0);
+            const uint4* urow = reinterpret_cast<const uint4*>(
+                reinterpret_cast<const unsigned short*>(j.U) +
+                ((size_t)tr.r * j.gamma + n) * j.V + n0 + col0);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              if (n0 + col0 + 8 * c < j.V) {
+                tw[c] = ld_stream16(trow + c);
+                if (resid) uw[c] = ld_stream16(urow + c);
+              }
+            }
+          }
+        }
+        ok = mbar_wait(&acc_full[as], accph[as], abort, status);
+        if (!ok) break;
+        tc_fence_after();
+        if constexpr (!GATHER) {
+          ok = mbar_wait(&u_full[us], uph, abort, status);
+          if (!ok) break;
+          const uint32_t u_base = smem_u32(sU + us * C::kTileBytes);
+          const uint32_t t_base = smem_u32(sT + us * C::kTileBytes);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int cc = (col0 >> 3) + c;
+            const uint32_t off = i * 128 + ((cc ^ (i & 7)) << 4);
+            tw[c] = lds128(t_base + off);
+            uw[c] = lds128(u_base + off);
+          }
+        }
+        float b[32];
+        tmem_ld32(taddr, b);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&acc_empty[as]);
+          if constexpr (!GATHER) mbar_arrive(&u_empty[us]);
+        }
         float sum = 0.0f;
-        if (tr.valid) {
+        if (live) {
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             float u[8], tv[8];
-            unpack_bf16x8(lds128(chunk_addr(t_base, col0 + c * 8)), tv);
-            if (resid) unpack_bf16x8(lds128(chunk_addr(u_base, col0 + c * 8)), u);
+            unpack_bf16x8(tw[c], tv);
+            unpack_bf16x8(uw[c], u);
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
               const int v = n0 + col0 + c * 8 + e;
-              if (v >= j.V) continue;
+              if (tail && v >= j.V) continue;
               const float pt = prob_of(tv[e] * j.scale, tn);
               if (MODE == MODE_RESID && !resid) {
                 sum += pt;
@@ -607,17 +730,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               sum += MODE == MODE_RESID ? fmaxf(pt - pd, 0.0f) : fminf(pt, pd);
             }
           }
+          // one partial per row and 32-column half
+          P.ps[(size_t)((n0 + col0) / 32) * j.rows + tr.prow] = sum;
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&acc_empty[as]);
-          mbar_arrive(&u_empty[us]);
+        if constexpr (!GATHER) {
+          if (++us == KU) { us = 0; uph ^= 1; }
         }
-        // one partial per row and 32-column half
-        if (tr.valid && n0 + col0 < j.V) P.ps[(size_t)((n0 + col0) / 32) * j.rows + tr.prow] = sum;
       }
-      if (++us == KU) { us = 0; uph ^= 1; }
       accph[as] ^= 1;
       as ^= 1;
     }

@@ -97,13 +97,17 @@ __device__ __forceinline__ void load8(const void* base, size_t row_off, int v, i
 
 // Rank-0 rows. One block per (row, segment) unit, grid-stride. MODE_STATS reduces the row's
 // primary logits (U if the row has a draft side, else the target); SUM / ARGMAX select which
-// halves of the partial are needed. MODE_RESID / MODE_TV reduce the pair value.
+// halves of the partial are needed. MODE_RESID / MODE_TV reduce the pair value. Each thread
+// issues kBatch independent 16-byte loads (per tensor) before doing any arithmetic on them.
+constexpr int kBatch = 4;
+
 template <int DT, int MODE, bool SUM, bool ARGMAX>
 __global__ void __launch_bounds__(256) stream_partials_kernel(RowJob j, int seg, int nseg, bool vec,
                                                               float* pm, float* ps, int* pi) {
-  const long long units = (long long)j.rows * nseg;
-  for (long long u = blockIdx.x; u < units; u += gridDim.x) {
-    const int row = (int)(u / nseg), sg = (int)(u % nseg);
+  const int units = j.rows * nseg;
+  const int step = blockDim.x * 8;  // columns per block-wide vector sweep
+  for (int u = blockIdx.x; u < units; u += gridDim.x) {
+    const int row = u / nseg, sg = u - row * nseg;
     const RowInfo ri = row_info(j, row);
     const int v0 = sg * seg, v1 = min(j.V, v0 + seg);
     const size_t out = (size_t)sg * j.rows + row;
@@ -120,26 +124,28 @@ __global__ void __launch_bounds__(256) stream_partials_kernel(RowJob j, int seg,
       const void* src = draft ? j.U : j.T;
       const size_t off = (size_t)(draft ? ri.urow : ri.trow) * j.V;
       StatsAcc acc = stats_empty();
-      for (int v = v0 + threadIdx.x * 8; v < v1; v += blockDim.x * 8) {
-        float x[8];
-        load8<DT>(src, off, v, v1, vec, x);
-        float g = -INFINITY;
+      for (int base = v0 + threadIdx.x * 8; base < v1; base += kBatch * step) {
+        float x[kBatch][8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          x[i] = __fmul_rn(x[i], j.scale);
-          if (ARGMAX && x[i] > acc.m && x[i] > g) {  // first strict maximum in order
-            g = x[i];
-            acc.idx = v + i;
+        for (int b = 0; b < kBatch; ++b) load8<DT>(src, off, base + b * step, v1, vec, x[b]);
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+          const int v = base + b * step;
+          float g = -INFINITY;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            x[b][i] = __fmul_rn(x[b][i], j.scale);
+            if (ARGMAX && x[b][i] > acc.m && x[b][i] > g) acc.idx = v + i;  // first maximum
+            g = fmaxf(g, x[b][i]);
           }
-          g = fmaxf(g, x[i]);
-        }
-        if (g > acc.m) {
-          if (SUM && acc.s != 0.0f) acc.s *= exp_shift(acc.m, g);
-          acc.m = g;
-        }
-        if (SUM && acc.m != -INFINITY) {
+          if (g > acc.m) {
+            if (SUM && acc.s != 0.0f) acc.s *= exp_shift(acc.m, g);
+            acc.m = g;
+          }
+          if (SUM && acc.m != -INFINITY) {
 #pragma unroll
-          for (int i = 0; i < 8; ++i) acc.s += exp_shift(x[i], acc.m);
+            for (int i = 0; i < 8; ++i) acc.s += exp_shift(x[b][i], acc.m);
+          }
         }
       }
       acc = block_merge(acc);
@@ -153,20 +159,26 @@ __global__ void __launch_bounds__(256) stream_partials_kernel(RowJob j, int seg,
       row_norms(j, ri, dn, tn);
       const bool pair = MODE == MODE_TV || ri.resid;
       float acc = 0.0f;
-      for (int v = v0 + threadIdx.x * 8; v < v1; v += blockDim.x * 8) {
-        float xt[8], xd[8];
-        load8<DT>(j.T, (size_t)ri.trow * j.V, v, v1, vec, xt);
-        if (pair) load8<DT>(j.U, (size_t)ri.urow * j.V, v, v1, vec, xd);
+      for (int base = v0 + threadIdx.x * 8; base < v1; base += kBatch * step) {
+        float xt[kBatch][8], xd[kBatch][8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          if (v + i >= v1) continue;
-          const float pt = prob_of(__fmul_rn(xt[i], j.scale), tn);
-          if (!pair) {
-            acc += pt;
-            continue;
+        for (int b = 0; b < kBatch; ++b) {
+          load8<DT>(j.T, (size_t)ri.trow * j.V, base + b * step, v1, vec, xt[b]);
+          if (pair) load8<DT>(j.U, (size_t)ri.urow * j.V, base + b * step, v1, vec, xd[b]);
+        }
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            if (base + b * step + i >= v1) continue;
+            const float pt = prob_of(__fmul_rn(xt[b][i], j.scale), tn);
+            if (!pair) {
+              acc += pt;
+              continue;
+            }
+            const float pd = prob_of(__fmul_rn(xd[b][i], j.scale), dn);
+            acc += MODE == MODE_RESID ? fmaxf(pt - pd, 0.0f) : fminf(pt, pd);
           }
-          const float pd = prob_of(__fmul_rn(xd[i], j.scale), dn);
-          acc += MODE == MODE_RESID ? fmaxf(pt - pd, 0.0f) : fminf(pt, pd);
         }
       }
       acc = block_sum(acc);
@@ -256,75 +268,128 @@ __device__ __forceinline__ double block_exscan_d(double x, double* total) {
   return ex;
 }
 
+// Value of element v of the crossing segment: exp(z_d - M) for a proposal, or the residual /
+// bonus mass q(v) for a final draw; z_d is passed in (bias already included).
+template <int UDT, int WDT>
+__device__ __forceinline__ float seg_value(const RowJob& j, const RowInfo& ri, bool resid,
+                                           float M, Norm dn, Norm tn, int v, float zd) {
+  if (!resid) return exp_shift(zd, M);
+  const float pt = prob_of(target_logit<UDT>(j, ri, v), tn);
+  if (!ri.resid) return pt;
+  return fmaxf(pt - prob_of(zd, dn), 0.0f);
+}
+
+// Draft logits of columns [v0, v0 + n) (n <= 64) into zs[], using all 256 threads. bf16
+// weights: a split-K dot product (256/64.. threads per column, 16-byte loads, shuffle
+// reduction); fp32 weights: the canonical fp32 chain, one thread per column.
+template <int UDT, int WDT>
+__device__ void segment_logits(const RowJob& j, const RowInfo& ri, int v0, int n, float* zs) {
+  const int tid = threadIdx.x;
+  if (WDT == SPEC_BF16 && j.rank > 0 && (j.rank % 8) == 0) {
+    const int tpc = blockDim.x / 64;          // threads per column (4)
+    const int col = tid / tpc, part = tid % tpc;
+    const int v = v0 + col;
+    float acc = 0.0f;
+    if (col < n) {
+      const uint4* w1 = reinterpret_cast<const uint4*>(
+          reinterpret_cast<const unsigned short*>(j.W1) + (size_t)ri.prev * j.rank);
+      const uint4* w2 = reinterpret_cast<const uint4*>(
+          reinterpret_cast<const unsigned short*>(j.W2) + (size_t)v * j.rank);
+      for (int c = part; c < j.rank / 8; c += tpc) {
+        const uint4 a = __ldg(w1 + c), b = __ldg(w2 + c);
+        const uint32_t aa[4] = {a.x, a.y, a.z, a.w}, bb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          acc = fmaf(__uint_as_float(aa[e] << 16), __uint_as_float(bb[e] << 16), acc);
+          acc = fmaf(__uint_as_float(aa[e] & 0xffff0000u), __uint_as_float(bb[e] & 0xffff0000u), acc);
+        }
+      }
+    }
+    for (int off = tpc / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (col < n && part == 0) {
+      const float s = __fadd_rn(ld_elem<UDT>(j.U, (size_t)ri.urow * j.V + v), acc);
+      zs[col] = __fmul_rn(s, j.scale);
+    }
+  } else {
+    if (tid < n) zs[tid] = draft_logit<UDT, WDT>(j, ri, v0 + tid);
+  }
+  __syncthreads();
+}
+
 // One block (256 threads) per row.
 //   kind 0 (MODE_STATS partials): greedy argmax, or inverse-CDF draw from the softmax;
 //   kind 1 (MODE_RESID partials): inverse-CDF draw from the residual / bonus distribution.
-// The crossing segment is recomputed element by element; everything else uses the partials.
+// Only the crossing segment is recomputed element by element; everything else uses the
+// partials. Markov segments (<= 64 columns) are rebuilt once into shared memory.
 template <int UDT, int WDT>
 __global__ void __launch_bounds__(256) select_kernel(RowJob j, int seg, int nseg, const float* pm,
                                                      const float* ps, const int* pi,
                                                      SelectOut o) {
-  __shared__ int sh_c;
+  __shared__ int sh_c, sh_x, sh_last;
   __shared__ double sh_rem;
   __shared__ float sh_M, sh_lz;
+  __shared__ float zs[64];   // draft logits of the segment starting at sh_zv0
+  __shared__ float es[64];
+  __shared__ int sh_zv0;
   const int row = blockIdx.x;
   if (row >= j.rows) return;
   const RowInfo ri = row_info(j, row);
   const int tid = threadIdx.x;
-  const int resid = o.kind == 1;
+  const bool resid = o.kind == 1;
+  const bool markov = resid ? (ri.resid && j.rank > 0) : j.rank > 0;
+  const bool need_z = j.rank > 0 && (!resid || ri.resid);
 
-  // 1. normaliser from the partials
+  // 1. normaliser from the partials (a contiguous run of segments per thread)
+  const int run = (nseg + blockDim.x - 1) / blockDim.x;
+  const int c0 = min(nseg, tid * run), c1 = min(nseg, c0 + run);
   float M = -INFINITY;
+  int gidx = 0x7fffffff;
   if (!resid) {
     StatsAcc a = stats_empty();
-    for (int c = tid; c < nseg; c += blockDim.x) {
+    for (int c = c0; c < c1; ++c) {
       const size_t q = (size_t)c * j.rows + row;
       a = stats_merge(a, {pm[q], ps[q], pi ? pi[q] : 0x7fffffff});
     }
     a = block_merge(a);
     M = a.m;
-    if (o.greedy) {
-      // argmax from the partials' first maxima
-      if (tid == 0) {
-        int x = a.idx;
-        if (!(M > -INFINITY) || x < 0 || x >= j.V) {
-          atomicOr(j.status, SPEC_DEV_NONFINITE);
-          x = 0;
-        }
-        sh_c = x;
-      }
-    }
+    gidx = a.idx;
   }
-  // run of segments owned by this thread
-  const int run = (nseg + blockDim.x - 1) / blockDim.x;
-  const int c0 = min(nseg, tid * run), c1 = min(nseg, c0 + run);
   double local = 0.0;
   for (int c = c0; c < c1; ++c) {
     const size_t q = (size_t)c * j.rows + row;
-    local += resid ? (double)ps[q]
-                   : (ps[q] == 0.0f ? 0.0 : (double)ps[q] * (double)exp_shift(pm[q], M));
+    local += resid ? (double)ps[q] : (ps[q] == 0.0f ? 0.0 : (double)(ps[q] * exp_shift(pm[q], M)));
   }
   double Z;
   const double before = block_exscan_d(local, &Z);
-  if (!resid && tid == 0) {
+  if (tid == 0) {
     sh_M = M;
-    sh_lz = (float)log(Z);
-    if (!(Z > 0.0) || !isfinite(Z) || !(M > -INFINITY)) atomicOr(j.status, SPEC_DEV_NONFINITE);
+    sh_lz = resid ? 0.0f : (float)log(Z);
+    sh_c = -1;
+    sh_rem = 0.0;
+    sh_x = -1;
+    sh_last = -1;
+    sh_zv0 = -1;
+    if (!resid && (!(Z > 0.0) || !isfinite(Z) || !(M > -INFINITY)))
+      atomicOr(j.status, SPEC_DEV_NONFINITE);
   }
+  __syncthreads();
 
-  int x;
+  int x = -1;
   if (!resid && o.greedy) {
-    __syncthreads();
-    x = sh_c;
+    x = gidx;
+    if (x < 0 || x >= j.V) {
+      if (tid == 0) atomicOr(j.status, SPEC_DEV_NONFINITE);
+      x = 0;
+    }
+    if (markov && o.logp) {  // rebuild the segment holding x for its log-probability
+      const int v0 = (x / 64) * 64;
+      segment_logits<UDT, WDT>(j, ri, v0, min(64, j.V - v0), zs);
+      if (tid == 0) sh_zv0 = v0;
+      __syncthreads();
+    }
   } else {
     // 2. crossing segment for t = u * Z
-    const double u = (double)o.uni[(size_t)row * o.uni_stride + o.uni_offset];
-    const double t = u * Z;
-    if (tid == 0) {
-      sh_c = -1;
-      sh_rem = 0.0;
-    }
-    __syncthreads();
+    const double t = (double)o.uni[(size_t)row * o.uni_stride + o.uni_offset] * Z;
     if (before <= t && before + local > t) {
       double cum = before;
       int lastc = -1;
@@ -332,7 +397,7 @@ __global__ void __launch_bounds__(256) select_kernel(RowJob j, int seg, int nseg
       for (int c = c0; c < c1; ++c) {
         const size_t q = (size_t)c * j.rows + row;
         const double w = resid ? (double)ps[q]
-                               : (ps[q] == 0.0f ? 0.0 : (double)ps[q] * (double)exp_shift(pm[q], M));
+                               : (ps[q] == 0.0f ? 0.0 : (double)(ps[q] * exp_shift(pm[q], M)));
         if (cum + w > t) {
           lastc = c;
           lastw = t - cum;
@@ -348,60 +413,87 @@ __global__ void __launch_bounds__(256) select_kernel(RowJob j, int seg, int nseg
       sh_rem = lastw;
     }
     __syncthreads();
-    if (sh_c < 0) {
-      // rounding left no crossing: take the last segment with positive mass, at its end
-      if (tid == 0) {
-        int last = -1;
-        for (int c = nseg - 1; c >= 0 && last < 0; --c)
-          if (ps[(size_t)c * j.rows + row] > 0.0f) last = c;
-        if (last < 0) atomicOr(j.status, resid ? SPEC_DEV_EMPTY_RESIDUAL : SPEC_DEV_NONFINITE);
-        sh_c = last;
-        sh_rem = 1e300;
-      }
-      __syncthreads();
-    }
-    const int cstar = sh_c;
-    const double rem = sh_rem;
-    // 3. recompute the crossing segment and scan it in token order
-    Norm dn, tn;
-    if (resid) row_norms(j, ri, dn, tn);
-    const int v0 = max(cstar, 0) * seg, v1 = min(j.V, v0 + seg);
-    const int per = (seg + blockDim.x - 1) / blockDim.x;
-    const int e0 = min(v1, v0 + tid * per), e1 = min(v1, e0 + per);
-    float mine = 0.0f;
-    for (int v = e0; v < e1; ++v)
-      mine += resid ? pair_value<UDT, WDT, MODE_RESID>(j, ri, dn, tn, v)
-                    : exp_shift(draft_logit<UDT, WDT>(j, ri, v), M);
-    double segtot;
-    const double sbefore = block_exscan_d((double)mine, &segtot);
-    __shared__ int sh_x;
-    __shared__ int sh_last;
-    if (tid == 0) {
-      sh_x = -1;
-      sh_last = -1;
+    if (sh_c < 0 && tid == 0) {
+      // rounding left no crossing: the end of the last segment with positive mass
+      int last = -1;
+      for (int c = nseg - 1; c >= 0 && last < 0; --c)
+        if (ps[(size_t)c * j.rows + row] > 0.0f) last = c;
+      if (last < 0) atomicOr(j.status, resid ? SPEC_DEV_EMPTY_RESIDUAL : SPEC_DEV_NONFINITE);
+      sh_c = last;
+      sh_rem = 1e300;
     }
     __syncthreads();
-    if (cstar >= 0) {
-      if (sbefore <= rem && sbefore + (double)mine > rem) {
-        double cum = sbefore;
-        for (int v = e0; v < e1; ++v) {
-          const float w = resid ? pair_value<UDT, WDT, MODE_RESID>(j, ri, dn, tn, v)
-                                : exp_shift(draft_logit<UDT, WDT>(j, ri, v), M);
-          if (cum + (double)w > rem) {
-            sh_x = v;
-            break;
+    const int cstar = sh_c;
+    const double rem = sh_rem;
+    Norm dn = {0.0f, 0.0f}, tn = {0.0f, 0.0f};
+    if (resid) row_norms(j, ri, dn, tn);
+    const int v0 = max(cstar, 0) * seg, v1 = min(j.V, v0 + seg);
+    if (seg <= 64) {
+      // 3a. small segment: values into shared memory, warp 0 scans in token order
+      if (need_z) {
+        segment_logits<UDT, WDT>(j, ri, v0, v1 - v0, zs);
+        if (tid == 0) sh_zv0 = v0;
+      }
+      for (int e = tid; e < v1 - v0; e += blockDim.x) {
+        const float zd = need_z ? zs[e] : (ri.urow >= 0 ? draft_logit<UDT, WDT>(j, ri, v0 + e) : 0.0f);
+        es[e] = seg_value<UDT, WDT>(j, ri, resid, M, dn, tn, v0 + e, zd);
+      }
+      __syncthreads();
+      if (tid < 32 && cstar >= 0) {
+        const int n = v1 - v0;
+        float a0 = tid < n ? es[tid] : 0.0f, a1 = tid + 32 < n ? es[tid + 32] : 0.0f;
+        float s0 = a0, s1 = a1;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const float y0 = __shfl_up_sync(0xffffffffu, s0, off);
+          const float y1 = __shfl_up_sync(0xffffffffu, s1, off);
+          if (tid >= off) {
+            s0 += y0;
+            s1 += y1;
           }
-          cum += w;
+        }
+        const float tot0 = __shfl_sync(0xffffffffu, s0, 31);
+        s1 += tot0;
+        const float r = (float)fmin(rem, 1e30);
+        const unsigned m0 = __ballot_sync(0xffffffffu, s0 > r && tid < n);
+        const unsigned m1 = __ballot_sync(0xffffffffu, s1 > r && tid + 32 < n);
+        const unsigned p0 = __ballot_sync(0xffffffffu, a0 > 0.0f), p1 = __ballot_sync(0xffffffffu, a1 > 0.0f);
+        if (tid == 0) {
+          if (m0) sh_x = v0 + __ffs(m0) - 1;
+          else if (m1) sh_x = v0 + 32 + __ffs(m1) - 1;
+          sh_last = p1 ? v0 + 32 + 31 - __clz(p1) : (p0 ? v0 + 31 - __clz(p0) : -1);
         }
       }
-      // last positive element of the segment (fallback for a remainder past its end)
-      int lastp = -1;
-      for (int v = e1 - 1; v >= e0 && lastp < 0; --v) {
-        const float w = resid ? pair_value<UDT, WDT, MODE_RESID>(j, ri, dn, tn, v)
-                              : exp_shift(draft_logit<UDT, WDT>(j, ri, v), M);
-        if (w > 0.0f) lastp = v;
+    } else {
+      // 3b. long segment (no Markov bias): per-thread runs, block scan, rescan one run
+      const int per = (seg + blockDim.x - 1) / blockDim.x;
+      const int e0 = min(v1, v0 + tid * per), e1 = min(v1, e0 + per);
+      float mine = 0.0f;
+      for (int v = e0; v < e1; ++v)
+        mine += seg_value<UDT, WDT>(j, ri, resid, M, dn, tn, v,
+                                    ri.urow >= 0 ? draft_logit<UDT, WDT>(j, ri, v) : 0.0f);
+      double segtot;
+      const double sbefore = block_exscan_d((double)mine, &segtot);
+      if (cstar >= 0) {
+        if (sbefore <= rem && sbefore + (double)mine > rem) {
+          double cum = sbefore;
+          for (int v = e0; v < e1; ++v) {
+            const float w = seg_value<UDT, WDT>(j, ri, resid, M, dn, tn, v,
+                                                ri.urow >= 0 ? draft_logit<UDT, WDT>(j, ri, v) : 0.0f);
+            if (cum + (double)w > rem) {
+              sh_x = v;
+              break;
+            }
+            cum += w;
+          }
+        }
+        int lastp = -1;
+        for (int v = e1 - 1; v >= e0 && lastp < 0; --v)
+          if (seg_value<UDT, WDT>(j, ri, resid, M, dn, tn, v,
+                                  ri.urow >= 0 ? draft_logit<UDT, WDT>(j, ri, v) : 0.0f) > 0.0f)
+            lastp = v;
+        if (lastp >= 0) atomicMax(&sh_last, lastp);
       }
-      if (lastp >= 0) atomicMax(&sh_last, lastp);
     }
     __syncthreads();
     x = sh_x >= 0 ? sh_x : sh_last;
@@ -422,7 +514,12 @@ __global__ void __launch_bounds__(256) select_kernel(RowJob j, int seg, int nseg
     if (!resid) {
       const size_t q = (size_t)row * j.gamma + (j.k - 1);
       o.tokens[q] = x;
-      if (o.logp) o.logp[q] = draft_logit<UDT, WDT>(j, ri, x) - sh_M - sh_lz;
+      if (o.logp) {
+        const int zv0 = sh_zv0;
+        const float zx = (zv0 >= 0 && x >= zv0 && x < zv0 + 64) ? zs[x - zv0]
+                                                                : draft_logit<UDT, WDT>(j, ri, x);
+        o.logp[q] = zx - sh_M - sh_lz;
+      }
       if (o.stats) {
         o.stats[2 * q] = sh_M;
         o.stats[2 * q + 1] = sh_lz;
