@@ -81,7 +81,7 @@ size_t partial_entries(int op, int R, int gamma, int V, int rank) {
   size_t e = 0;
   switch (op) {
     case SPEC_OP_PROPOSE: e = (size_t)R * seg_draft; break;
-    case SPEC_OP_VERIFY_GREEDY: e = tgt; break;
+    case SPEC_OP_VERIFY_GREEDY: e = tr; break;
     case SPEC_OP_TARGET_STATS: e = tgt; break;
     case SPEC_OP_VERIFY_REJECTION: e = tgt > (size_t)R * seg_draft ? tgt : (size_t)R * seg_draft; break;
     case SPEC_OP_TV_CONFIDENCE: e = tgt > dr * seg_draft ? tgt : dr * seg_draft; break;
@@ -198,10 +198,7 @@ void target_stats_pass(const void* target, int dtype, float scale, int R, int ga
   j.T = target;
   j.lengths = lengths;
   j.status = w.status;
-  const int nseg = stream_nseg(V);
-  launch_stream_partials(j, dtype, kStreamSeg, nseg, vec_ok(target, nullptr, dtype, V), true,
-                         false, w.pm, w.ps, w.pi, grid_for((long long)j.rows * nseg, 1), s);
-  launch_finalize_stats(j.rows, nseg, w.pm, w.ps, out, lengths, gamma + 1, w.status, s);
+  launch_row_stats(j, dtype, vec_ok(target, nullptr, dtype, V), out, nullptr, s);
 }
 
 }  // namespace
@@ -358,11 +355,9 @@ int spec_verify_greedy(const void* target, int t_dtype, const int32_t* draft_tok
   j.T = target;
   j.lengths = lengths;
   j.status = w.status;
-  const int nseg = stream_nseg(V);
-  launch_stream_partials(j, t_dtype, kStreamSeg, nseg, vec_ok(target, nullptr, t_dtype, V), false,
-                         true, w.pm, nullptr, w.pi, grid_for((long long)j.rows * nseg, 1), s);
-  launch_greedy_scan(R, gamma, V, nseg, w.pm, w.pi, draft_tokens, lengths, accept_len, out_tokens,
-                     next_anchor, w.status, s);
+  launch_row_stats(j, t_dtype, vec_ok(target, nullptr, t_dtype, V), nullptr, w.pi, s);
+  launch_greedy_scan(R, gamma, w.pi, draft_tokens, lengths, accept_len, out_tokens, next_anchor,
+                     w.status, s);
   return finish();
 }
 

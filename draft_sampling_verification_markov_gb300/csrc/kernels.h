@@ -35,10 +35,12 @@ void launch_select(const RowJob& j, int udt, int wdt, int seg, int nseg, const f
 void launch_finalize_stats(int rows, int nseg, const float* pm, const float* ps, float* stats,
                            const int32_t* lengths, int rows_per_req, uint32_t* status,
                            cudaStream_t s);
-void launch_greedy_scan(int R, int gamma, int V, int nseg, const float* pm, const int* pi,
-                        const int32_t* tokens, const int32_t* lengths, int32_t* accept_len,
-                        int32_t* out_tokens, int32_t* next_anchor, uint32_t* status,
-                        cudaStream_t s);
+void launch_greedy_scan(int R, int gamma, const int* amax, const int32_t* tokens,
+                        const int32_t* lengths, int32_t* accept_len, int32_t* out_tokens,
+                        int32_t* next_anchor, uint32_t* status, cudaStream_t s);
+// Per-row (m, log Z) and/or first argmax of target rows (MAP_TARGET job), one block per row.
+void launch_row_stats(const RowJob& j, int dtype, bool vec, float* stats, int* argmax,
+                      cudaStream_t s);
 void launch_accept(int dtype, int R, int gamma, int V, float scale, const void* T,
                    const float* tstats, const int32_t* tokens, const float* dlogp,
                    const float* u_accept, const int32_t* lengths, int32_t* final_n,

@@ -3,24 +3,29 @@
 // DSpark", section 4 "Markov Head": B(x_{k-1}, .) = W1[x_{k-1}] W2 added to the base logits,
 // section 3 softmax; section 5 TV label; the residual of rejection sampling).
 //
-// One tile = 128 rows (requests, TMEM lanes) x BN vocabulary columns, K = rank (<= 256).
+// One tile = 128 rows (requests, TMEM lanes) x N vocabulary columns (N = 128 for softmax
+// partials, 64 for the TV / residual passes), K = rank (<= 256, a multiple of 64).
 //   A  [128 x rank] bf16: the W1 rows of each row's previous token, gathered by the epilogue
-//      warps into shared memory in the 128-byte-swizzled K-major layout (once per row block).
-//   B  [BN x rank] bf16: W2 rows (W2 stored [V, rank], K-major) by TMA, kept in L2 with an
-//      evict-last policy (every row block and every draft position reads all of W2).
-//   D  [128 x BN] fp32 in tensor memory, two stages, read back with tcgen05.ld by the epilogue.
-//   U / T tiles: the base-logit (and target) rows of the same 128 rows x BN columns, by TMA
-//      with an evict-first policy (read once); when the rows of a tile are not equally spaced
-//      (the final rows of rejection verification) each epilogue thread loads its own row
-//      segment with 16-byte loads issued before it waits for the accumulator.
+//      warps and stored into tensor memory with tcgen05.st (lane = row, two bf16 of K per
+//      32-bit column), once per row block; the MMA reads A from tensor memory.
+//   B  [N x rank] bf16: W2 rows (W2 stored [V, rank], K-major) by TMA, one whole tile per
+//      pipeline stage, kept in L2 with an evict-last policy and prefetched two tiles ahead.
+//   D  [128 x N] fp32 in tensor memory, two stages, read back with tcgen05.ld.
+//   U / T tiles: the base-logit (and target) rows of the tile, by TMA with an evict-first
+//      policy (read once), 64-column boxes in the 128-byte-swizzled layout; rows that are not
+//      equally spaced (the final rows of rejection verification) come four at a time with
+//      tile::gather4 into the same layout.
+// The logit stream starts only once the first A block is in tensor memory, so that the W1
+// row gather is not queued behind it. The single MMA-issuing thread is the critical resource
+// (each mbarrier wait and tcgen05.commit costs it ~0.1 us), hence N = 128 instructions and
+// whole-tile B stages: it waits twice and commits twice per tile.
 // Warp roles (352 threads, one CTA per SM, persistent over a contiguous range of tiles):
 //   warp 0  W2 (B operand) TMA producer;  warp 1  TMEM allocator + single-thread MMA issuer;
-//   warp 2  U / T tile producer (decoupled from the B ring so logit rows stream ahead);
-//   warps 3..10  epilogue: warp w reads TMEM lanes 32*(w%4).. and column half (w-3)/4.
-// Epilogues (per row, per 64-column segment):
+//   warp 2  U / T tile producer;  warps 3..10  epilogue: warp w reads TMEM lanes 32*(w%4)..
+//   and column half (w-3)/4 of the tile.
+// Epilogues (per row, per N/2-column half tile, one partial each):
 //   MODE_STATS  z = (U + bias) * scale -> (max z, sum exp(z - max), first argmax);
-//   MODE_TV     sum min(p_d, p_t);    MODE_RESID  sum max(0, p_t - p_d) (p_t on bonus rows);
-//   these two write one partial per row and 32-column half (markov_tc_seg).
+//   MODE_TV     sum min(p_d, p_t);    MODE_RESID  sum max(0, p_t - p_d) (p_t on bonus rows).
 // Every mbarrier wait is bounded (about a second); on expiry the CTA sets SPEC_DEV_TIMEOUT,
 // drains its own copies and MMAs, frees its tensor memory and returns.
 #include <cuda.h>
@@ -33,22 +38,29 @@
 namespace spec {
 namespace tc {
 
-constexpr int kBM = 128;
+constexpr int kBM = 128;                            // rows per tile (one MMA, 128 TMEM lanes)
 constexpr int kEpiWarps = 8;
 constexpr int kFirstEpi = 3;                       // warps 0..2: B producer, MMA, U/T producer
 constexpr int kThreads = (kFirstEpi + kEpiWarps) * 32;
 constexpr long long kSpinCycles = 4000000000LL;  // ~2 s at the maximum SM clock
-constexpr uint32_t kAtomBytes = kBM * 128;       // 128 rows x 128 B (64 bf16 of K)
+constexpr uint32_t kBoxBytes = kBM * 128;         // one TMA box: 128 rows x 64 columns (bf16)
 
-// BN = 128 (softmax partials, U only): A 64 KB + B 4 x 16 KB + U 3 x 32 KB = 224 KB.
-// BN = 64 (TV / residual, U and T): A 64 KB + B 6 x 8 KB + (U + T) 3 x 2 x 18 KB = 220 KB.
-template <int BN>
+// Per pass mode. Shared memory (A lives in tensor memory); a B stage holds a whole tile of W2 so
+// that the single MMA-issuing thread waits once and commits twice per tile:
+//   MODE_STATS: N = 128: B 2 x 64 KB + U 3 x 32 KB          = 224 KB; TMEM 2 x 128 + 128 cols
+//   MODE_TV / MODE_RESID: N = 64: B 3 x 32 KB + (U + T) 3 x 2 x 16 KB = 192 KB; TMEM 2 x 64 + 128
+template <int MODE>
 struct Cfg {
-  static constexpr int kBStages = BN == 128 ? 4 : 6;
+  static constexpr int kBN = MODE == MODE_STATS ? 128 : 64;  // vocabulary columns per tile
+  static constexpr int kBoxes = kBN / 64;                     // 64-column boxes per logit tile
+  static constexpr uint32_t kBAtomBytes = kBN * 128;          // kBN W2 rows x 64 K
+  static constexpr uint32_t kBStageBytes = 4 * kBAtomBytes;   // K <= 256
+  static constexpr int kBStages = MODE == MODE_STATS ? 2 : 3;
+  static constexpr uint32_t kTileBytes = kBoxes * kBoxBytes;
   static constexpr int kUStages = 3;
-  static constexpr uint32_t kBStageBytes = BN * 128;
-  static constexpr uint32_t kRowPitch = BN * 2 + 16;  // gathered rows (pair modes only)
-  static constexpr uint32_t kTileBytes = BN == 128 ? kBM * BN * 2 : kBM * kRowPitch;
+  static constexpr int kAccCols = 2 * kBN;                    // two accumulator stages
+  static constexpr int kTmemCols = MODE == MODE_STATS ? 512 : 256;
+  static constexpr int kSeg = kBN / 2;                        // columns per epilogue warp / partial
 };
 
 // ------------------------------------------------------------------------------ PTX wrappers
@@ -128,6 +140,29 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+// Prefetch a tile of a 2-D tensor into L2 (no shared-memory destination).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int c0, int c1,
+                                                uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.prefetch.tensor.2d.L2.global.tile.L2::cache_hint [%0, {%1, %2}], %3;" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(c0), "r"(c1), "l"(policy)
+      : "memory");
+}
+
+// Four rows (r0..r3) x 64 columns of a 2-D tensor whose box is one row high, into 512
+// consecutive bytes of shared memory (swizzled by address like a 4-row box).
+__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, int c0, int r0,
+                                            int r1, int r2, int r3, uint64_t* bar,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
+      "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1,
                                             int c2, uint64_t* bar, uint64_t policy) {
   asm volatile(
@@ -170,6 +205,32 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+
+// D (+)= A x B^T with A read from tensor memory (lane = row, K packed two bf16 per column).
+__device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// 16 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
@@ -281,11 +342,10 @@ __device__ __forceinline__ void unpack_bf16x8(uint4 w, float* x) {
 // ------------------------------------------------------------------------------ tiles
 
 struct Tiles {
-  int n_mt, n_nt;  // row blocks and column tiles
+  int n_mt, n_nt;  // row blocks (128 rows) and column tiles
   int rb;          // row blocks per draft position (MAP_ALL_POS)
 };
 
-// Row m of the pass for lane row i of row block mt, and its request / position.
 struct TileRow {
   int valid;
   int r;
@@ -293,6 +353,7 @@ struct TileRow {
   int prow;   // partial row index in the pass
 };
 
+// Row `i` (0..127) of row block mt.
 __device__ __forceinline__ TileRow tile_row(const RowJob& j, const Tiles& t, int mt, int i) {
   TileRow o;
   if (j.map == MAP_ALL_POS) {
@@ -318,12 +379,13 @@ struct TcParams {
   int* pi;
 };
 
-template <int BN, int MODE, bool ARGMAX, bool GATHER>
+template <int MODE, bool ARGMAX, bool GATHER>
 __global__ void __launch_bounds__(kThreads, 1)
     markov_tc_kernel(const __grid_constant__ CUtensorMap map_w2,
                      const __grid_constant__ CUtensorMap map_u,
                      const __grid_constant__ CUtensorMap map_t, const TcParams P) {
-  using C = Cfg<BN>;
+  using C = Cfg<MODE>;
+  constexpr int BN = C::kBN;
   constexpr int KB = C::kBStages, KU = C::kUStages;
   constexpr bool kPair = MODE != MODE_STATS;  // needs target tiles
   constexpr int kHalf = BN / 2;               // columns per epilogue warp
@@ -333,8 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const RowJob& j = P.j;
   const int ka_n = j.rank / 64;
-  unsigned char* sA = smem;                                         // ka_n atoms
-  unsigned char* sB = sA + 4 * kAtomBytes;                          // KB stages
+  unsigned char* sB = smem;                                         // KB stages
   unsigned char* sU = sB + KB * C::kBStageBytes;                    // KU stages
   unsigned char* sT = sU + KU * C::kTileBytes;                      // KU stages (pair modes)
   unsigned char* tail = sT + (kPair ? KU * C::kTileBytes : 0);
@@ -380,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(tmem_slot)),
-                 "r"(2 * BN < 32 ? 32 : 2 * BN)
+                 "r"(C::kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -395,28 +456,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     int bs = 0;
     uint32_t bph = 0;
     bool ok = true;
+    constexpr int kPrefetch = 2;  // tiles ahead of the shared-memory ring, into L2
+    if (lane == 0)
+      for (long long t = t_begin; t < t_begin + kPrefetch && t < t_end; ++t)
+        for (int ka = 0; ka < ka_n; ++ka)
+          tma_prefetch_2d(&map_w2, ka * 64, (int)(t % P.t.n_nt) * BN, pol_keep);
     for (long long t = t_begin; t < t_end && ok; ++t) {
       const int n0 = (int)(t % P.t.n_nt) * BN;
-      for (int ka = 0; ka < ka_n && ok; ++ka) {
-        ok = mbar_wait(&b_empty[bs], bph ^ 1, abort, status);
-        if (ok && lane == 0) {
-          mbar_arrive_expect_tx(&b_full[bs], C::kBStageBytes);
-          tma_load_2d(sB + bs * C::kBStageBytes, &map_w2, ka * 64, n0, &b_full[bs], pol_keep);
-        }
-        if (++bs == KB) { bs = 0; bph ^= 1; }
+      if (lane == 0 && t + kPrefetch < t_end)
+        for (int ka = 0; ka < ka_n; ++ka)
+          tma_prefetch_2d(&map_w2, ka * 64, (int)((t + kPrefetch) % P.t.n_nt) * BN, pol_keep);
+      ok = mbar_wait(&b_empty[bs], bph ^ 1, abort, status);
+      if (ok && lane == 0) {
+        mbar_arrive_expect_tx(&b_full[bs], ka_n * C::kBAtomBytes);
+        for (int ka = 0; ka < ka_n; ++ka)
+          tma_load_2d(sB + bs * C::kBStageBytes + ka * C::kBAtomBytes, &map_w2, ka * 64, n0,
+                      &b_full[bs], pol_keep);
       }
+      if (++bs == KB) { bs = 0; bph ^= 1; }
     }
     // drain: every issued copy lands before the CTA moves on
     if (lane == 0)
       for (int s = 0; s < KB; ++s) mbar_drain(&b_full[s], (s < bs) ? bph : (bph ^ 1));
   } else if (warp == 2) {
     // ---------------------------------------------------------------- U / T producer
-    // (idle in gather mode: the epilogue loads the gathered final rows itself)
-    if constexpr (!GATHER) {
     const uint64_t pol_stream = policy_evict_first();
     int us = 0;
     uint32_t uph = 0;
-    bool ok = true;
+    // start streaming logit rows once the first A block is in tensor memory: the W1 gather is
+    // latency-bound and must not queue behind this stream
+    bool ok = t_begin >= t_end || mbar_wait(a_full, 0, abort, status);
     for (long long t = t_begin; t < t_end && ok; ++t) {
       const int mt = (int)(t / P.t.n_nt), nt = (int)(t % P.t.n_nt);
       const int n0 = nt * BN;
@@ -424,23 +493,45 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       unsigned char* du = sU + us * C::kTileBytes;
       unsigned char* dt = sT + us * C::kTileBytes;
-      if (lane == 0) {
-        const TileRow tr = tile_row(j, P.t, mt, 0);
-        const int r0 = tr.r, kk = tr.k - 1;
-        constexpr int nbox = BN / 64;
-        mbar_arrive_expect_tx(&u_full[us], (kPair ? 2u : 1u) * nbox * kAtomBytes);
-        for (int b = 0; b < nbox; ++b) {
-          tma_load_3d(du + b * kAtomBytes, &map_u, n0 + b * 64, kk, r0, &u_full[us], pol_stream);
-          if constexpr (kPair)
-            tma_load_3d(dt + b * kAtomBytes, &map_t, n0 + b * 64, kk, r0, &u_full[us],
-                        pol_stream);
+      if constexpr (!GATHER) {
+        if (lane == 0) {
+          const TileRow tr = tile_row(j, P.t, mt, 0);
+          const int r0 = tr.r, kk = tr.k - 1;
+          mbar_arrive_expect_tx(&u_full[us], (kPair ? 2u : 1u) * C::kTileBytes);
+          for (int b = 0; b < C::kBoxes; ++b) {
+            tma_load_3d(du + b * kBoxBytes, &map_u, n0 + b * 64, kk, r0, &u_full[us], pol_stream);
+            if constexpr (kPair)
+              tma_load_3d(dt + b * kBoxBytes, &map_t, n0 + b * 64, kk, r0, &u_full[us],
+                          pol_stream);
+          }
         }
+      } else {
+        // final rows of rejection verification, four rows per tile::gather4 (lane g loads rows
+        // 4g..4g+3); rows past R and the U rows of bonus rows point at row 0 and are ignored
+        static_assert(C::kBoxes == 1, "gathered tiles are one box wide");
+        int tr4[4], ur4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int r = mt * kBM + 4 * lane + e;
+          tr4[e] = 0;
+          ur4[e] = 0;
+          if (r < j.R) {
+            const int n = j.final_n[r];
+            tr4[e] = r * (j.gamma + 1) + n;
+            if (j.final_kind[r]) ur4[e] = r * j.gamma + n;
+          }
+        }
+        if (lane == 0) mbar_arrive_expect_tx(&u_full[us], 2u * C::kTileBytes);
+        __syncwarp();
+        tma_gather4(dt + lane * 512, &map_t, n0, tr4[0], tr4[1], tr4[2], tr4[3], &u_full[us],
+                    pol_stream);
+        tma_gather4(du + lane * 512, &map_u, n0, ur4[0], ur4[1], ur4[2], ur4[3], &u_full[us],
+                    pol_stream);
       }
       if (++us == KU) { us = 0; uph ^= 1; }
     }
     if (lane == 0)
       for (int s = 0; s < KU; ++s) mbar_drain(&u_full[s], (s < us) ? uph : (uph ^ 1));
-    }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     constexpr uint32_t idesc = idesc_bf16(kBM, BN);
@@ -461,22 +552,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ok = mbar_wait(&acc_empty[as], accph[as] ^ 1, abort, status);
         if (!ok) break;
+        ok = mbar_wait(&b_full[bs], bph, abort, status);
+        if (!ok) break;
         tc_fence_after();
         const uint32_t d = tmem + as * BN;
-        for (int ka = 0; ka < ka_n && ok; ++ka) {
-          ok = mbar_wait(&b_full[bs], bph, abort, status);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t a_base = smem_u32(sA + ka * kAtomBytes);
-          const uint32_t b_base = smem_u32(sB + bs * C::kBStageBytes);
+        for (int ka = 0; ka < ka_n; ++ka) {
+          const uint32_t b_base = smem_u32(sB + bs * C::kBStageBytes + ka * C::kBAtomBytes);
+          const uint32_t a = tmem + C::kAccCols + ka * 32;
+          // K = 16 per instruction: 8 tensor-memory columns of A, 32 bytes of a B row
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)
-            mma_bf16(d, sw128_desc(a_base + ks * 32), sw128_desc(b_base + ks * 32), idesc,
-                     (ka | ks) != 0);
-          mma_commit(&b_empty[bs]);
-          if (++bs == KB) { bs = 0; bph ^= 1; }
+            mma_bf16_ta(d, a + ks * 8, sw128_desc(b_base + ks * 32), idesc, (ka | ks) != 0);
         }
-        if (!ok) break;
+        mma_commit(&b_empty[bs]);
+        if (++bs == KB) { bs = 0; bph ^= 1; }
         mma_commit(&acc_full[as]);
         accph[as] ^= 1;
         as ^= 1;
@@ -491,10 +580,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= kFirstEpi) {
     // ---------------------------------------------------------------- epilogue
     const int ew = warp - kFirstEpi;
-    const int q = warp & 3;                       // TMEM lane quarter
-    const int h = ew >> 2;                        // column half
-    const int i = q * 32 + lane;                  // row within the tile
-    const int et = threadIdx.x - kFirstEpi * 32;  // 0..255
+    const int q = warp & 3;          // TMEM lane quarter
+    const int h = ew >> 2;           // column half
+    const int i = q * 32 + lane;     // row within the tile (TMEM lane)
     int as = 0, us = 0;
     uint32_t accph[2] = {0, 0}, uph = 0, aeph = 0;
     int cur_mt = -1;
@@ -502,6 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (long long t = t_begin; t < t_end && ok; ++t) {
       const int mt = (int)(t / P.t.n_nt), nt = (int)(t % P.t.n_nt);
       const int n0 = nt * BN;
+      const TileRow tr = tile_row(j, P.t, mt, i);
       if (mt != cur_mt) {
         if (cur_mt >= 0) {
           ok = mbar_wait(a_empty, aeph, abort, status);
@@ -509,80 +598,82 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
         }
         cur_mt = mt;
-        // gather A: row ii <- W1[prev(ii)] in the swizzled K-major layout. All loads of a
-        // thread are issued before any store so that they overlap (up to 16 x 16 B).
-        const int chunks = ka_n * 8;  // 16-byte chunks per row
-        constexpr int kMaxPer = kBM * 32 / (kEpiWarps * 32);
-        uint4 v[kMaxPer];
-#pragma unroll
-        for (int it = 0; it < kMaxPer; ++it) {
-          const int c = et + it * kEpiWarps * 32;
-          v[it] = make_uint4(0, 0, 0, 0);
-          if (c < kBM * chunks) {
-            const int ii = c / chunks, cc = c % chunks;
-            const TileRow tr = tile_row(j, P.t, mt, ii);
-            if (tr.valid) {
-              int prev;
-              if (j.map == MAP_FINAL) {
-                const int n = j.final_n[tr.r];
-                prev = n == 0 ? j.anchors[tr.r] : j.tokens[(size_t)tr.r * j.gamma + n - 1];
-              } else {
-                prev = tr.k == 1 ? j.anchors[tr.r] : j.tokens[(size_t)tr.r * j.gamma + tr.k - 2];
-              }
-              if (prev < 0 || prev >= j.V) {
-                atomicOr(status, SPEC_DEV_BAD_TOKEN);
-                prev = 0;
-              }
-              v[it] = __ldg(reinterpret_cast<const uint4*>(
-                                reinterpret_cast<const unsigned short*>(j.W1) +
-                                (size_t)prev * j.rank) +
-                            cc);
-            }
+        // gather A into tensor memory: thread (q, h) owns row i and half h of its K; one load
+        // of the previous token, then all of its W1 chunks in flight, then tcgen05.st (a bad
+        // token is flagged afterwards)
+        int prev = 0;
+        if (tr.valid) {
+          if (j.map == MAP_FINAL) {
+            const int n = j.final_n[tr.r];
+            prev = n == 0 ? j.anchors[tr.r] : j.tokens[(size_t)tr.r * j.gamma + n - 1];
+          } else {
+            prev = tr.k == 1 ? j.anchors[tr.r] : j.tokens[(size_t)tr.r * j.gamma + tr.k - 2];
           }
         }
+        const bool bad = tr.valid && (prev < 0 || prev >= j.V);
+        const int per = j.rank / 16;  // 16-byte chunks of this thread's half row (<= 16)
+        const uint4* src = reinterpret_cast<const uint4*>(
+                               reinterpret_cast<const unsigned short*>(j.W1) +
+                               (size_t)(bad ? 0 : prev) * j.rank) + h * per;
+        uint32_t w[64];
 #pragma unroll
-        for (int it = 0; it < kMaxPer; ++it) {
-          const int c = et + it * kEpiWarps * 32;
-          if (c < kBM * chunks) {
-            const int ii = c / chunks, cc = c % chunks;
-            const int ka = cc >> 3, cw = cc & 7;
-            *reinterpret_cast<uint4*>(sA + ka * kAtomBytes + ii * 128 + ((cw ^ (ii & 7)) << 4)) =
-                v[it];
-          }
+        for (int it = 0; it < 16; ++it) {
+          const uint4 v = (tr.valid && it < per) ? __ldg(src + it) : make_uint4(0, 0, 0, 0);
+          w[4 * it] = v.x;
+          w[4 * it + 1] = v.y;
+          w[4 * it + 2] = v.z;
+          w[4 * it + 3] = v.w;
         }
-        fence_async_smem();
+        // chunk c of the half holds K elements 8c..8c+7 = columns 4c..4c+3 of the half
+        const uint32_t a_addr =
+            tmem + ((uint32_t)(q * 32) << 16) + C::kAccCols + h * (j.rank / 4);
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+          if (4 * b < per) tmem_st16(a_addr + 16 * b, w + 16 * b);
+        tmem_wait_st();
+        if (bad) atomicOr(status, SPEC_DEV_BAD_TOKEN);
+        tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(a_full);
       }
-      const TileRow tr = tile_row(j, P.t, mt, i);
-      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + as * BN + h * kHalf;
       const int col0 = h * kHalf;  // first tile column of this warp
+      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + as * BN + col0;
       const bool tail = n0 + BN > j.V;
+      const bool live = tr.valid && n0 + col0 < j.V;
 
-      if constexpr (MODE == MODE_STATS) {
-        ok = mbar_wait(&acc_full[as], accph[as], abort, status);
-        if (!ok) break;
-        tc_fence_after();
-        ok = mbar_wait(&u_full[us], uph, abort, status);
-        if (!ok) break;
-        // both TMEM reads and all shared-memory reads first, then release the stages
-        uint32_t braw[64];
-        tmem_ld32_async(taddr, braw);
-        tmem_ld32_async(taddr + 32, braw + 32);
-        const uint32_t u_base = smem_u32(sU + us * C::kTileBytes);
-        uint4 uw[8];
+      ok = mbar_wait(&acc_full[as], accph[as], abort, status);
+      if (!ok) break;
+      tc_fence_after();
+      ok = mbar_wait(&u_full[us], uph, abort, status);
+      if (!ok) break;
+      // TMEM reads and shared-memory reads first, then release the stages
+      uint32_t braw[kHalf];
+      tmem_ld32_async(taddr, braw);
+      if constexpr (kHalf == 64) tmem_ld32_async(taddr + 32, braw + 32);
+      const uint32_t u_base = smem_u32(sU + us * C::kTileBytes);
+      const uint32_t t_base = smem_u32(sT + us * C::kTileBytes);
+      uint4 uw[kHalf / 8], tw[kHalf / 8];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const int cc = c, b = col0 >> 6;
-          uw[c] = lds128(u_base + b * kAtomBytes + i * 128 + ((cc ^ (i & 7)) << 4));
-        }
-        tmem_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&acc_empty[as]);
-          mbar_arrive(&u_empty[us]);
-        }
+      for (int c = 0; c < kHalf / 8; ++c) {
+        const int col = col0 + 8 * c;
+        const int b = col >> 6, cc = (col & 63) >> 3;
+        const uint32_t off = b * kBoxBytes + i * 128 + ((cc ^ (i & 7)) << 4);
+        uw[c] = lds128(u_base + off);
+        if constexpr (kPair) tw[c] = lds128(t_base + off);
+      }
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&acc_empty[as]);
+        mbar_arrive(&u_empty[us]);
+      }
+      if (++us == KU) { us = 0; uph ^= 1; }
+      accph[as] ^= 1;
+      as ^= 1;
+
+      const size_t o = (size_t)((n0 + col0) / kHalf) * j.rows + tr.prow;
+      if constexpr (MODE == MODE_STATS) {
         // z = (bias + U) * scale, two columns per instruction
         const unsigned long long sc2 = pack2(j.scale, j.scale);
         float z[64];
@@ -637,15 +728,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           s = ((acc4[0] + acc4[1]) + (acc4[2] + acc4[3])) * (1.0f - delta * kLn2);
         }
-        if (tr.valid && n0 + col0 < j.V) {
-          const size_t o = (size_t)((n0 + col0) / 64) * j.rows + tr.prow;
+        if (live) {
           P.pm[o] = m;
           P.ps[o] = s;
           if (ARGMAX) P.pi[o] = idx;
         }
-        if (++us == KU) { us = 0; uph ^= 1; }
       } else {
-        // pair modes: BN = 64, each warp half holds 32 columns (4 chunks of 8)
         Norm dn = {0.0f, 0.0f}, tn = {0.0f, 0.0f};
         bool resid = true;
         if (tr.valid) {
@@ -659,61 +747,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (resid) dn = load_norm(j.dstats, (long long)tr.r * j.gamma + n);
           }
         }
-        const bool live = tr.valid && n0 + col0 < j.V;
-        uint4 tw[4], uw[4];
-        if constexpr (GATHER) {
-          // gathered final rows: this thread loads its own row segment (issued before the
-          // wait for the accumulator so that the loads overlap it)
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            tw[c] = make_uint4(0, 0, 0, 0);
-            uw[c] = make_uint4(0, 0, 0, 0);
-          }
-          if (live) {
-            const int n = j.final_n[tr.r];
-            const uint4* trow = reinterpret_cast<const uint4*>(
-                reinterpret_cast<const unsigned short*>(j.T) +
-                ((size_t)tr.r * (j.gamma + 1) + n) * j.V + n0 + col0);
-            const uint4* urow = reinterpret_cast<const uint4*>(
-                reinterpret_cast<const unsigned short*>(j.U) +
-                ((size_t)tr.r * j.gamma + n) * j.V + n0 + col0);
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              if (n0 + col0 + 8 * c < j.V) {
-                tw[c] = ld_stream16(trow + c);
-                if (resid) uw[c] = ld_stream16(urow + c);
-              }
-            }
-          }
-        }
-        ok = mbar_wait(&acc_full[as], accph[as], abort, status);
-        if (!ok) break;
-        tc_fence_after();
-        if constexpr (!GATHER) {
-          ok = mbar_wait(&u_full[us], uph, abort, status);
-          if (!ok) break;
-          const uint32_t u_base = smem_u32(sU + us * C::kTileBytes);
-          const uint32_t t_base = smem_u32(sT + us * C::kTileBytes);
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const int cc = (col0 >> 3) + c;
-            const uint32_t off = i * 128 + ((cc ^ (i & 7)) << 4);
-            tw[c] = lds128(t_base + off);
-            uw[c] = lds128(u_base + off);
-          }
-        }
-        float b[32];
-        tmem_ld32(taddr, b);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&acc_empty[as]);
-          if constexpr (!GATHER) mbar_arrive(&u_empty[us]);
-        }
-        float sum = 0.0f;
         if (live) {
+          float sum = 0.0f;
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < kHalf / 8; ++c) {
             float u[8], tv[8];
             unpack_bf16x8(tw[c], tv);
             unpack_bf16x8(uw[c], u);
@@ -726,19 +763,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 sum += pt;
                 continue;
               }
-              const float pd = prob_of((u[e] + b[c * 8 + e]) * j.scale, dn);
+              const float pd = prob_of((u[e] + __uint_as_float(braw[c * 8 + e])) * j.scale, dn);
               sum += MODE == MODE_RESID ? fmaxf(pt - pd, 0.0f) : fminf(pt, pd);
             }
           }
-          // one partial per row and 32-column half
-          P.ps[(size_t)((n0 + col0) / 32) * j.rows + tr.prow] = sum;
-        }
-        if constexpr (!GATHER) {
-          if (++us == KU) { us = 0; uph ^= 1; }
+          P.ps[o] = sum;
         }
       }
-      accph[as] ^= 1;
-      as ^= 1;
     }
   }
 
@@ -747,7 +778,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                 "r"(2 * BN < 32 ? 32 : 2 * BN)
+                 "r"(C::kTmemCols)
                  : "memory");
   }
 }
@@ -783,18 +814,18 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN>
-size_t smem_bytes(bool pair) {
-  using C = Cfg<BN>;
-  return 1024 + 4 * kAtomBytes + C::kBStages * C::kBStageBytes +
-         (pair ? 2 : 1) * C::kUStages * C::kTileBytes + 512;
+template <int MODE>
+size_t smem_bytes() {
+  using C = Cfg<MODE>;
+  return 1024 + C::kBStages * C::kBStageBytes +
+         (MODE != MODE_STATS ? 2 : 1) * C::kUStages * C::kTileBytes + 512;
 }
 
-template <int BN, int MODE, bool ARGMAX, bool GATHER>
+template <int MODE, bool ARGMAX, bool GATHER>
 cudaError_t launch_t(const TcParams& p, const CUtensorMap& w2, const CUtensorMap& u,
                      const CUtensorMap& t, int grid, cudaStream_t s) {
-  const size_t smem = smem_bytes<BN>(MODE != MODE_STATS);
-  auto k = markov_tc_kernel<BN, MODE, ARGMAX, GATHER>;
+  const size_t smem = smem_bytes<MODE>();
+  auto k = markov_tc_kernel<MODE, ARGMAX, GATHER>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   k<<<grid, kThreads, smem, s>>>(w2, u, t, p);
@@ -824,7 +855,7 @@ cudaError_t launch_markov_tc(const RowJob& j, float* pm, float* ps, int* pi, boo
   using namespace tc;
   TraceScope ts(SPEC_KCLASS_MARKOV, s);
   const bool pair = j.mode != MODE_STATS;
-  const int BN = pair ? 64 : 128;
+  const int BN = pair ? Cfg<MODE_TV>::kBN : Cfg<MODE_STATS>::kBN;
   TcParams p;
   p.j = j;
   p.pm = pm;
@@ -858,13 +889,21 @@ cudaError_t launch_markov_tc(const RowJob& j, float* pm, float* ps, int* pi, boo
       const cuuint64_t st[2] = {(cuuint64_t)j.V * 2, (cuuint64_t)j.V * 2 * (j.gamma + 1)};
       if (!make_map(&t, j.T, 3, dt, st, box)) return cudaErrorInvalidValue;
     }
+  } else {
+    // rows gathered four at a time: 2-D maps over all rows, boxes one row high
+    const cuuint32_t box[2] = {64, 1};
+    const cuuint64_t du[2] = {(cuuint64_t)j.V, (cuuint64_t)j.R * j.gamma};
+    const cuuint64_t dt[2] = {(cuuint64_t)j.V, (cuuint64_t)j.R * (j.gamma + 1)};
+    const cuuint64_t sv[1] = {(cuuint64_t)j.V * 2};
+    if (!make_map(&u, j.U, 2, du, sv, box)) return cudaErrorInvalidValue;
+    if (!make_map(&t, j.T, 2, dt, sv, box)) return cudaErrorInvalidValue;
   }
   if (j.mode == MODE_STATS) {
-    if (argmax) return launch_t<128, MODE_STATS, true, false>(p, w2, u, t, grid, s);
-    return launch_t<128, MODE_STATS, false, false>(p, w2, u, t, grid, s);
+    if (argmax) return launch_t<MODE_STATS, true, false>(p, w2, u, t, grid, s);
+    return launch_t<MODE_STATS, false, false>(p, w2, u, t, grid, s);
   }
-  if (j.mode == MODE_TV) return launch_t<64, MODE_TV, false, false>(p, w2, u, t, grid, s);
-  return launch_t<64, MODE_RESID, false, true>(p, w2, u, t, grid, s);
+  if (j.mode == MODE_TV) return launch_t<MODE_TV, false, false>(p, w2, u, t, grid, s);
+  return launch_t<MODE_RESID, false, true>(p, w2, u, t, grid, s);
 }
 
 }  // namespace spec

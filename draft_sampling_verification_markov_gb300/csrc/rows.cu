@@ -187,6 +187,143 @@ __global__ void __launch_bounds__(256) stream_partials_kernel(RowJob j, int seg,
   }
 }
 
+// Per-row softmax normaliser and/or argmax of target rows, one 512-thread block per row (two
+// resident per SM): raw 16-byte words are loaded one batch ahead of the arithmetic, the maximum
+// is tracked on the raw values (the scale is positive), exp((x - max) * scale) uses packed pair
+// arithmetic, and (m, log Z) / the first argmax are written directly. Rows beyond a request's
+// verified length are skipped.
+constexpr int kRowThreads = 512;
+
+__device__ __forceinline__ unsigned long long pk2(float lo, float hi) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void upk2(unsigned long long v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ unsigned long long addx2(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ unsigned long long mulx2(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// One 16-byte word (8 values) into the running (mx, s2, idx); s2 holds two partial sums.
+template <int DT, bool STATS, bool ARGMAX>
+__device__ __forceinline__ void row_word(const float (&x)[8], int v, float c, float& mx,
+                                         unsigned long long& s2, int& idx) {
+  const float g = fmaxf(fmax3(x[0], x[1], x[2]), fmax3(fmax3(x[3], x[4], x[5]), x[6], x[7]));
+  if (g > mx) {
+    if (ARGMAX) {
+#pragma unroll
+      for (int i = 7; i >= 0; --i)
+        if (x[i] == g) idx = v + i;
+    }
+    if (STATS && mx > -INFINITY) {
+      const float f = fast_exp2((mx - g) * c);
+      s2 = mulx2(s2, pk2(f, f));
+    }
+    mx = g;
+  }
+  if (STATS) {
+    const unsigned long long nm = pk2(-mx, -mx), c2 = pk2(c, c);
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) {
+      float a, b;
+      upk2(mulx2(addx2(pk2(x[i], x[i + 1]), nm), c2), a, b);
+      s2 = addx2(s2, pk2(fast_exp2(a), fast_exp2(b)));
+    }
+  }
+}
+
+template <int DT>
+__device__ __forceinline__ void unpack_word(const uint4& q, float (&x)[8]) {
+  if constexpr (DT == SPEC_BF16) {
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      x[2 * i] = __uint_as_float(w[i] << 16);
+      x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+  }
+}
+
+template <int DT, bool STATS, bool ARGMAX>
+__global__ void __launch_bounds__(kRowThreads, 2) row_stats_kernel(RowJob j, bool vec, float* stats,
+                                                                   int* argmax) {
+  const int row = blockIdx.x;
+  const RowInfo ri = row_info(j, row);
+  if (!ri.active) return;
+  const size_t off = (size_t)ri.trow * j.V;
+  const float c = j.scale * kLog2e;
+  float mx = -INFINITY;
+  unsigned long long s2 = pk2(0.0f, 0.0f);
+  int idx = 0x7fffffff;
+  if (DT == SPEC_BF16 && vec) {
+    // vector path: words w = tid + k * blockDim, kBatch words per batch, next batch in flight
+    const uint4* p = reinterpret_cast<const uint4*>(reinterpret_cast<const unsigned short*>(j.T) + off);
+    const int nw = j.V / 8;
+    const int stride = kBatch * kRowThreads;
+    uint4 cur[kBatch], nxt[kBatch];
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int w = threadIdx.x + b * kRowThreads;
+      cur[b] = w < nw ? ld_stream16(p + w) : make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
+    }
+    for (int w0 = threadIdx.x; w0 < nw; w0 += stride) {
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        const int w = w0 + stride + b * kRowThreads;
+        nxt[b] = w < nw ? ld_stream16(p + w) : make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
+      }
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        float x[8];
+        unpack_word<DT>(cur[b], x);  // padding words decode to -inf
+        row_word<DT, STATS, ARGMAX>(x, (w0 + b * kRowThreads) * 8, c, mx, s2, idx);
+      }
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) cur[b] = nxt[b];
+    }
+  } else {
+    for (int v = threadIdx.x * 8; v < j.V; v += kRowThreads * 8) {
+      float x[8];
+      load8<DT>(j.T, off, v, j.V, false, x);
+      row_word<DT, STATS, ARGMAX>(x, v, c, mx, s2, idx);
+    }
+  }
+  float sa, sb;
+  upk2(s2, sa, sb);
+  // merge in the scaled domain: (m = max * scale, s)
+  StatsAcc a = {mx > -INFINITY ? __fmul_rn(mx, j.scale) : -INFINITY, sa + sb, idx};
+  a = block_merge(a);
+  if (threadIdx.x == 0) {
+    if (STATS) {
+      if (!(a.s > 0.0f) || !isfinite(a.s) || !(a.m > -INFINITY)) atomicOr(j.status, SPEC_DEV_NONFINITE);
+      stats[2 * (size_t)row] = a.m;
+      stats[2 * (size_t)row + 1] = logf(a.s);
+    }
+    if (ARGMAX) {
+      int x = a.idx;
+      if (x < 0 || x >= j.V) {
+        atomicOr(j.status, SPEC_DEV_NONFINITE);
+        x = 0;
+      }
+      argmax[row] = x;
+    }
+  }
+}
+
 // ------------------------------------------------------------------------------ generic Markov producer
 
 // One warp per (row, 64-column chunk); lane l handles columns c*64 + l and c*64 + 32 + l.
@@ -295,13 +432,26 @@ __device__ void segment_logits(const RowJob& j, const RowInfo& ri, int v0, int n
           reinterpret_cast<const unsigned short*>(j.W1) + (size_t)ri.prev * j.rank);
       const uint4* w2 = reinterpret_cast<const uint4*>(
           reinterpret_cast<const unsigned short*>(j.W2) + (size_t)v * j.rank);
-      for (int c = part; c < j.rank / 8; c += tpc) {
-        const uint4 a = __ldg(w1 + c), b = __ldg(w2 + c);
-        const uint32_t aa[4] = {a.x, a.y, a.z, a.w}, bb[4] = {b.x, b.y, b.z, b.w};
+      const int nc = j.rank / 8;  // 16-byte chunks per weight row
+      for (int c0 = part; c0 < nc; c0 += 8 * tpc) {
+        // up to 8 chunk pairs per thread in flight before any arithmetic
+        uint4 a[8], b[8];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          acc = fmaf(__uint_as_float(aa[e] << 16), __uint_as_float(bb[e] << 16), acc);
-          acc = fmaf(__uint_as_float(aa[e] & 0xffff0000u), __uint_as_float(bb[e] & 0xffff0000u), acc);
+        for (int q = 0; q < 8; ++q) {
+          const int c = c0 + q * tpc;
+          a[q] = c < nc ? __ldg(w1 + c) : make_uint4(0, 0, 0, 0);
+          b[q] = c < nc ? __ldg(w2 + c) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const uint32_t aa[4] = {a[q].x, a[q].y, a[q].z, a[q].w};
+          const uint32_t bb[4] = {b[q].x, b[q].y, b[q].z, b[q].w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            acc = fmaf(__uint_as_float(aa[e] << 16), __uint_as_float(bb[e] << 16), acc);
+            acc = fmaf(__uint_as_float(aa[e] & 0xffff0000u), __uint_as_float(bb[e] & 0xffff0000u),
+                       acc);
+          }
         }
       }
     }
@@ -336,29 +486,58 @@ __global__ void __launch_bounds__(256) select_kernel(RowJob j, int seg, int nseg
   const RowInfo ri = row_info(j, row);
   const int tid = threadIdx.x;
   const bool resid = o.kind == 1;
+  const float u_row = (o.greedy && !resid) ? 0.0f : o.uni[(size_t)row * o.uni_stride + o.uni_offset];
   const bool markov = resid ? (ri.resid && j.rank > 0) : j.rank > 0;
   const bool need_z = j.rank > 0 && (!resid || ri.resid);
 
   // 1. normaliser from the partials (a contiguous run of segments per thread)
   const int run = (nseg + blockDim.x - 1) / blockDim.x;
   const int c0 = min(nseg, tid * run), c1 = min(nseg, c0 + run);
+  // the run's partials are loaded together (one memory round trip), kRun at a time
+  constexpr int kRun = 16;
   float M = -INFINITY;
   int gidx = 0x7fffffff;
   if (!resid) {
     StatsAcc a = stats_empty();
-    for (int c = c0; c < c1; ++c) {
-      const size_t q = (size_t)c * j.rows + row;
-      a = stats_merge(a, {pm[q], ps[q], pi ? pi[q] : 0x7fffffff});
+    for (int cb = c0; cb < c1; cb += kRun) {
+      float lm[kRun], ls[kRun];
+      int li[kRun];
+#pragma unroll
+      for (int k = 0; k < kRun; ++k) {
+        const int c = cb + k;
+        lm[k] = -INFINITY;
+        ls[k] = 0.0f;
+        li[k] = 0x7fffffff;
+        if (c < c1) {
+          const size_t q = (size_t)c * j.rows + row;
+          lm[k] = pm[q];
+          ls[k] = ps[q];
+          if (pi) li[k] = pi[q];
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < kRun; ++k) a = stats_merge(a, {lm[k], ls[k], li[k]});
     }
     a = block_merge(a);
     M = a.m;
     gidx = a.idx;
   }
-  double local = 0.0;
-  for (int c = c0; c < c1; ++c) {
-    const size_t q = (size_t)c * j.rows + row;
-    local += resid ? (double)ps[q] : (ps[q] == 0.0f ? 0.0 : (double)(ps[q] * exp_shift(pm[q], M)));
+  float localf = 0.0f;  // a thread's run is short: fp32 here, fp64 only across threads
+  for (int cb = c0; cb < c1; cb += kRun) {
+    float w[kRun];
+#pragma unroll
+    for (int k = 0; k < kRun; ++k) {
+      const int c = cb + k;
+      w[k] = 0.0f;
+      if (c < c1) {
+        const size_t q = (size_t)c * j.rows + row;
+        w[k] = resid ? ps[q] : (ps[q] == 0.0f ? 0.0f : ps[q] * exp_shift(pm[q], M));
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kRun; ++k) localf += w[k];
   }
+  const double local = (double)localf;
   double Z;
   const double before = block_exscan_d(local, &Z);
   if (tid == 0) {
@@ -389,15 +568,14 @@ __global__ void __launch_bounds__(256) select_kernel(RowJob j, int seg, int nseg
     }
   } else {
     // 2. crossing segment for t = u * Z
-    const double t = (double)o.uni[(size_t)row * o.uni_stride + o.uni_offset] * Z;
+    const double t = (double)u_row * Z;
     if (before <= t && before + local > t) {
       double cum = before;
       int lastc = -1;
       double lastw = 0.0;
       for (int c = c0; c < c1; ++c) {
         const size_t q = (size_t)c * j.rows + row;
-        const double w = resid ? (double)ps[q]
-                               : (ps[q] == 0.0f ? 0.0 : (double)(ps[q] * exp_shift(pm[q], M)));
+        const double w = (double)(resid ? ps[q] : (ps[q] == 0.0f ? 0.0f : ps[q] * exp_shift(pm[q], M)));
         if (cum + w > t) {
           lastc = c;
           lastw = t - cum;
@@ -559,14 +737,12 @@ __global__ void finalize_stats_kernel(int rows, int nseg, const float* pm, const
   }
 }
 
-// Greedy longest-prefix match + bonus, one thread per request, from target argmax partials.
-__global__ void greedy_scan_kernel(int R, int gamma, int V, int nseg, const float* pm,
-                                   const int* pi, const int32_t* tokens, const int32_t* lengths,
-                                   int32_t* accept_len, int32_t* out_tokens,
-                                   int32_t* next_anchor, uint32_t* status) {
+// Greedy longest-prefix match + bonus, one thread per request, from per-row target argmaxes.
+__global__ void greedy_scan_kernel(int R, int gamma, const int* amax, const int32_t* tokens,
+                                   const int32_t* lengths, int32_t* accept_len,
+                                   int32_t* out_tokens, int32_t* next_anchor, uint32_t* status) {
   const int r = blockIdx.x * blockDim.x + threadIdx.x;
   if (r >= R) return;
-  const int rows = R * (gamma + 1);
   int l = gamma;
   if (lengths) {
     l = lengths[r];
@@ -577,21 +753,7 @@ __global__ void greedy_scan_kernel(int R, int gamma, int V, int nseg, const floa
   }
   int n = 0, y = 0;
   for (int i = 0; i <= l; ++i) {
-    const int row = r * (gamma + 1) + i;
-    float best = -INFINITY;
-    int idx = -1;
-    for (int c = 0; c < nseg; ++c) {
-      const float m = pm[(size_t)c * rows + row];
-      if (m > best) {
-        best = m;
-        idx = pi[(size_t)c * rows + row];
-      }
-    }
-    if (idx < 0 || idx >= V) {
-      atomicOr(status, SPEC_DEV_NONFINITE);
-      idx = 0;
-    }
-    y = idx;
+    y = amax[(size_t)r * (gamma + 1) + i];
     if (i == l || tokens[(size_t)r * gamma + i] != y) break;
     n = i + 1;
   }
@@ -604,45 +766,55 @@ __global__ void greedy_scan_kernel(int R, int gamma, int V, int nseg, const floa
   if (next_anchor) next_anchor[r] = y;
 }
 
-// Rejection-sampling acceptance scan, one thread per request. Accept x_k iff
-// u_accept * p_d(x_k) < p_t,k-1(x_k); records n_r and whether the final token is a residual
-// draw (rejection) or a bonus draw (all l accepted).
+// Rejection-sampling acceptance scan, one warp per request: lane k tests position k+1
+// (accept x_k iff u_accept * p_d(x_k) < p_t,k-1(x_k); the tests are independent), and n_r is
+// the first failing position. Records n_r and whether the final token is a residual draw
+// (a rejection) or a bonus draw (all l accepted).
 template <int DT>
 __global__ void accept_kernel(int R, int gamma, int V, float scale, const void* T,
                               const float* tstats, const int32_t* tokens, const float* dlogp,
                               const float* u_accept, const int32_t* lengths, int32_t* final_n,
                               int32_t* final_kind, int32_t* accept_len, int32_t* out_tokens,
                               uint32_t* status) {
-  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  const int lane = threadIdx.x & 31;
+  const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (r >= R) return;
   int l = gamma;
   if (lengths) {
     l = lengths[r];
     if (l < 0 || l > gamma) {
-      atomicOr(status, SPEC_DEV_BAD_LENGTH);
+      if (lane == 0) atomicOr(status, SPEC_DEV_BAD_LENGTH);
       l = l < 0 ? 0 : gamma;
     }
   }
-  int n = 0;
-  for (int k = 1; k <= l; ++k) {
-    int x = tokens[(size_t)r * gamma + k - 1];
-    if (x < 0 || x >= V) {
-      atomicOr(status, SPEC_DEV_BAD_TOKEN);
-      break;  // an invalid proposal is rejected
+  int n = l;
+  for (int k0 = 0; k0 < l && n == l; k0 += 32) {
+    const int k = k0 + lane;  // tests position k + 1
+    bool reject = false;
+    if (k < l) {
+      const int x = tokens[(size_t)r * gamma + k];
+      if (x < 0 || x >= V) {
+        atomicOr(status, SPEC_DEV_BAD_TOKEN);
+        reject = true;  // an invalid proposal is rejected
+      } else {
+        const long long trow = (long long)r * (gamma + 1) + k;
+        const float t = __fmul_rn(ld_elem<DT>(T, (size_t)trow * V + x), scale);
+        const float pt = prob_of(t, load_norm(tstats, trow));
+        const float pd = fast_exp2(dlogp[(size_t)r * gamma + k] * kLog2e);  // exp(log p_d)
+        reject = !(u_accept[(size_t)r * gamma + k] * pd < pt);
+      }
     }
-    const long long trow = (long long)r * (gamma + 1) + (k - 1);
-    const float t = __fmul_rn(ld_elem<DT>(T, (size_t)trow * V + x), scale);
-    const float pt = prob_of(t, load_norm(tstats, trow));
-    const float pd = fast_exp2(dlogp[(size_t)r * gamma + k - 1] * kLog2e);  // exp(log p_d)
-    if (!(u_accept[(size_t)r * gamma + k - 1] * pd < pt)) break;
-    n = k;
+    const unsigned m = __ballot_sync(0xffffffffu, reject);
+    if (m) n = k0 + __ffs(m) - 1;
   }
-  final_n[r] = n;
-  final_kind[r] = n < l ? 1 : 0;
-  accept_len[r] = n;
+  if (lane == 0) {
+    final_n[r] = n;
+    final_kind[r] = n < l ? 1 : 0;
+    accept_len[r] = n;
+  }
   if (out_tokens) {
     int32_t* o = out_tokens + (size_t)r * (gamma + 1);
-    for (int i = 0; i <= gamma; ++i) o[i] = i < n ? tokens[(size_t)r * gamma + i] : -1;
+    for (int i = lane; i <= gamma; i += 32) o[i] = i < n ? tokens[(size_t)r * gamma + i] : -1;
   }
 }
 
@@ -699,6 +871,22 @@ void launch_ffma_t(const RowJob& j, int nseg, bool argmax, float* pm, float* ps,
 }
 }  // namespace
 
+void launch_row_stats(const RowJob& j, int dtype, bool vec, float* stats, int* argmax,
+                      cudaStream_t s) {
+  TraceScope ts(SPEC_KCLASS_STREAM, s);
+  if (j.rows == 0) return;
+  const bool st = stats != nullptr, am = argmax != nullptr;
+  if (dtype == SPEC_BF16) {
+    if (st && am) row_stats_kernel<SPEC_BF16, true, true><<<j.rows, kRowThreads, 0, s>>>(j, vec, stats, argmax);
+    else if (st) row_stats_kernel<SPEC_BF16, true, false><<<j.rows, kRowThreads, 0, s>>>(j, vec, stats, argmax);
+    else row_stats_kernel<SPEC_BF16, false, true><<<j.rows, kRowThreads, 0, s>>>(j, vec, stats, argmax);
+  } else {
+    if (st && am) row_stats_kernel<SPEC_F32, true, true><<<j.rows, kRowThreads, 0, s>>>(j, vec, stats, argmax);
+    else if (st) row_stats_kernel<SPEC_F32, true, false><<<j.rows, kRowThreads, 0, s>>>(j, vec, stats, argmax);
+    else row_stats_kernel<SPEC_F32, false, true><<<j.rows, kRowThreads, 0, s>>>(j, vec, stats, argmax);
+  }
+}
+
 void launch_stream_partials(const RowJob& j, int dtype, int seg, int nseg, bool vec, bool sum,
                             bool argmax, float* pm, float* ps, int* pi, int grid, cudaStream_t s) {
   TraceScope ts(SPEC_KCLASS_STREAM, s);
@@ -753,13 +941,12 @@ void launch_finalize_stats(int rows, int nseg, const float* pm, const float* ps,
                                                         rows_per_req, status);
 }
 
-void launch_greedy_scan(int R, int gamma, int V, int nseg, const float* pm, const int* pi,
-                        const int32_t* tokens, const int32_t* lengths, int32_t* accept_len,
-                        int32_t* out_tokens, int32_t* next_anchor, uint32_t* status,
-                        cudaStream_t s) {
+void launch_greedy_scan(int R, int gamma, const int* amax, const int32_t* tokens,
+                        const int32_t* lengths, int32_t* accept_len, int32_t* out_tokens,
+                        int32_t* next_anchor, uint32_t* status, cudaStream_t s) {
   TraceScope ts(SPEC_KCLASS_OTHER, s);
-  greedy_scan_kernel<<<(R + 127) / 128, 128, 0, s>>>(R, gamma, V, nseg, pm, pi, tokens, lengths,
-                                                     accept_len, out_tokens, next_anchor, status);
+  greedy_scan_kernel<<<(R + 127) / 128, 128, 0, s>>>(R, gamma, amax, tokens, lengths, accept_len,
+                                                     out_tokens, next_anchor, status);
 }
 
 void launch_accept(int dtype, int R, int gamma, int V, float scale, const void* T,
@@ -767,14 +954,14 @@ void launch_accept(int dtype, int R, int gamma, int V, float scale, const void* 
                    const float* u_accept, const int32_t* lengths, int32_t* final_n,
                    int32_t* final_kind, int32_t* accept_len, int32_t* out_tokens,
                    uint32_t* status, cudaStream_t s) {
-  const int grid = (R + 127) / 128;
   TraceScope ts(SPEC_KCLASS_OTHER, s);
+  const int grid = (R + 7) / 8;  // one warp per request, 8 warps per block
   if (dtype == SPEC_BF16)
-    accept_kernel<SPEC_BF16><<<grid, 128, 0, s>>>(R, gamma, V, scale, T, tstats, tokens, dlogp,
+    accept_kernel<SPEC_BF16><<<grid, 256, 0, s>>>(R, gamma, V, scale, T, tstats, tokens, dlogp,
                                                   u_accept, lengths, final_n, final_kind,
                                                   accept_len, out_tokens, status);
   else
-    accept_kernel<SPEC_F32><<<grid, 128, 0, s>>>(R, gamma, V, scale, T, tstats, tokens, dlogp,
+    accept_kernel<SPEC_F32><<<grid, 256, 0, s>>>(R, gamma, V, scale, T, tstats, tokens, dlogp,
                                                  u_accept, lengths, final_n, final_kind,
                                                  accept_len, out_tokens, status);
 }
