@@ -10,7 +10,7 @@
 //      32-bit column), once per row block; the MMA reads A from tensor memory.
 //   B  [N x rank] bf16: W2 rows (W2 stored [V, rank], K-major) by TMA, one whole tile per
 //      pipeline stage, kept in L2 with an evict-last policy and prefetched two tiles ahead.
-//   D  [128 x N] fp32 in tensor memory, two stages, read back with tcgen05.ld.
+//   D  [128 x N] fp32 in tensor memory, three stages, read back with tcgen05.ld.
 //   U / T tiles: the base-logit (and target) rows of the tile, by TMA with an evict-first
 //      policy (read once), 64-column boxes in the 128-byte-swizzled layout; rows that are not
 //      equally spaced (the final rows of rejection verification) come four at a time with
@@ -47,8 +47,9 @@ constexpr uint32_t kBoxBytes = kBM * 128;         // one TMA box: 128 rows x 64 
 
 // Per pass mode. Shared memory (A lives in tensor memory); a B stage holds a whole tile of W2 so
 // that the single MMA-issuing thread waits once and commits twice per tile:
-//   MODE_STATS: N = 128: B 2 x 64 KB + U 3 x 32 KB          = 224 KB; TMEM 2 x 128 + 128 cols
-//   MODE_TV / MODE_RESID: N = 64: B 3 x 32 KB + (U + T) 3 x 2 x 16 KB = 192 KB; TMEM 2 x 64 + 128
+//   MODE_STATS: N = 128: B 2 x 64 KB + U 3 x 32 KB          = 224 KB; TMEM 3 x 128 + 128 cols
+//   MODE_TV / MODE_RESID: N = 64: B 3 x 32 KB + (U + T) 3 x 2 x 16 KB = 192 KB; TMEM 3 x 64 + 128
+// Three accumulator stages give the MMA thread slack against the epilogue's release of a stage.
 template <int MODE>
 struct Cfg {
   static constexpr int kBN = MODE == MODE_STATS ? 128 : 64;  // vocabulary columns per tile
@@ -58,8 +59,9 @@ struct Cfg {
   static constexpr int kBStages = MODE == MODE_STATS ? 2 : 3;
   static constexpr uint32_t kTileBytes = kBoxes * kBoxBytes;
   static constexpr int kUStages = 3;
-  static constexpr int kAccCols = 2 * kBN;                    // two accumulator stages
-  static constexpr int kTmemCols = MODE == MODE_STATS ? 512 : 256;
+  static constexpr int kAccStages = 3;                        // accumulator stages in TMEM
+  static constexpr int kAccCols = kAccStages * kBN;
+  static constexpr int kTmemCols = 512;                       // accumulators + A (rank/2)
   static constexpr int kSeg = kBN / 2;                        // columns per epilogue warp / partial
 };
 
@@ -404,8 +406,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* u_full = b_empty + KB;
   uint64_t* u_empty = u_full + KU;
   uint64_t* acc_full = u_empty + KU;
-  uint64_t* acc_empty = acc_full + 2;
-  uint64_t* a_full = acc_empty + 2;
+  uint64_t* acc_empty = acc_full + C::kAccStages;
+  uint64_t* a_full = acc_empty + C::kAccStages;
   uint64_t* a_empty = a_full + 1;
   uint64_t* drain = a_empty + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -428,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&u_full[s], 1);
       mbar_init(&u_empty[s], kEpiWarps);
     }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < C::kAccStages; ++s) {
       mbar_init(&acc_full[s], 1);
       mbar_init(&acc_empty[s], kEpiWarps);
     }
@@ -537,7 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t idesc = idesc_bf16(kBM, BN);
     int bs = 0, as = 0;
     uint32_t bph = 0, aph = 0;
-    uint32_t accph[2] = {0, 0};
+    uint32_t accph[C::kAccStages] = {};
     bool ok = true;
     int cur_mt = -1;
     if (lane == 0) {
@@ -568,7 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (++bs == KB) { bs = 0; bph ^= 1; }
         mma_commit(&acc_full[as]);
         accph[as] ^= 1;
-        as ^= 1;
+        if (++as == C::kAccStages) as = 0;
         const bool last_of_block = (t + 1 == t_end) || ((int)((t + 1) / P.t.n_nt) != mt);
         if (last_of_block) mma_commit(a_empty);
       }
@@ -584,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int h = ew >> 2;           // column half
     const int i = q * 32 + lane;     // row within the tile (TMEM lane)
     int as = 0, us = 0;
-    uint32_t accph[2] = {0, 0}, uph = 0, aeph = 0;
+    uint32_t accph[C::kAccStages] = {}, uph = 0, aeph = 0;
     int cur_mt = -1;
     bool ok = true;
     for (long long t = t_begin; t < t_end && ok; ++t) {
@@ -670,7 +672,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (++us == KU) { us = 0; uph ^= 1; }
       accph[as] ^= 1;
-      as ^= 1;
+      if (++as == C::kAccStages) as = 0;
 
       const size_t o = (size_t)((n0 + col0) / kHalf) * j.rows + tr.prow;
       if constexpr (MODE == MODE_STATS) {
