@@ -238,6 +238,7 @@ const char* spec_status_string(int status) {
     case SPEC_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
     case SPEC_ERR_CUDA: return "CUDA error";
     case SPEC_ERR_UNSUPPORTED: return "unsupported combination";
+    case SPEC_ERR_TOO_LARGE: return "size beyond the fixed scratch of this entry point";
     default: return "unknown status";
   }
 }

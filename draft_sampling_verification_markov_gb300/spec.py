@@ -21,6 +21,8 @@ SPEC_F32, SPEC_BF16 = 0, 1
 (SPEC_DEV_BAD_TOKEN, SPEC_DEV_NONFINITE, SPEC_DEV_EMPTY_RESIDUAL, SPEC_DEV_BAD_LENGTH,
  SPEC_DEV_TIMEOUT) = 1, 2, 4, 8, 16
 SPEC_SCHEDULE_MAX_CANDIDATES = 16384
+SPEC_NOALLOC_MAX_ROWS = 65536
+SPEC_ERR_TOO_LARGE = -7
 
 _lib = None
 
@@ -60,6 +62,7 @@ def lib():
         L.spec_tv_confidence.argtypes = [vp, vp, i, vp, vp, i, i, vp, vp, vp, vp, f, i, i, i, vp,
                                          vp, vp, sz, vp]
         L.spec_schedule_prefix.argtypes = [vp, vp, i, i, i, vp, vp, vp, vp, sz, vp]
+        L.spec_verify_greedy_noalloc.argtypes = [vp, i, vp, vp, i, i, i, vp, vp, vp, vp, vp]
         L.spec_launch_count.restype = ctypes.c_ulonglong
         L.spec_trace_events.argtypes = [i, vp, vp, i]
         L.spec_trace_events.restype = i
@@ -67,7 +70,8 @@ def lib():
         L.spec_trace_count.restype = i
         for name in ("spec_workspace_init", "spec_device_status", "spec_markov_propose",
                      "spec_verify_greedy", "spec_target_stats", "spec_verify_rejection",
-                     "spec_tv_confidence", "spec_schedule_prefix"):
+                     "spec_tv_confidence", "spec_schedule_prefix",
+                     "spec_verify_greedy_noalloc"):
             getattr(L, name).restype = i
         _lib = L
     return _lib
@@ -208,6 +212,30 @@ def spec_verify_greedy(target, draft_tokens, lengths=None, *, accept_len=None, o
                                   gamma, V, _ptr(accept_len), _ptr(out_tokens), _ptr(next_anchor),
                                   wp, wn, _stream(stream))
     _check("spec_verify_greedy", rc)
+    return accept_len, out_tokens, next_anchor
+
+
+def spec_verify_greedy_noalloc(target, draft_tokens, lengths=None, *, accept_len=None,
+                               out_tokens=None, next_anchor=None, device_status=None, stream=None):
+    """spec_verify_greedy without a workspace, for callers that cannot allocate device memory
+    where they call it: the library's own fixed device scratch stands in for the workspace.
+    Output tensors left as None are allocated here by torch (pass them to avoid that);
+    `device_status` is an optional int32 device tensor of one element that receives the call's
+    SPEC_DEV_* bits."""
+    R, rows, V = target.shape
+    gamma = rows - 1
+    dev = target.device
+    if accept_len is None:
+        accept_len = torch.empty(R, dtype=torch.int32, device=dev)
+    if out_tokens is None:
+        out_tokens = torch.empty(R, gamma + 1, dtype=torch.int32, device=dev)
+    if next_anchor is None:
+        next_anchor = torch.empty(R, dtype=torch.int32, device=dev)
+    rc = lib().spec_verify_greedy_noalloc(_ptr(target), _dt(target), _ptr(draft_tokens),
+                                          _ptr(lengths), R, gamma, V, _ptr(accept_len),
+                                          _ptr(out_tokens), _ptr(next_anchor),
+                                          _ptr(device_status), _stream(stream))
+    _check("spec_verify_greedy_noalloc", rc)
     return accept_len, out_tokens, next_anchor
 
 

@@ -53,6 +53,7 @@ extern "C" {
 #define SPEC_ERR_WORKSPACE_TOO_SMALL (-3)
 #define SPEC_ERR_CUDA (-4)               /* a CUDA runtime call or launch failed */
 #define SPEC_ERR_UNSUPPORTED (-6)        /* a combination this build does not implement */
+#define SPEC_ERR_TOO_LARGE (-7)          /* sizes beyond a fixed limit (SPEC_NOALLOC_MAX_ROWS) */
 
 /* dtype codes */
 #define SPEC_F32 0
@@ -229,6 +230,33 @@ int spec_tv_confidence(const void* U, const void* target, int l_dtype, const voi
 int spec_schedule_prefix(const float* survival, const double* sps, int Bmax, int R, int gamma,
                          int32_t* lengths, int32_t* B_out, double* theta_out, void* ws,
                          size_t ws_bytes, void* stream);
+
+/* Largest R * (gamma + 1) that spec_verify_greedy_noalloc accepts. */
+#define SPEC_NOALLOC_MAX_ROWS 65536
+
+/*
+ * Greedy verification that allocates nothing and takes no workspace.
+ * The paper has no counterpart: this entry point exists for callers that cannot allocate
+ * device memory at the call site (a plug-in inside an engine that reserves all device memory at
+ * start-up, a latency-critical loop that must not meet cudaMalloc's implicit synchronisation,
+ * a host whose memory is owned by another framework's allocator). It computes exactly what
+ * spec_verify_greedy computes, with the same arguments and outputs, except:
+ *   - its scratch (a status word and one argmax per target row, 256 + 4 * 65536 bytes) is a
+ *     fixed device array inside the library, held by every GPU that loads the library until the
+ *     process exits; R * (gamma + 1) above SPEC_NOALLOC_MAX_ROWS returns SPEC_ERR_TOO_LARGE
+ *     before any launch;
+ *   - the first call on a device looks up that array's device address (once per device, with
+ *     that device current); make that first call before any stream capture;
+ *   - every call on a device shares the one array, so calls whose work overlaps on the GPU
+ *     (other streams, other host threads) race and give undefined results: order them;
+ *   - the device status bits of this call (SPEC_DEV_*, cleared at the start of every call) are
+ *     copied into *device_status (a device pointer, optional) at the end of the call's work.
+ * It calls no cudaMalloc, cudaFree or allocating library routine.
+ */
+int spec_verify_greedy_noalloc(const void* target, int t_dtype, const int32_t* draft_tokens,
+                               const int32_t* lengths, int R, int gamma, int V,
+                               int32_t* accept_len, int32_t* out_tokens, int32_t* next_anchor,
+                               uint32_t* device_status, void* stream);
 
 /*
  * Tracing (no counterpart on the pages; instrumentation of this library).

@@ -89,6 +89,12 @@ def test_validation_rejects_before_launch(cuda_lib):
     # Bmax < R, and too many candidates
     assert sched(bogus, bogus, 3, 4, 2, bogus, bogus, bogus, bogus, 1024, None) == -1
     assert sched(bogus, bogus, 1 << 20, 2048, 16, bogus, bogus, bogus, bogus, 1024, None) == -1
+    # the no-allocation greedy verify: beyond its fixed scratch, then a bad dtype
+    na = cuda_lib.spec_verify_greedy_noalloc
+    na.restype = ctypes.c_int
+    na.argtypes = [vp, ctypes.c_int, vp, vp] + [ctypes.c_int] * 3 + [vp] * 5
+    assert na(bogus, 0, bogus, None, 16385, 3, 8, bogus, bogus, bogus, None, None) == -7
+    assert na(bogus, 9, bogus, None, 4, 3, 8, bogus, bogus, bogus, None, None) == -2
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
