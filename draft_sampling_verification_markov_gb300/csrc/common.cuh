@@ -103,11 +103,90 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
-__device__ __forceinline__ double warp_sum_d(double x) {
+// ------------------------------------------------------------------------------ double-float sums
+// Long sums and prefix sums are carried as an unevaluated pair hi + lo of fp32 numbers: Knuth's
+// TwoSum yields the exact rounding error of an fp32 addition, so a pair keeps about 48 bits
+// while using only fp32 arithmetic (fp64 runs at a small fraction of the fp32 rate here).
+struct DF {
+  float hi, lo;
+};
+
+__device__ __forceinline__ DF df_zero() { return {0.0f, 0.0f}; }
+
+// s + e == a + b exactly, s = fl(a + b) (Knuth, TAOCP vol. 2, 4.2.2).
+__device__ __forceinline__ DF two_sum(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  const float e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+  return {s, e};
+}
+
+// The same when |a| >= |b| (Dekker).
+__device__ __forceinline__ DF fast_two_sum(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  return {s, __fsub_rn(b, __fsub_rn(s, a))};
+}
+
+__device__ __forceinline__ DF df_add(DF a, float b) {
+  const DF s = two_sum(a.hi, b);
+  return fast_two_sum(s.hi, __fadd_rn(s.lo, a.lo));
+}
+
+__device__ __forceinline__ DF df_add(DF a, DF b) {
+  const DF s = two_sum(a.hi, b.hi);
+  const DF t = two_sum(a.lo, b.lo);
+  const DF u = fast_two_sum(s.hi, __fadd_rn(s.lo, t.hi));
+  return fast_two_sum(u.hi, __fadd_rn(u.lo, t.lo));
+}
+
+__device__ __forceinline__ DF df_neg(DF a) { return {-a.hi, -a.lo}; }
+
+// a * b for an fp32 b (the product's rounding error from an fma).
+__device__ __forceinline__ DF df_mul(DF a, float b) {
+  const float p = __fmul_rn(a.hi, b);
+  const float e = fmaf(a.hi, b, -p);
+  return fast_two_sum(p, fmaf(a.lo, b, e));
+}
+
+// a > b for normalised pairs (|lo| at most half an ulp of hi).
+__device__ __forceinline__ bool df_gt(DF a, DF b) {
+  return a.hi > b.hi || (a.hi == b.hi && a.lo > b.lo);
+}
+
+__device__ __forceinline__ float df_float(DF a) { return __fadd_rn(a.hi, a.lo); }
+
+__device__ __forceinline__ DF df_shfl_xor(DF a, int off) {
+  return {__shfl_xor_sync(0xffffffffu, a.hi, off), __shfl_xor_sync(0xffffffffu, a.lo, off)};
+}
+
+__device__ __forceinline__ DF df_shfl_up(DF a, int off) {
+  return {__shfl_up_sync(0xffffffffu, a.hi, off), __shfl_up_sync(0xffffffffu, a.lo, off)};
+}
+
+__device__ __forceinline__ DF df_shfl(DF a, int lane) {
+  return {__shfl_sync(0xffffffffu, a.hi, lane), __shfl_sync(0xffffffffu, a.lo, lane)};
+}
+
+// Warp sum; df_add is commutative, so every lane receives the same pair.
+__device__ __forceinline__ DF warp_sum_df(DF x) {
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+  for (int off = 16; off > 0; off >>= 1) x = df_add(x, df_shfl_xor(x, off));
   return x;
 }
+
+// Inclusive warp prefix sum in lane order.
+__device__ __forceinline__ DF warp_scan_df(DF x) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const DF y = df_shfl_up(x, off);
+    if (lane >= off) x = df_add(y, x);
+  }
+  return x;
+}
+
+// log(hi + lo) for a positive normalised pair.
+__device__ __forceinline__ float df_log(DF a) { return logf(a.hi) + a.lo / a.hi; }
 
 __device__ __forceinline__ float warp_max(float x) {
 #pragma unroll

@@ -41,7 +41,8 @@ namespace tc {
 constexpr int kBM = 128;                            // rows per tile (one MMA, 128 TMEM lanes)
 constexpr int kEpiWarps = 8;
 constexpr int kFirstEpi = 3;                       // warps 0..2: B producer, MMA, U/T producer
-constexpr int kThreads = (kFirstEpi + kEpiWarps) * 32;
+constexpr int kIssuer2 = kFirstEpi + kEpiWarps;     // the second MMA issuer warp
+constexpr int kThreads = (kIssuer2 + 1) * 32;
 constexpr long long kSpinCycles = 4000000000LL;  // ~2 s at the maximum SM clock
 constexpr uint32_t kBoxBytes = kBM * 128;         // one TMA box: 128 rows x 64 columns (bf16)
 
@@ -379,6 +380,7 @@ struct TcParams {
   float* pm;
   float* ps;
   int* pi;
+  int nseg;  // partial segments per row (row-major partial arrays)
 };
 
 template <int MODE, bool ARGMAX, bool GATHER>
@@ -435,8 +437,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&acc_empty[s], kEpiWarps);
     }
     mbar_init(a_full, kEpiWarps);
-    mbar_init(a_empty, 1);
-    mbar_init(drain, 1);
+    mbar_init(a_empty, 2);  // one arrival per MMA issuer
+    mbar_init(drain, 2);
     *abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -459,15 +461,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t bph = 0;
     bool ok = true;
     constexpr int kPrefetch = 2;  // tiles ahead of the shared-memory ring, into L2
+    int nt = (int)(t_begin % P.t.n_nt), pf = nt;
     if (lane == 0)
-      for (long long t = t_begin; t < t_begin + kPrefetch && t < t_end; ++t)
-        for (int ka = 0; ka < ka_n; ++ka)
-          tma_prefetch_2d(&map_w2, ka * 64, (int)(t % P.t.n_nt) * BN, pol_keep);
+      for (long long t = t_begin; t < t_begin + kPrefetch && t < t_end; ++t) {
+        for (int ka = 0; ka < ka_n; ++ka) tma_prefetch_2d(&map_w2, ka * 64, pf * BN, pol_keep);
+        if (++pf == P.t.n_nt) pf = 0;
+      }
     for (long long t = t_begin; t < t_end && ok; ++t) {
-      const int n0 = (int)(t % P.t.n_nt) * BN;
+      const int n0 = nt * BN;
+      if (++nt == P.t.n_nt) nt = 0;
       if (lane == 0 && t + kPrefetch < t_end)
-        for (int ka = 0; ka < ka_n; ++ka)
-          tma_prefetch_2d(&map_w2, ka * 64, (int)((t + kPrefetch) % P.t.n_nt) * BN, pol_keep);
+        for (int ka = 0; ka < ka_n; ++ka) tma_prefetch_2d(&map_w2, ka * 64, pf * BN, pol_keep);
+      if (t + kPrefetch < t_end && ++pf == P.t.n_nt) pf = 0;
       ok = mbar_wait(&b_empty[bs], bph ^ 1, abort, status);
       if (ok && lane == 0) {
         mbar_arrive_expect_tx(&b_full[bs], ka_n * C::kBAtomBytes);
@@ -488,8 +493,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // start streaming logit rows once the first A block is in tensor memory: the W1 gather is
     // latency-bound and must not queue behind this stream
     bool ok = t_begin >= t_end || mbar_wait(a_full, 0, abort, status);
+    int mt_c = (int)(t_begin / P.t.n_nt), nt_c = (int)(t_begin % P.t.n_nt);
     for (long long t = t_begin; t < t_end && ok; ++t) {
-      const int mt = (int)(t / P.t.n_nt), nt = (int)(t % P.t.n_nt);
+      const int mt = mt_c, nt = nt_c;
+      if (++nt_c == P.t.n_nt) { nt_c = 0; ++mt_c; }
       const int n0 = nt * BN;
       ok = mbar_wait(&u_empty[us], uph ^ 1, abort, status);
       if (!ok) break;
@@ -534,27 +541,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (lane == 0)
       for (int s = 0; s < KU; ++s) mbar_drain(&u_full[s], (s < us) ? uph : (uph ^ 1));
-  } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA issuer
+  } else if (warp == 1 || warp == kIssuer2) {
+    // ---------------------------------------------------------------- MMA issuers
+    // Two threads issue alternate tiles. Issuing blocks while the tensor pipe's queue is full,
+    // so one thread's barrier waits and bookkeeping overlap the other thread's MMAs.
     constexpr uint32_t idesc = idesc_bf16(kBM, BN);
-    int bs = 0, as = 0;
-    uint32_t bph = 0, aph = 0;
-    uint32_t accph[C::kAccStages] = {};
-    bool ok = true;
-    int cur_mt = -1;
+    const int p = warp == 1 ? 0 : 1;
     if (lane == 0) {
-      for (long long t = t_begin; t < t_end && ok; ++t) {
-        const int mt = (int)(t / P.t.n_nt);
+      bool ok = true;
+      int mt = (int)(t_begin / P.t.n_nt), nt = (int)(t_begin % P.t.n_nt);
+      int cur_mt = -1, blk = -1;
+      bool owned = false;  // this thread issued a tile of the current A block
+      const int n_local = (int)(t_end - t_begin);
+      for (int i = 0; i < n_local && ok; ++i) {
         if (mt != cur_mt) {
-          ok = mbar_wait(a_full, aph, abort, status);
-          aph ^= 1;
+          // the A block is released once both issuers' MMAs on it are done; a thread that
+          // issued none of its tiles arrives directly (after a_full, so that its arrival
+          // belongs to this block's phase)
+          if (blk >= 0) {
+            if (owned) mma_commit(a_empty);
+            else mbar_arrive(a_empty);
+          }
+          ++blk;
+          owned = false;
           cur_mt = mt;
+          ok = mbar_wait(a_full, blk & 1, abort, status);
           if (!ok) break;
           tc_fence_after();
         }
-        ok = mbar_wait(&acc_empty[as], accph[as] ^ 1, abort, status);
+        if (++nt == P.t.n_nt) { nt = 0; ++mt; }
+        if ((i & 1) != p) continue;
+        const int as = i % C::kAccStages, bs = i % KB;
+        ok = mbar_wait(&acc_empty[as], ((i / C::kAccStages) & 1) ^ 1, abort, status);
         if (!ok) break;
-        ok = mbar_wait(&b_full[bs], bph, abort, status);
+        ok = mbar_wait(&b_full[bs], (i / KB) & 1, abort, status);
         if (!ok) break;
         tc_fence_after();
         const uint32_t d = tmem + as * BN;
@@ -567,19 +587,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_bf16_ta(d, a + ks * 8, sw128_desc(b_base + ks * 32), idesc, (ka | ks) != 0);
         }
         mma_commit(&b_empty[bs]);
-        if (++bs == KB) { bs = 0; bph ^= 1; }
         mma_commit(&acc_full[as]);
-        accph[as] ^= 1;
-        if (++as == C::kAccStages) as = 0;
-        const bool last_of_block = (t + 1 == t_end) || ((int)((t + 1) / P.t.n_nt) != mt);
-        if (last_of_block) mma_commit(a_empty);
+        owned = true;
       }
-      // all MMAs issued by this thread complete before tensor memory is released
+      if (ok && blk >= 0) {
+        if (owned) mma_commit(a_empty);
+        else mbar_arrive(a_empty);
+      }
+      // all MMAs issued by either thread complete before tensor memory is released
       mma_commit(drain);
       mbar_drain(drain, 0);
     }
     __syncwarp();
-  } else if (warp >= kFirstEpi) {
+  } else if (warp >= kFirstEpi && warp < kFirstEpi + kEpiWarps) {
     // ---------------------------------------------------------------- epilogue
     const int ew = warp - kFirstEpi;
     const int q = warp & 3;          // TMEM lane quarter
@@ -589,8 +609,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t accph[C::kAccStages] = {}, uph = 0, aeph = 0;
     int cur_mt = -1;
     bool ok = true;
+    int mt_c = (int)(t_begin / P.t.n_nt), nt_c = (int)(t_begin % P.t.n_nt);
+    Norm dn = {0.0f, 0.0f}, tn = {0.0f, 0.0f};  // this row's softmax normalisers (pair modes)
+    bool resid = true;                          // residual (true) or bonus row (MODE_RESID)
     for (long long t = t_begin; t < t_end && ok; ++t) {
-      const int mt = (int)(t / P.t.n_nt), nt = (int)(t % P.t.n_nt);
+      const int mt = mt_c, nt = nt_c;
+      if (++nt_c == P.t.n_nt) { nt_c = 0; ++mt_c; }
       const int n0 = nt * BN;
       const TileRow tr = tile_row(j, P.t, mt, i);
       if (mt != cur_mt) {
@@ -637,6 +661,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(a_full);
+        // per-row normalisers, loaded once per row block
+        if constexpr (kPair) {
+          dn = {0.0f, 0.0f};
+          tn = {0.0f, 0.0f};
+          resid = true;
+          if (tr.valid) {
+            if constexpr (MODE == MODE_TV) {
+              tn = load_norm(j.tstats, (long long)tr.r * (j.gamma + 1) + (tr.k - 1));
+              dn = load_norm(j.dstats, (long long)tr.r * j.gamma + (tr.k - 1));
+            } else {
+              const int n = j.final_n[tr.r];
+              resid = j.final_kind[tr.r] != 0;
+              tn = load_norm(j.tstats, (long long)tr.r * (j.gamma + 1) + n);
+              if (resid) dn = load_norm(j.dstats, (long long)tr.r * j.gamma + n);
+            }
+          }
+        }
       }
       const int col0 = h * kHalf;  // first tile column of this warp
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + as * BN + col0;
@@ -674,7 +715,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       accph[as] ^= 1;
       if (++as == C::kAccStages) as = 0;
 
-      const size_t o = (size_t)((n0 + col0) / kHalf) * j.rows + tr.prow;
+      const size_t o = (size_t)tr.prow * P.nseg + (n0 + col0) / kHalf;
       if constexpr (MODE == MODE_STATS) {
         // z = (bias + U) * scale, two columns per instruction
         const unsigned long long sc2 = pack2(j.scale, j.scale);
@@ -736,19 +777,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (ARGMAX) P.pi[o] = idx;
         }
       } else {
-        Norm dn = {0.0f, 0.0f}, tn = {0.0f, 0.0f};
-        bool resid = true;
-        if (tr.valid) {
-          if constexpr (MODE == MODE_TV) {
-            tn = load_norm(j.tstats, (long long)tr.r * (j.gamma + 1) + (tr.k - 1));
-            dn = load_norm(j.dstats, (long long)tr.r * j.gamma + (tr.k - 1));
-          } else {
-            const int n = j.final_n[tr.r];
-            resid = j.final_kind[tr.r] != 0;
-            tn = load_norm(j.tstats, (long long)tr.r * (j.gamma + 1) + n);
-            if (resid) dn = load_norm(j.dstats, (long long)tr.r * j.gamma + n);
-          }
-        }
         if (live) {
           float sum = 0.0f;
 #pragma unroll
@@ -867,6 +895,7 @@ cudaError_t launch_markov_tc(const RowJob& j, float* pm, float* ps, int* pi, boo
   p.t.rb = rb;
   p.t.n_mt = j.map == MAP_ALL_POS ? rb * j.gamma : rb;
   p.t.n_nt = (j.V + BN - 1) / BN;
+  p.nseg = (j.V + BN / 2 - 1) / (BN / 2);
   const long long total = (long long)p.t.n_mt * p.t.n_nt;
   if (total == 0) return cudaSuccess;
   const int grid = (int)(total < num_sms() ? total : num_sms());

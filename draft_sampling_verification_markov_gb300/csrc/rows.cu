@@ -110,7 +110,7 @@ __global__ void __launch_bounds__(256) stream_partials_kernel(RowJob j, int seg,
     const int row = u / nseg, sg = u - row * nseg;
     const RowInfo ri = row_info(j, row);
     const int v0 = sg * seg, v1 = min(j.V, v0 + seg);
-    const size_t out = (size_t)sg * j.rows + row;
+    const size_t out = (size_t)row * nseg + sg;
     if (!ri.active) {
       if (threadIdx.x == 0) {
         if (pm) pm[out] = -INFINITY;
@@ -337,7 +337,7 @@ __global__ void __launch_bounds__(256) markov_ffma_partials(RowJob j, int nseg, 
        u += stride) {
     const int row = (int)(u / nseg), c = (int)(u % nseg);
     const RowInfo ri = row_info(j, row);
-    const size_t out = (size_t)c * j.rows + row;
+    const size_t out = (size_t)row * nseg + c;
     if constexpr (MODE == MODE_STATS) {
       StatsAcc acc = stats_empty();
 #pragma unroll
@@ -373,36 +373,30 @@ __global__ void __launch_bounds__(256) markov_ffma_partials(RowJob j, int nseg, 
 
 // ------------------------------------------------------------------------------ select
 
-// Exclusive block scan of one double per thread (blockDim.x == 256); returns the exclusive
-// prefix and writes the block total.
-__device__ __forceinline__ double block_exscan_d(double x, double* total) {
-  __shared__ double sm[32];
+// Exclusive block scan of one double-float per thread; returns the exclusive prefix and writes
+// the block total.
+__device__ __forceinline__ DF block_exscan_df(DF x, DF* total) {
+  __shared__ DF sm[33];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  double inc = x;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const double y = __shfl_up_sync(0xffffffffu, inc, off);
-    if (lane >= off) inc += y;
-  }
+  const DF inc = warp_scan_df(x);
+  DF ex = df_shfl_up(inc, 1);
+  if (lane == 0) ex = df_zero();
   __syncthreads();
   if (lane == 31) sm[warp] = inc;
   __syncthreads();
   if (warp == 0) {
-    double w = lane < nw ? sm[lane] : 0.0;
-    double wi = w;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const double y = __shfl_up_sync(0xffffffffu, wi, off);
-      if (lane >= off) wi += y;
-    }
-    if (lane < nw) sm[lane] = wi - w;  // exclusive warp offsets
-    if (lane == nw - 1) sm[31] = wi;
+    const DF w = lane < nw ? sm[lane] : df_zero();
+    const DF wi = warp_scan_df(w);
+    DF wex = df_shfl_up(wi, 1);
+    if (lane == 0) wex = df_zero();
+    if (lane < nw) sm[lane] = wex;
+    if (lane == nw - 1) sm[32] = wi;
   }
   __syncthreads();
-  const double ex = sm[warp] + inc - x;
-  *total = sm[31];
+  const DF r = df_add(sm[warp], ex);
+  *total = sm[32];
   __syncthreads();
-  return ex;
+  return r;
 }
 
 // Value of element v of the crossing segment: exp(z_d - M) for a proposal, or the residual /
@@ -476,7 +470,7 @@ __global__ void __launch_bounds__(256) select_kernel(RowJob j, int seg, int nseg
                                                      const float* ps, const int* pi,
                                                      SelectOut o) {
   __shared__ int sh_c, sh_x, sh_last;
-  __shared__ double sh_rem;
+  __shared__ float sh_rem;
   __shared__ float sh_M, sh_lz;
   __shared__ float zs[64];   // draft logits of the segment starting at sh_zv0
   __shared__ float es[64];
@@ -490,66 +484,86 @@ __global__ void __launch_bounds__(256) select_kernel(RowJob j, int seg, int nseg
   const bool markov = resid ? (ri.resid && j.rank > 0) : j.rank > 0;
   const bool need_z = j.rank > 0 && (!resid || ri.resid);
 
-  // 1. normaliser from the partials (a contiguous run of segments per thread)
-  const int run = (nseg + blockDim.x - 1) / blockDim.x;
-  const int c0 = min(nseg, tid * run), c1 = min(nseg, c0 + run);
-  // the run's partials are loaded together (one memory round trip), kRun at a time
-  constexpr int kRun = 16;
+  // 1. normaliser from the partials. Warp w owns the contiguous segment range [s0, s1) of the
+  // row's (row-major) partials and lane l a contiguous run [c0, c1) of it; a run of up to kPer
+  // segments stays in registers through the crossing search below.
+  const int warp = tid >> 5, lane = tid & 31, nwarps = blockDim.x >> 5;
+  const int s0 = (int)((long long)nseg * warp / nwarps);
+  const int s1 = (int)((long long)nseg * (warp + 1) / nwarps);
+  const int per = (s1 - s0 + 31) / 32;
+  const int c0 = min(s1, s0 + lane * per), c1 = min(s1, c0 + per);
+  const float* rpm = pm + (size_t)row * nseg;
+  const float* rps = ps + (size_t)row * nseg;
+  constexpr int kPer = 16;
+  const bool in_regs = per <= kPer;  // the same for every thread of the block
+  float lm[kPer], ls[kPer];
   float M = -INFINITY;
   int gidx = 0x7fffffff;
   if (!resid) {
+    const int* rpi = pi ? pi + (size_t)row * nseg : nullptr;
     StatsAcc a = stats_empty();
-    for (int cb = c0; cb < c1; cb += kRun) {
-      float lm[kRun], ls[kRun];
-      int li[kRun];
+    for (int cb = c0; cb < c1; cb += kPer) {
+      int li[kPer];
 #pragma unroll
-      for (int k = 0; k < kRun; ++k) {
+      for (int k = 0; k < kPer; ++k) {
         const int c = cb + k;
         lm[k] = -INFINITY;
         ls[k] = 0.0f;
         li[k] = 0x7fffffff;
         if (c < c1) {
-          const size_t q = (size_t)c * j.rows + row;
-          lm[k] = pm[q];
-          ls[k] = ps[q];
-          if (pi) li[k] = pi[q];
+          lm[k] = rpm[c];
+          ls[k] = rps[c];
+          if (rpi) li[k] = rpi[c];
         }
       }
 #pragma unroll
-      for (int k = 0; k < kRun; ++k) a = stats_merge(a, {lm[k], ls[k], li[k]});
+      for (int k = 0; k < kPer; ++k) a = stats_merge(a, {lm[k], ls[k], li[k]});
     }
     a = block_merge(a);
     M = a.m;
     gidx = a.idx;
   }
-  float localf = 0.0f;  // a thread's run is short: fp32 here, fp64 only across threads
-  for (int cb = c0; cb < c1; cb += kRun) {
-    float w[kRun];
+  // 2. segment weights (each partial's share of Z, fp32); run sums, an inclusive warp scan of
+  // them and the warp totals as double-float pairs; Z and every warp's offset are sums of the
+  // warp totals in warp order
+  auto weight = [&](float pmv, float psv) -> float {
+    return resid ? psv : (psv == 0.0f ? 0.0f : psv * exp_shift(pmv, M));
+  };
+  DF lsum = df_zero();
+  if (in_regs) {
+    if (resid) {
 #pragma unroll
-    for (int k = 0; k < kRun; ++k) {
-      const int c = cb + k;
-      w[k] = 0.0f;
-      if (c < c1) {
-        const size_t q = (size_t)c * j.rows + row;
-        w[k] = resid ? ps[q] : (ps[q] == 0.0f ? 0.0f : ps[q] * exp_shift(pm[q], M));
+      for (int k = 0; k < kPer; ++k) {
+        lm[k] = 0.0f;
+        ls[k] = c0 + k < c1 ? rps[c0 + k] : 0.0f;
       }
     }
 #pragma unroll
-    for (int k = 0; k < kRun; ++k) localf += w[k];
+    for (int k = 0; k < kPer; ++k) {
+      ls[k] = c0 + k < c1 ? weight(lm[k], ls[k]) : 0.0f;  // ls now holds the weights
+      lsum = df_add(lsum, ls[k]);
+    }
+  } else {
+    for (int c = c0; c < c1; ++c) lsum = df_add(lsum, weight(resid ? 0.0f : rpm[c], rps[c]));
   }
-  const double local = (double)localf;
-  double Z;
-  const double before = block_exscan_d(local, &Z);
+  const DF incl = warp_scan_df(lsum);
+  DF run_before = df_shfl_up(incl, 1);  // the warp's mass before this run
+  if (lane == 0) run_before = df_zero();
+  __shared__ DF sh_wt[32];
+  if (lane == 31) sh_wt[warp] = incl;
+  __syncthreads();
+  DF Z = df_zero();
+  for (int w = 0; w < nwarps; ++w) Z = df_add(Z, sh_wt[w]);
   if (tid == 0) {
     sh_M = M;
-    sh_lz = resid ? 0.0f : (float)log(Z);
+    const bool zok = Z.hi > 0.0f && isfinite(Z.hi);
+    sh_lz = resid ? 0.0f : (zok ? df_log(Z) : logf(Z.hi));
     sh_c = -1;
-    sh_rem = 0.0;
+    sh_rem = 0.0f;
     sh_x = -1;
     sh_last = -1;
     sh_zv0 = -1;
-    if (!resid && (!(Z > 0.0) || !isfinite(Z) || !(M > -INFINITY)))
-      atomicOr(j.status, SPEC_DEV_NONFINITE);
+    if (!resid && (!zok || !(M > -INFINITY))) atomicOr(j.status, SPEC_DEV_NONFINITE);
   }
   __syncthreads();
 
@@ -567,42 +581,70 @@ __global__ void __launch_bounds__(256) select_kernel(RowJob j, int seg, int nseg
       __syncthreads();
     }
   } else {
-    // 2. crossing segment for t = u * Z
-    const double t = (double)u_row * Z;
-    if (before <= t && before + local > t) {
-      double cum = before;
-      int lastc = -1;
-      double lastw = 0.0;
-      for (int c = c0; c < c1; ++c) {
-        const size_t q = (size_t)c * j.rows + row;
-        const double w = (double)(resid ? ps[q] : (ps[q] == 0.0f ? 0.0f : ps[q] * exp_shift(pm[q], M)));
-        if (cum + w > t) {
-          lastc = c;
-          lastw = t - cum;
-          break;
-        }
-        if (w > 0.0) {
-          lastc = c;
-          lastw = 1e300;  // summation-order rounding: end of the last positive segment
-        }
-        cum += w;
+    // 3. crossing segment for t = u * Z: the warp whose mass holds t, the first lane of it
+    // whose cumulative mass exceeds t, then that lane's run in order
+    const DF t = df_mul(Z, u_row);
+    DF before = df_zero();
+    int wstar = -1;
+    for (int w = 0; w < nwarps; ++w) {
+      const DF next = df_add(before, sh_wt[w]);
+      if (df_gt(next, t)) {
+        wstar = w;
+        break;
       }
-      sh_c = lastc;
-      sh_rem = lastw;
+      before = next;
+    }
+    if (warp == wstar) {
+      const unsigned hit = __ballot_sync(0xffffffffu, df_gt(df_add(before, incl), t));
+      if (hit && lane == __ffs(hit) - 1) {
+        DF cum = df_add(before, run_before);
+        int found = -1, lastpos = -1;
+        float remv = 1e30f;
+        if (in_regs) {
+#pragma unroll
+          for (int k = 0; k < kPer; ++k) {
+            if (found < 0 && c0 + k < c1) {
+              const float wv = ls[k];
+              const DF next = df_add(cum, wv);
+              if (df_gt(next, t)) {
+                found = c0 + k;
+                remv = df_float(df_add(t, df_neg(cum)));
+              }
+              if (wv > 0.0f) lastpos = c0 + k;
+              cum = next;
+            }
+          }
+        } else {
+          for (int c = c0; c < c1 && found < 0; ++c) {
+            const float wv = weight(resid ? 0.0f : rpm[c], rps[c]);
+            const DF next = df_add(cum, wv);
+            if (df_gt(next, t)) {
+              found = c;
+              remv = df_float(df_add(t, df_neg(cum)));
+            }
+            if (wv > 0.0f) lastpos = c;
+            cum = next;
+          }
+        }
+        // without a crossing in the run (summation-order rounding) the draw ends the run's
+        // last segment with positive mass
+        sh_c = found >= 0 ? found : lastpos;
+        sh_rem = found >= 0 ? remv : 1e30f;
+      }
     }
     __syncthreads();
     if (sh_c < 0 && tid == 0) {
       // rounding left no crossing: the end of the last segment with positive mass
       int last = -1;
       for (int c = nseg - 1; c >= 0 && last < 0; --c)
-        if (ps[(size_t)c * j.rows + row] > 0.0f) last = c;
+        if (rps[c] > 0.0f) last = c;
       if (last < 0) atomicOr(j.status, resid ? SPEC_DEV_EMPTY_RESIDUAL : SPEC_DEV_NONFINITE);
       sh_c = last;
-      sh_rem = 1e300;
+      sh_rem = 1e30f;
     }
     __syncthreads();
     const int cstar = sh_c;
-    const double rem = sh_rem;
+    const float rem = sh_rem;
     Norm dn = {0.0f, 0.0f}, tn = {0.0f, 0.0f};
     if (resid) row_norms(j, ri, dn, tn);
     const int v0 = max(cstar, 0) * seg, v1 = min(j.V, v0 + seg);
@@ -632,9 +674,8 @@ __global__ void __launch_bounds__(256) select_kernel(RowJob j, int seg, int nseg
         }
         const float tot0 = __shfl_sync(0xffffffffu, s0, 31);
         s1 += tot0;
-        const float r = (float)fmin(rem, 1e30);
-        const unsigned m0 = __ballot_sync(0xffffffffu, s0 > r && tid < n);
-        const unsigned m1 = __ballot_sync(0xffffffffu, s1 > r && tid + 32 < n);
+        const unsigned m0 = __ballot_sync(0xffffffffu, s0 > rem && tid < n);
+        const unsigned m1 = __ballot_sync(0xffffffffu, s1 > rem && tid + 32 < n);
         const unsigned p0 = __ballot_sync(0xffffffffu, a0 > 0.0f), p1 = __ballot_sync(0xffffffffu, a1 > 0.0f);
         if (tid == 0) {
           if (m0) sh_x = v0 + __ffs(m0) - 1;
@@ -646,23 +687,24 @@ __global__ void __launch_bounds__(256) select_kernel(RowJob j, int seg, int nseg
       // 3b. long segment (no Markov bias): per-thread runs, block scan, rescan one run
       const int per = (seg + blockDim.x - 1) / blockDim.x;
       const int e0 = min(v1, v0 + tid * per), e1 = min(v1, e0 + per);
-      float mine = 0.0f;
+      DF mine = df_zero();
       for (int v = e0; v < e1; ++v)
-        mine += seg_value<UDT, WDT>(j, ri, resid, M, dn, tn, v,
-                                    ri.urow >= 0 ? draft_logit<UDT, WDT>(j, ri, v) : 0.0f);
-      double segtot;
-      const double sbefore = block_exscan_d((double)mine, &segtot);
+        mine = df_add(mine, seg_value<UDT, WDT>(j, ri, resid, M, dn, tn, v,
+                                                ri.urow >= 0 ? draft_logit<UDT, WDT>(j, ri, v) : 0.0f));
+      DF segtot;
+      const DF sbefore = block_exscan_df(mine, &segtot);
+      const DF r = {rem, 0.0f};
       if (cstar >= 0) {
-        if (sbefore <= rem && sbefore + (double)mine > rem) {
-          double cum = sbefore;
+        if (!df_gt(sbefore, r) && df_gt(df_add(sbefore, mine), r)) {
+          DF cum = sbefore;
           for (int v = e0; v < e1; ++v) {
             const float w = seg_value<UDT, WDT>(j, ri, resid, M, dn, tn, v,
                                                 ri.urow >= 0 ? draft_logit<UDT, WDT>(j, ri, v) : 0.0f);
-            if (cum + (double)w > rem) {
+            cum = df_add(cum, w);
+            if (df_gt(cum, r)) {
               sh_x = v;
               break;
             }
-            cum += w;
           }
         }
         int lastp = -1;
@@ -722,18 +764,21 @@ __global__ void finalize_stats_kernel(int rows, int nseg, const float* pm, const
   if (lengths && (row % rows_per_req) > min(max(lengths[row / rows_per_req], 0), rows_per_req - 1))
     return;  // row beyond the verified length: never read
   float M = -INFINITY;
-  for (int c = lane; c < nseg; c += 32) M = fmaxf(M, pm[(size_t)c * rows + row]);
+  const float* rpm = pm + (size_t)row * nseg;
+  const float* rps = ps + (size_t)row * nseg;
+  for (int c = lane; c < nseg; c += 32) M = fmaxf(M, rpm[c]);
   M = warp_max(M);
-  double Z = 0.0;
+  DF Z = df_zero();
   for (int c = lane; c < nseg; c += 32) {
-    const size_t q = (size_t)c * rows + row;
-    if (ps[q] != 0.0f) Z += (double)ps[q] * (double)exp_shift(pm[q], M);
+    const float pmq = rpm[c], psq = rps[c];
+    if (psq != 0.0f) Z = df_add(Z, psq * exp_shift(pmq, M));
   }
-  Z = warp_sum_d(Z);
+  Z = warp_sum_df(Z);
   if (lane == 0) {
-    if (!(Z > 0.0) || !isfinite(Z) || !(M > -INFINITY)) atomicOr(status, SPEC_DEV_NONFINITE);
+    const bool zok = Z.hi > 0.0f && isfinite(Z.hi);
+    if (!zok || !(M > -INFINITY)) atomicOr(status, SPEC_DEV_NONFINITE);
     stats[2 * (size_t)row] = M;
-    stats[2 * (size_t)row + 1] = (float)log(Z);
+    stats[2 * (size_t)row + 1] = zok ? df_log(Z) : logf(Z.hi);
   }
 }
 
@@ -825,15 +870,14 @@ __global__ void tv_finalize_kernel(int R, int gamma, int nseg, const float* ps, 
   const int lane = threadIdx.x & 31;
   const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (r >= R) return;
-  const int rows = R * gamma;
   float a = 1.0f;
   for (int k = 0; k < gamma; ++k) {
     const int row = r * gamma + k;
-    double c = 0.0;
-    for (int s = lane; s < nseg; s += 32) c += (double)ps[(size_t)s * rows + row];
-    c = warp_sum_d(c);
+    DF c = df_zero();
+    for (int s = lane; s < nseg; s += 32) c = df_add(c, ps[(size_t)row * nseg + s]);
+    c = warp_sum_df(c);
     if (lane == 0) {
-      float cf = (float)c;
+      float cf = df_float(c);
       cf = fminf(fmaxf(cf, 0.0f), 1.0f);
       a = __fmul_rn(a, cf);
       conf[row] = cf;
