@@ -326,6 +326,11 @@ int spec_markov_propose(const void* U, int u_dtype, const void* W1, const void* 
       rc = markov_pass(j, u_dtype, wdt, w, greedy, s, &seg, &nseg);
       if (rc != SPEC_OK) return rc;
     }
+    // the next position's Markov pass re-reads all of W2: have L2 fetch it during this select
+    const size_t w2_bytes = (size_t)V * rank * esize(wdt);
+    const bool pf = rank > 0 && k < gamma && aligned16(W2) && w2_bytes % 16 == 0;
+    o.l2_prefetch = pf ? W2 : nullptr;
+    o.l2_prefetch_bytes = pf ? w2_bytes : 0;
     launch_select(j, u_dtype, wdt, seg, nseg, w.pm, w.ps, greedy ? w.pi : nullptr, o, s);
   }
   return finish();

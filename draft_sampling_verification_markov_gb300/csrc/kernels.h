@@ -23,6 +23,10 @@ struct SelectOut {
   const float* uni;      // uniforms, indexed row * uni_stride + uni_offset
   int uni_stride, uni_offset;
   int greedy;
+  // optional: bytes the next kernel reads (the Markov projection), pulled into L2 while this
+  // latency-bound kernel runs; 16-byte aligned, a multiple of 16 bytes
+  const void* l2_prefetch;
+  unsigned long long l2_prefetch_bytes;
 };
 
 void launch_stream_partials(const RowJob& j, int dtype, int seg, int nseg, bool vec, bool sum,

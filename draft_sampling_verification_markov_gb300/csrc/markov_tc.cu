@@ -4,22 +4,23 @@
 // section 3 softmax; section 5 TV label; the residual of rejection sampling).
 //
 // One tile = 128 rows (requests, TMEM lanes) x N vocabulary columns (N = 128 for softmax
-// partials, 64 for the TV / residual passes), K = rank (<= 256, a multiple of 64).
-//   A  [128 x rank] bf16: the W1 rows of each row's previous token, gathered by the epilogue
-//      warps and stored into tensor memory with tcgen05.st (lane = row, two bf16 of K per
-//      32-bit column), once per row block; the MMA reads A from tensor memory.
+// partials, 64 for the TV / residual passes), K = rank (<= 256, a multiple of 64). A work unit
+// is one W2 column tile against a pair of row blocks: the B tile is loaded once and feeds both
+// blocks' MMA groups, which halves the W2 bytes each SM pulls into shared memory.
+//   A  [128 x rank] bf16 per row block: the W1 rows of each row's previous token, gathered by
+//      the epilogue warps and stored into tensor memory with tcgen05.st (lane = row, two bf16
+//      of K per 32-bit column); both blocks of the current pair stay resident.
 //   B  [N x rank] bf16: W2 rows (W2 stored [V, rank], K-major) by TMA, one whole tile per
-//      pipeline stage, kept in L2 with an evict-last policy and prefetched two tiles ahead.
-//   D  [128 x N] fp32 in tensor memory, three stages, read back with tcgen05.ld.
-//   U / T tiles: the base-logit (and target) rows of the tile, by TMA with an evict-first
-//      policy (read once), 64-column boxes in the 128-byte-swizzled layout; rows that are not
-//      equally spaced (the final rows of rejection verification) come four at a time with
-//      tile::gather4 into the same layout.
+//      pipeline stage, kept in L2 with an evict-last policy and prefetched two units ahead.
+//   D  [128 x N] fp32 in tensor memory (2 stages at N = 128, 4 at N = 64), read back with
+//      tcgen05.ld.
+//   U / T tiles: the base-logit (and target) rows of each (unit, row block), by TMA with an
+//      evict-first policy (read once), 64-column boxes in the 128-byte-swizzled layout; rows
+//      that are not equally spaced (the final rows of rejection verification) come four at a
+//      time with tile::gather4 into the same layout.
 // The logit stream starts only once the first A block is in tensor memory, so that the W1
-// row gather is not queued behind it. The single MMA-issuing thread is the critical resource
-// (each mbarrier wait and tcgen05.commit costs it ~0.1 us), hence N = 128 instructions and
-// whole-tile B stages: it waits twice and commits twice per tile.
-// Warp roles (352 threads, one CTA per SM, persistent over a contiguous range of tiles):
+// row gather is not queued behind it.
+// Warp roles (352 threads, one CTA per SM, persistent over a contiguous range of units):
 //   warp 0  W2 (B operand) TMA producer;  warp 1  TMEM allocator + single-thread MMA issuer;
 //   warp 2  U / T tile producer;  warps 3..10  epilogue: warp w reads TMEM lanes 32*(w%4)..
 //   and column half (w-3)/4 of the tile.
@@ -41,16 +42,13 @@ namespace tc {
 constexpr int kBM = 128;                            // rows per tile (one MMA, 128 TMEM lanes)
 constexpr int kEpiWarps = 8;
 constexpr int kFirstEpi = 3;                       // warps 0..2: B producer, MMA, U/T producer
-constexpr int kIssuer2 = kFirstEpi + kEpiWarps;     // the second MMA issuer warp
-constexpr int kThreads = (kIssuer2 + 1) * 32;
+constexpr int kThreads = (kFirstEpi + kEpiWarps) * 32;
 constexpr long long kSpinCycles = 4000000000LL;  // ~2 s at the maximum SM clock
 constexpr uint32_t kBoxBytes = kBM * 128;         // one TMA box: 128 rows x 64 columns (bf16)
 
-// Per pass mode. Shared memory (A lives in tensor memory); a B stage holds a whole tile of W2 so
-// that the single MMA-issuing thread waits once and commits twice per tile:
-//   MODE_STATS: N = 128: B 2 x 64 KB + U 3 x 32 KB          = 224 KB; TMEM 3 x 128 + 128 cols
-//   MODE_TV / MODE_RESID: N = 64: B 3 x 32 KB + (U + T) 3 x 2 x 16 KB = 192 KB; TMEM 3 x 64 + 128
-// Three accumulator stages give the MMA thread slack against the epilogue's release of a stage.
+// Per pass mode. Shared memory (A lives in tensor memory):
+//   MODE_STATS: N = 128: B 2 x 64 KB + U 3 x 32 KB          = 224 KB; TMEM 2 x 128 + 2 x 128 cols
+//   MODE_TV / MODE_RESID: N = 64: B 3 x 32 KB + (U + T) 3 x 2 x 16 KB = 192 KB; TMEM 4 x 64 + 2 x 128
 template <int MODE>
 struct Cfg {
   static constexpr int kBN = MODE == MODE_STATS ? 128 : 64;  // vocabulary columns per tile
@@ -60,9 +58,11 @@ struct Cfg {
   static constexpr int kBStages = MODE == MODE_STATS ? 2 : 3;
   static constexpr uint32_t kTileBytes = kBoxes * kBoxBytes;
   static constexpr int kUStages = 3;
-  static constexpr int kAccStages = 3;                        // accumulator stages in TMEM
+  static constexpr int kAccStages = MODE == MODE_STATS ? 2 : 4;  // accumulator stages in TMEM
   static constexpr int kAccCols = kAccStages * kBN;
-  static constexpr int kTmemCols = 512;                       // accumulators + A (rank/2)
+  static constexpr int kACols = 128;                          // one A block (rank <= 256)
+  static constexpr int kTmemCols = 512;                       // accumulators + two A blocks
+  static_assert(kAccCols + 2 * kACols <= kTmemCols, "tensor memory budget");
   static constexpr int kSeg = kBN / 2;                        // columns per epilogue warp / partial
 };
 
@@ -383,6 +383,28 @@ struct TcParams {
   int nseg;  // partial segments per row (row-major partial arrays)
 };
 
+// Per-row normalisers of the pair modes for one row (loaded once per row block).
+template <int MODE>
+__device__ __forceinline__ void row_norms_tc(const RowJob& j, const TileRow& tr, Norm& dn,
+                                             Norm& tn, bool& resid) {
+  dn = {0.0f, 0.0f};
+  tn = {0.0f, 0.0f};
+  resid = true;
+  if (!tr.valid) return;
+  if constexpr (MODE == MODE_TV) {
+    tn = load_norm(j.tstats, (long long)tr.r * (j.gamma + 1) + (tr.k - 1));
+    dn = load_norm(j.dstats, (long long)tr.r * j.gamma + (tr.k - 1));
+  } else {
+    const int n = j.final_n[tr.r];
+    resid = j.final_kind[tr.r] != 0;
+    tn = load_norm(j.tstats, (long long)tr.r * (j.gamma + 1) + n);
+    if (resid) dn = load_norm(j.dstats, (long long)tr.r * j.gamma + n);
+  }
+}
+
+// Work unit: one column tile of W2 against a pair of row blocks (2*mp, 2*mp + 1; the last pair
+// of an odd count holds one block). The B tile is loaded once and feeds one MMA group per row
+// block, and both blocks' A operands stay in tensor memory while the CTA works on the pair.
 template <int MODE, bool ARGMAX, bool GATHER>
 __global__ void __launch_bounds__(kThreads, 1)
     markov_tc_kernel(const __grid_constant__ CUtensorMap map_w2,
@@ -390,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const __grid_constant__ CUtensorMap map_t, const TcParams P) {
   using C = Cfg<MODE>;
   constexpr int BN = C::kBN;
-  constexpr int KB = C::kBStages, KU = C::kUStages;
+  constexpr int KB = C::kBStages, KU = C::kUStages, KA = C::kAccStages;
   constexpr bool kPair = MODE != MODE_STATS;  // needs target tiles
   constexpr int kHalf = BN / 2;               // columns per epilogue warp
 
@@ -408,9 +430,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* u_full = b_empty + KB;
   uint64_t* u_empty = u_full + KU;
   uint64_t* acc_full = u_empty + KU;
-  uint64_t* acc_empty = acc_full + C::kAccStages;
-  uint64_t* a_full = acc_empty + C::kAccStages;
-  uint64_t* a_empty = a_full + 1;
+  uint64_t* acc_empty = acc_full + KA;
+  uint64_t* a_full = acc_empty + KA;  // [2]: A of the pair's first / second row block
+  uint64_t* a_empty = a_full + 2;
   uint64_t* drain = a_empty + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -418,10 +440,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint32_t* status = j.status;
 
-  // contiguous range of tiles for this CTA
-  const long long total = (long long)P.t.n_mt * P.t.n_nt;
-  const long long t_begin = total * blockIdx.x / gridDim.x;
-  const long long t_end = total * (blockIdx.x + 1) / gridDim.x;
+  // contiguous range of units for this CTA
+  const int n_nt = P.t.n_nt;
+  const int n_mp = (P.t.n_mt + 1) / 2;
+  const long long total = (long long)n_mp * n_nt;
+  const long long u_begin = total * blockIdx.x / gridDim.x;
+  const long long u_end = total * (blockIdx.x + 1) / gridDim.x;
+  const int mp_first = (int)(u_begin / n_nt), nt_first = (int)(u_begin % n_nt);
+  const int n_mt = P.t.n_mt;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < KB; ++s) {
@@ -432,13 +458,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&u_full[s], 1);
       mbar_init(&u_empty[s], kEpiWarps);
     }
-    for (int s = 0; s < C::kAccStages; ++s) {
+    for (int s = 0; s < KA; ++s) {
       mbar_init(&acc_full[s], 1);
       mbar_init(&acc_empty[s], kEpiWarps);
     }
-    mbar_init(a_full, kEpiWarps);
-    mbar_init(a_empty, 2);  // one arrival per MMA issuer
-    mbar_init(drain, 2);
+    mbar_init(&a_full[0], kEpiWarps);
+    mbar_init(&a_full[1], kEpiWarps);
+    mbar_init(a_empty, 1);
+    mbar_init(drain, 1);
     *abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -460,19 +487,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     int bs = 0;
     uint32_t bph = 0;
     bool ok = true;
-    constexpr int kPrefetch = 2;  // tiles ahead of the shared-memory ring, into L2
-    int nt = (int)(t_begin % P.t.n_nt), pf = nt;
+    constexpr int kPrefetch = 2;  // units ahead of the shared-memory ring, into L2
+    int nt = nt_first, pf = nt_first;
     if (lane == 0)
-      for (long long t = t_begin; t < t_begin + kPrefetch && t < t_end; ++t) {
+      for (long long u = u_begin; u < u_begin + kPrefetch && u < u_end; ++u) {
         for (int ka = 0; ka < ka_n; ++ka) tma_prefetch_2d(&map_w2, ka * 64, pf * BN, pol_keep);
-        if (++pf == P.t.n_nt) pf = 0;
+        if (++pf == n_nt) pf = 0;
       }
-    for (long long t = t_begin; t < t_end && ok; ++t) {
+    for (long long u = u_begin; u < u_end && ok; ++u) {
       const int n0 = nt * BN;
-      if (++nt == P.t.n_nt) nt = 0;
-      if (lane == 0 && t + kPrefetch < t_end)
+      if (++nt == n_nt) nt = 0;
+      if (lane == 0 && u + kPrefetch < u_end)
         for (int ka = 0; ka < ka_n; ++ka) tma_prefetch_2d(&map_w2, ka * 64, pf * BN, pol_keep);
-      if (t + kPrefetch < t_end && ++pf == P.t.n_nt) pf = 0;
+      if (u + kPrefetch < u_end && ++pf == n_nt) pf = 0;
       ok = mbar_wait(&b_empty[bs], bph ^ 1, abort, status);
       if (ok && lane == 0) {
         mbar_arrive_expect_tx(&b_full[bs], ka_n * C::kBAtomBytes);
@@ -492,109 +519,108 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t uph = 0;
     // start streaming logit rows once the first A block is in tensor memory: the W1 gather is
     // latency-bound and must not queue behind this stream
-    bool ok = t_begin >= t_end || mbar_wait(a_full, 0, abort, status);
-    int mt_c = (int)(t_begin / P.t.n_nt), nt_c = (int)(t_begin % P.t.n_nt);
-    for (long long t = t_begin; t < t_end && ok; ++t) {
-      const int mt = mt_c, nt = nt_c;
-      if (++nt_c == P.t.n_nt) { nt_c = 0; ++mt_c; }
+    bool ok = u_begin >= u_end || mbar_wait(&a_full[0], 0, abort, status);
+    int mp = mp_first, nt = nt_first;
+    for (long long u = u_begin; u < u_end && ok; ++u) {
       const int n0 = nt * BN;
-      ok = mbar_wait(&u_empty[us], uph ^ 1, abort, status);
-      if (!ok) break;
-      unsigned char* du = sU + us * C::kTileBytes;
-      unsigned char* dt = sT + us * C::kTileBytes;
-      if constexpr (!GATHER) {
-        if (lane == 0) {
-          const TileRow tr = tile_row(j, P.t, mt, 0);
-          const int r0 = tr.r, kk = tr.k - 1;
-          mbar_arrive_expect_tx(&u_full[us], (kPair ? 2u : 1u) * C::kTileBytes);
-          for (int b = 0; b < C::kBoxes; ++b) {
-            tma_load_3d(du + b * kBoxBytes, &map_u, n0 + b * 64, kk, r0, &u_full[us], pol_stream);
-            if constexpr (kPair)
-              tma_load_3d(dt + b * kBoxBytes, &map_t, n0 + b * 64, kk, r0, &u_full[us],
+      const int nb = 2 * mp + 1 < n_mt ? 2 : 1;
+      for (int sb = 0; sb < nb && ok; ++sb) {
+        const int mt = 2 * mp + sb;
+        ok = mbar_wait(&u_empty[us], uph ^ 1, abort, status);
+        if (!ok) break;
+        unsigned char* du = sU + us * C::kTileBytes;
+        unsigned char* dt = sT + us * C::kTileBytes;
+        if constexpr (!GATHER) {
+          if (lane == 0) {
+            const TileRow tr = tile_row(j, P.t, mt, 0);
+            const int r0 = tr.r, kk = tr.k - 1;
+            mbar_arrive_expect_tx(&u_full[us], (kPair ? 2u : 1u) * C::kTileBytes);
+            for (int b = 0; b < C::kBoxes; ++b) {
+              tma_load_3d(du + b * kBoxBytes, &map_u, n0 + b * 64, kk, r0, &u_full[us],
                           pol_stream);
+              if constexpr (kPair)
+                tma_load_3d(dt + b * kBoxBytes, &map_t, n0 + b * 64, kk, r0, &u_full[us],
+                            pol_stream);
+            }
           }
-        }
-      } else {
-        // final rows of rejection verification, four rows per tile::gather4 (lane g loads rows
-        // 4g..4g+3); rows past R and the U rows of bonus rows point at row 0 and are ignored
-        static_assert(C::kBoxes == 1, "gathered tiles are one box wide");
-        int tr4[4], ur4[4];
+        } else {
+          // final rows of rejection verification, four rows per tile::gather4 (lane g loads
+          // rows 4g..4g+3); rows past R and the U rows of bonus rows point at row 0 and are
+          // ignored
+          static_assert(C::kBoxes == 1, "gathered tiles are one box wide");
+          int tr4[4], ur4[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int r = mt * kBM + 4 * lane + e;
-          tr4[e] = 0;
-          ur4[e] = 0;
-          if (r < j.R) {
-            const int n = j.final_n[r];
-            tr4[e] = r * (j.gamma + 1) + n;
-            if (j.final_kind[r]) ur4[e] = r * j.gamma + n;
+          for (int e = 0; e < 4; ++e) {
+            const int r = mt * kBM + 4 * lane + e;
+            tr4[e] = 0;
+            ur4[e] = 0;
+            if (r < j.R) {
+              const int n = j.final_n[r];
+              tr4[e] = r * (j.gamma + 1) + n;
+              if (j.final_kind[r]) ur4[e] = r * j.gamma + n;
+            }
           }
+          if (lane == 0) mbar_arrive_expect_tx(&u_full[us], 2u * C::kTileBytes);
+          __syncwarp();
+          tma_gather4(dt + lane * 512, &map_t, n0, tr4[0], tr4[1], tr4[2], tr4[3], &u_full[us],
+                      pol_stream);
+          tma_gather4(du + lane * 512, &map_u, n0, ur4[0], ur4[1], ur4[2], ur4[3], &u_full[us],
+                      pol_stream);
         }
-        if (lane == 0) mbar_arrive_expect_tx(&u_full[us], 2u * C::kTileBytes);
-        __syncwarp();
-        tma_gather4(dt + lane * 512, &map_t, n0, tr4[0], tr4[1], tr4[2], tr4[3], &u_full[us],
-                    pol_stream);
-        tma_gather4(du + lane * 512, &map_u, n0, ur4[0], ur4[1], ur4[2], ur4[3], &u_full[us],
-                    pol_stream);
+        if (++us == KU) { us = 0; uph ^= 1; }
       }
-      if (++us == KU) { us = 0; uph ^= 1; }
+      if (++nt == n_nt) { nt = 0; ++mp; }
     }
     if (lane == 0)
       for (int s = 0; s < KU; ++s) mbar_drain(&u_full[s], (s < us) ? uph : (uph ^ 1));
-  } else if (warp == 1 || warp == kIssuer2) {
-    // ---------------------------------------------------------------- MMA issuers
-    // Two threads issue alternate tiles. Issuing blocks while the tensor pipe's queue is full,
-    // so one thread's barrier waits and bookkeeping overlap the other thread's MMAs.
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
     constexpr uint32_t idesc = idesc_bf16(kBM, BN);
-    const int p = warp == 1 ? 0 : 1;
     if (lane == 0) {
       bool ok = true;
-      int mt = (int)(t_begin / P.t.n_nt), nt = (int)(t_begin % P.t.n_nt);
-      int cur_mt = -1, blk = -1;
-      bool owned = false;  // this thread issued a tile of the current A block
-      const int n_local = (int)(t_end - t_begin);
-      for (int i = 0; i < n_local && ok; ++i) {
-        if (mt != cur_mt) {
-          // the A block is released once both issuers' MMAs on it are done; a thread that
-          // issued none of its tiles arrives directly (after a_full, so that its arrival
-          // belongs to this block's phase)
-          if (blk >= 0) {
-            if (owned) mma_commit(a_empty);
-            else mbar_arrive(a_empty);
-          }
-          ++blk;
-          owned = false;
-          cur_mt = mt;
-          ok = mbar_wait(a_full, blk & 1, abort, status);
-          if (!ok) break;
-          tc_fence_after();
+      int bs = 0, as = 0;
+      uint32_t bph = 0;
+      uint32_t accph[KA] = {};
+      int mp = mp_first, nt = nt_first, cur_mp = -1, pair_i = -1;
+      for (long long u = u_begin; u < u_end && ok; ++u) {
+        const int nb = 2 * mp + 1 < n_mt ? 2 : 1;
+        const bool first = mp != cur_mp;
+        if (first) {
+          cur_mp = mp;
+          ++pair_i;
         }
-        if (++nt == P.t.n_nt) { nt = 0; ++mt; }
-        if ((i & 1) != p) continue;
-        const int as = i % C::kAccStages, bs = i % KB;
-        ok = mbar_wait(&acc_empty[as], ((i / C::kAccStages) & 1) ^ 1, abort, status);
-        if (!ok) break;
-        ok = mbar_wait(&b_full[bs], (i / KB) & 1, abort, status);
+        ok = mbar_wait(&b_full[bs], bph, abort, status);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t d = tmem + as * BN;
-        for (int ka = 0; ka < ka_n; ++ka) {
-          const uint32_t b_base = smem_u32(sB + bs * C::kBStageBytes + ka * C::kBAtomBytes);
-          const uint32_t a = tmem + C::kAccCols + ka * 32;
-          // K = 16 per instruction: 8 tensor-memory columns of A, 32 bytes of a B row
+        for (int sb = 0; sb < nb && ok; ++sb) {
+          if (first) {
+            ok = mbar_wait(&a_full[sb], pair_i & 1, abort, status);
+            if (!ok) break;
+          }
+          ok = mbar_wait(&acc_empty[as], accph[as] ^ 1, abort, status);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t d = tmem + as * BN;
+          const uint32_t a = tmem + C::kAccCols + sb * C::kACols;
+          for (int ka = 0; ka < ka_n; ++ka) {
+            const uint32_t b_base = smem_u32(sB + bs * C::kBStageBytes + ka * C::kBAtomBytes);
+            // K = 16 per instruction: 8 tensor-memory columns of A, 32 bytes of a B row
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            mma_bf16_ta(d, a + ks * 8, sw128_desc(b_base + ks * 32), idesc, (ka | ks) != 0);
+            for (int ks = 0; ks < 4; ++ks)
+              mma_bf16_ta(d, a + ka * 32 + ks * 8, sw128_desc(b_base + ks * 32), idesc,
+                          (ka | ks) != 0);
+          }
+          mma_commit(&acc_full[as]);
+          accph[as] ^= 1;
+          if (++as == KA) as = 0;
         }
+        if (!ok) break;
         mma_commit(&b_empty[bs]);
-        mma_commit(&acc_full[as]);
-        owned = true;
+        if (++bs == KB) { bs = 0; bph ^= 1; }
+        if (++nt == n_nt) { nt = 0; ++mp; }
+        if (u + 1 == u_end || mp != cur_mp) mma_commit(a_empty);  // last unit of this pair
       }
-      if (ok && blk >= 0) {
-        if (owned) mma_commit(a_empty);
-        else mbar_arrive(a_empty);
-      }
-      // all MMAs issued by either thread complete before tensor memory is released
+      // all MMAs issued by this thread complete before tensor memory is released
       mma_commit(drain);
       mbar_drain(drain, 0);
     }
@@ -606,200 +632,194 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int h = ew >> 2;           // column half
     const int i = q * 32 + lane;     // row within the tile (TMEM lane)
     int as = 0, us = 0;
-    uint32_t accph[C::kAccStages] = {}, uph = 0, aeph = 0;
-    int cur_mt = -1;
+    uint32_t accph[KA] = {}, uph = 0, aeph = 0;
+    int mp = mp_first, nt = nt_first, cur_mp = -1;
     bool ok = true;
-    int mt_c = (int)(t_begin / P.t.n_nt), nt_c = (int)(t_begin % P.t.n_nt);
-    Norm dn = {0.0f, 0.0f}, tn = {0.0f, 0.0f};  // this row's softmax normalisers (pair modes)
-    bool resid = true;                          // residual (true) or bonus row (MODE_RESID)
-    for (long long t = t_begin; t < t_end && ok; ++t) {
-      const int mt = mt_c, nt = nt_c;
-      if (++nt_c == P.t.n_nt) { nt_c = 0; ++mt_c; }
+    // this row's normalisers in the pair's two row blocks (pair modes)
+    Norm dn0 = {0.0f, 0.0f}, tn0 = {0.0f, 0.0f}, dn1 = {0.0f, 0.0f}, tn1 = {0.0f, 0.0f};
+    bool rs0 = true, rs1 = true;
+    for (long long u = u_begin; u < u_end && ok; ++u) {
       const int n0 = nt * BN;
-      const TileRow tr = tile_row(j, P.t, mt, i);
-      if (mt != cur_mt) {
-        if (cur_mt >= 0) {
+      const int nb = 2 * mp + 1 < n_mt ? 2 : 1;
+      if (mp != cur_mp) {
+        if (cur_mp >= 0) {
           ok = mbar_wait(a_empty, aeph, abort, status);
           aeph ^= 1;
           if (!ok) break;
         }
-        cur_mt = mt;
-        // gather A into tensor memory: thread (q, h) owns row i and half h of its K; one load
-        // of the previous token, then all of its W1 chunks in flight, then tcgen05.st (a bad
-        // token is flagged afterwards)
-        int prev = 0;
-        if (tr.valid) {
-          if (j.map == MAP_FINAL) {
-            const int n = j.final_n[tr.r];
-            prev = n == 0 ? j.anchors[tr.r] : j.tokens[(size_t)tr.r * j.gamma + n - 1];
-          } else {
-            prev = tr.k == 1 ? j.anchors[tr.r] : j.tokens[(size_t)tr.r * j.gamma + tr.k - 2];
-          }
-        }
-        const bool bad = tr.valid && (prev < 0 || prev >= j.V);
-        const int per = j.rank / 16;  // 16-byte chunks of this thread's half row (<= 16)
-        const uint4* src = reinterpret_cast<const uint4*>(
-                               reinterpret_cast<const unsigned short*>(j.W1) +
-                               (size_t)(bad ? 0 : prev) * j.rank) + h * per;
-        uint32_t w[64];
-#pragma unroll
-        for (int it = 0; it < 16; ++it) {
-          const uint4 v = (tr.valid && it < per) ? __ldg(src + it) : make_uint4(0, 0, 0, 0);
-          w[4 * it] = v.x;
-          w[4 * it + 1] = v.y;
-          w[4 * it + 2] = v.z;
-          w[4 * it + 3] = v.w;
-        }
-        // chunk c of the half holds K elements 8c..8c+7 = columns 4c..4c+3 of the half
-        const uint32_t a_addr =
-            tmem + ((uint32_t)(q * 32) << 16) + C::kAccCols + h * (j.rank / 4);
-#pragma unroll
-        for (int b = 0; b < 4; ++b)
-          if (4 * b < per) tmem_st16(a_addr + 16 * b, w + 16 * b);
-        tmem_wait_st();
-        if (bad) atomicOr(status, SPEC_DEV_BAD_TOKEN);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(a_full);
-        // per-row normalisers, loaded once per row block
-        if constexpr (kPair) {
-          dn = {0.0f, 0.0f};
-          tn = {0.0f, 0.0f};
-          resid = true;
+        cur_mp = mp;
+        // gather A into tensor memory, one row block after the other: thread (q, h) owns row i
+        // and half h of its K; one load of the previous token, then all of its W1 chunks in
+        // flight, then tcgen05.st (a bad token is flagged afterwards)
+        for (int sb = 0; sb < nb; ++sb) {
+          const TileRow tr = tile_row(j, P.t, 2 * mp + sb, i);
+          int prev = 0;
           if (tr.valid) {
-            if constexpr (MODE == MODE_TV) {
-              tn = load_norm(j.tstats, (long long)tr.r * (j.gamma + 1) + (tr.k - 1));
-              dn = load_norm(j.dstats, (long long)tr.r * j.gamma + (tr.k - 1));
-            } else {
+            if (j.map == MAP_FINAL) {
               const int n = j.final_n[tr.r];
-              resid = j.final_kind[tr.r] != 0;
-              tn = load_norm(j.tstats, (long long)tr.r * (j.gamma + 1) + n);
-              if (resid) dn = load_norm(j.dstats, (long long)tr.r * j.gamma + n);
+              prev = n == 0 ? j.anchors[tr.r] : j.tokens[(size_t)tr.r * j.gamma + n - 1];
+            } else {
+              prev = tr.k == 1 ? j.anchors[tr.r] : j.tokens[(size_t)tr.r * j.gamma + tr.k - 2];
             }
+          }
+          const bool bad = tr.valid && (prev < 0 || prev >= j.V);
+          const int per = j.rank / 16;  // 16-byte chunks of this thread's half row (<= 16)
+          const uint4* src = reinterpret_cast<const uint4*>(
+                                 reinterpret_cast<const unsigned short*>(j.W1) +
+                                 (size_t)(bad ? 0 : prev) * j.rank) + h * per;
+          uint32_t w[64];
+#pragma unroll
+          for (int it = 0; it < 16; ++it) {
+            const uint4 v = (tr.valid && it < per) ? __ldg(src + it) : make_uint4(0, 0, 0, 0);
+            w[4 * it] = v.x;
+            w[4 * it + 1] = v.y;
+            w[4 * it + 2] = v.z;
+            w[4 * it + 3] = v.w;
+          }
+          // chunk c of the half holds K elements 8c..8c+7 = columns 4c..4c+3 of the half
+          const uint32_t a_addr = tmem + ((uint32_t)(q * 32) << 16) + C::kAccCols +
+                                  sb * C::kACols + h * (j.rank / 4);
+#pragma unroll
+          for (int b = 0; b < 4; ++b)
+            if (4 * b < per) tmem_st16(a_addr + 16 * b, w + 16 * b);
+          tmem_wait_st();
+          if (bad) atomicOr(status, SPEC_DEV_BAD_TOKEN);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&a_full[sb]);
+          if constexpr (kPair) {
+            if (sb == 0) row_norms_tc<MODE>(j, tr, dn0, tn0, rs0);
+            else row_norms_tc<MODE>(j, tr, dn1, tn1, rs1);
           }
         }
       }
       const int col0 = h * kHalf;  // first tile column of this warp
-      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + as * BN + col0;
       const bool tail = n0 + BN > j.V;
-      const bool live = tr.valid && n0 + col0 < j.V;
+#pragma unroll 1
+      for (int sb = 0; sb < nb && ok; ++sb) {
+        const TileRow tr = tile_row(j, P.t, 2 * mp + sb, i);
+        const bool live = tr.valid && n0 + col0 < j.V;
+        const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + as * BN + col0;
+        ok = mbar_wait(&acc_full[as], accph[as], abort, status);
+        if (!ok) break;
+        tc_fence_after();
+        ok = mbar_wait(&u_full[us], uph, abort, status);
+        if (!ok) break;
+        // TMEM reads and shared-memory reads first, then release the stages
+        uint32_t braw[kHalf];
+        tmem_ld32_async(taddr, braw);
+        if constexpr (kHalf == 64) tmem_ld32_async(taddr + 32, braw + 32);
+        const uint32_t u_base = smem_u32(sU + us * C::kTileBytes);
+        const uint32_t t_base = smem_u32(sT + us * C::kTileBytes);
+        uint4 uw[kHalf / 8], tw[kHalf / 8];
+#pragma unroll
+        for (int c = 0; c < kHalf / 8; ++c) {
+          const int col = col0 + 8 * c;
+          const int b = col >> 6, cc = (col & 63) >> 3;
+          const uint32_t off = b * kBoxBytes + i * 128 + ((cc ^ (i & 7)) << 4);
+          uw[c] = lds128(u_base + off);
+          if constexpr (kPair) tw[c] = lds128(t_base + off);
+        }
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&acc_empty[as]);
+          mbar_arrive(&u_empty[us]);
+        }
+        if (++us == KU) { us = 0; uph ^= 1; }
+        accph[as] ^= 1;
+        if (++as == KA) as = 0;
 
-      ok = mbar_wait(&acc_full[as], accph[as], abort, status);
-      if (!ok) break;
-      tc_fence_after();
-      ok = mbar_wait(&u_full[us], uph, abort, status);
-      if (!ok) break;
-      // TMEM reads and shared-memory reads first, then release the stages
-      uint32_t braw[kHalf];
-      tmem_ld32_async(taddr, braw);
-      if constexpr (kHalf == 64) tmem_ld32_async(taddr + 32, braw + 32);
-      const uint32_t u_base = smem_u32(sU + us * C::kTileBytes);
-      const uint32_t t_base = smem_u32(sT + us * C::kTileBytes);
-      uint4 uw[kHalf / 8], tw[kHalf / 8];
+        const size_t o = (size_t)tr.prow * P.nseg + (n0 + col0) / kHalf;
+        if constexpr (MODE == MODE_STATS) {
+          // z = (bias + U) * scale, two columns per instruction
+          const unsigned long long sc2 = pack2(j.scale, j.scale);
+          float z[64];
 #pragma unroll
-      for (int c = 0; c < kHalf / 8; ++c) {
-        const int col = col0 + 8 * c;
-        const int b = col >> 6, cc = (col & 63) >> 3;
-        const uint32_t off = b * kBoxBytes + i * 128 + ((cc ^ (i & 7)) << 4);
-        uw[c] = lds128(u_base + off);
-        if constexpr (kPair) tw[c] = lds128(t_base + off);
-      }
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&acc_empty[as]);
-        mbar_arrive(&u_empty[us]);
-      }
-      if (++us == KU) { us = 0; uph ^= 1; }
-      accph[as] ^= 1;
-      if (++as == C::kAccStages) as = 0;
-
-      const size_t o = (size_t)tr.prow * P.nseg + (n0 + col0) / kHalf;
-      if constexpr (MODE == MODE_STATS) {
-        // z = (bias + U) * scale, two columns per instruction
-        const unsigned long long sc2 = pack2(j.scale, j.scale);
-        float z[64];
+          for (int c = 0; c < 8; ++c) {
+            const uint32_t wv[4] = {uw[c].x, uw[c].y, uw[c].z, uw[c].w};
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint32_t w[4] = {uw[c].x, uw[c].y, uw[c].z, uw[c].w};
-#pragma unroll
-          for (int p = 0; p < 4; ++p) {
-            const int e = 8 * c + 2 * p;
-            const unsigned long long u2 =
-                pack2(__uint_as_float(w[p] << 16), __uint_as_float(w[p] & 0xffff0000u));
-            const unsigned long long b2 =
-                pack2(__uint_as_float(braw[e]), __uint_as_float(braw[e + 1]));
-            unpack2(mul2(add2(b2, u2), sc2), z[e], z[e + 1]);
-          }
-        }
-        if (tail) {
-#pragma unroll
-          for (int e = 0; e < 64; ++e)
-            if (n0 + col0 + e >= j.V) z[e] = -INFINITY;
-        }
-        // maximum (3-input tree) and, for greedy, its first position
-        float t22[22];
-#pragma unroll
-        for (int e = 0; e < 21; ++e) t22[e] = max3(z[3 * e], z[3 * e + 1], z[3 * e + 2]);
-        t22[21] = z[63];
-        float t8[8];
-#pragma unroll
-        for (int e = 0; e < 7; ++e) t8[e] = max3(t22[3 * e], t22[3 * e + 1], t22[3 * e + 2]);
-        t8[7] = t22[21];
-        const float m = max3(max3(t8[0], t8[1], t8[2]), max3(t8[3], t8[4], t8[5]),
-                             fmaxf(t8[6], t8[7]));
-        int idx = 0x7fffffff;
-        if (ARGMAX) {
-#pragma unroll
-          for (int e = 63; e >= 0; --e)
-            if (z[e] == m) idx = n0 + col0 + e;
-        }
-        // sum of exp(z - m): 2^(fma(z, log2e, -fl(m log2e))) carries the common factor 2^delta
-        // (delta = the exact rounding error of m log2e), removed once per partial below
-        float s = 0.0f;
-        if (m > -INFINITY) {
-          const float nml = -(m * kLog2e);
-          const float delta = fmaf(m, kLog2e, nml);
-          const unsigned long long l2 = pack2(kLog2e, kLog2e), n2 = pack2(nml, nml);
-          float acc4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-          for (int e = 0; e < 64; e += 2) {
-            float a, b;
-            unpack2(fma2(pack2(z[e], z[e + 1]), l2, n2), a, b);
-            acc4[(e >> 1) & 3] += fast_exp2(a) + fast_exp2(b);
-          }
-          s = ((acc4[0] + acc4[1]) + (acc4[2] + acc4[3])) * (1.0f - delta * kLn2);
-        }
-        if (live) {
-          P.pm[o] = m;
-          P.ps[o] = s;
-          if (ARGMAX) P.pi[o] = idx;
-        }
-      } else {
-        if (live) {
-          float sum = 0.0f;
-#pragma unroll
-          for (int c = 0; c < kHalf / 8; ++c) {
-            float u[8], tv[8];
-            unpack_bf16x8(tw[c], tv);
-            unpack_bf16x8(uw[c], u);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const int v = n0 + col0 + c * 8 + e;
-              if (tail && v >= j.V) continue;
-              const float pt = prob_of(tv[e] * j.scale, tn);
-              if (MODE == MODE_RESID && !resid) {
-                sum += pt;
-                continue;
-              }
-              const float pd = prob_of((u[e] + __uint_as_float(braw[c * 8 + e])) * j.scale, dn);
-              sum += MODE == MODE_RESID ? fmaxf(pt - pd, 0.0f) : fminf(pt, pd);
+            for (int p = 0; p < 4; ++p) {
+              const int e = 8 * c + 2 * p;
+              const unsigned long long u2 =
+                  pack2(__uint_as_float(wv[p] << 16), __uint_as_float(wv[p] & 0xffff0000u));
+              const unsigned long long b2 =
+                  pack2(__uint_as_float(braw[e]), __uint_as_float(braw[e + 1]));
+              unpack2(mul2(add2(b2, u2), sc2), z[e], z[e + 1]);
             }
           }
-          P.ps[o] = sum;
+          if (tail) {
+#pragma unroll
+            for (int e = 0; e < 64; ++e)
+              if (n0 + col0 + e >= j.V) z[e] = -INFINITY;
+          }
+          // maximum (3-input tree) and, for greedy, its first position
+          float t22[22];
+#pragma unroll
+          for (int e = 0; e < 21; ++e) t22[e] = max3(z[3 * e], z[3 * e + 1], z[3 * e + 2]);
+          t22[21] = z[63];
+          float t8[8];
+#pragma unroll
+          for (int e = 0; e < 7; ++e) t8[e] = max3(t22[3 * e], t22[3 * e + 1], t22[3 * e + 2]);
+          t8[7] = t22[21];
+          const float m = max3(max3(t8[0], t8[1], t8[2]), max3(t8[3], t8[4], t8[5]),
+                               fmaxf(t8[6], t8[7]));
+          int idx = 0x7fffffff;
+          if (ARGMAX) {
+#pragma unroll
+            for (int e = 63; e >= 0; --e)
+              if (z[e] == m) idx = n0 + col0 + e;
+          }
+          // sum of exp(z - m): 2^(fma(z, log2e, -fl(m log2e))) carries the common factor
+          // 2^delta (delta = the exact rounding error of m log2e), removed once per partial
+          float s = 0.0f;
+          if (m > -INFINITY) {
+            const float nml = -(m * kLog2e);
+            const float delta = fmaf(m, kLog2e, nml);
+            const unsigned long long l2 = pack2(kLog2e, kLog2e), n2 = pack2(nml, nml);
+            float acc4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+            for (int e = 0; e < 64; e += 2) {
+              float a, b;
+              unpack2(fma2(pack2(z[e], z[e + 1]), l2, n2), a, b);
+              acc4[(e >> 1) & 3] += fast_exp2(a) + fast_exp2(b);
+            }
+            s = ((acc4[0] + acc4[1]) + (acc4[2] + acc4[3])) * (1.0f - delta * kLn2);
+          }
+          if (live) {
+            P.pm[o] = m;
+            P.ps[o] = s;
+            if (ARGMAX) P.pi[o] = idx;
+          }
+        } else {
+          const Norm dn = sb ? dn1 : dn0, tn = sb ? tn1 : tn0;
+          const bool resid = sb ? rs1 : rs0;
+          if (live) {
+            float sum = 0.0f;
+#pragma unroll
+            for (int c = 0; c < kHalf / 8; ++c) {
+              float uv[8], tv[8];
+              unpack_bf16x8(tw[c], tv);
+              unpack_bf16x8(uw[c], uv);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const int v = n0 + col0 + c * 8 + e;
+                if (tail && v >= j.V) continue;
+                const float pt = prob_of(tv[e] * j.scale, tn);
+                if (MODE == MODE_RESID && !resid) {
+                  sum += pt;
+                  continue;
+                }
+                const float pd = prob_of((uv[e] + __uint_as_float(braw[c * 8 + e])) * j.scale, dn);
+                sum += MODE == MODE_RESID ? fmaxf(pt - pd, 0.0f) : fminf(pt, pd);
+              }
+            }
+            P.ps[o] = sum;
+          }
         }
       }
+      if (++nt == n_nt) { nt = 0; ++mp; }
     }
   }
 
@@ -896,7 +916,8 @@ cudaError_t launch_markov_tc(const RowJob& j, float* pm, float* ps, int* pi, boo
   p.t.n_mt = j.map == MAP_ALL_POS ? rb * j.gamma : rb;
   p.t.n_nt = (j.V + BN - 1) / BN;
   p.nseg = (j.V + BN / 2 - 1) / (BN / 2);
-  const long long total = (long long)p.t.n_mt * p.t.n_nt;
+  // work units: one column tile against a pair of row blocks
+  const long long total = (long long)((p.t.n_mt + 1) / 2) * p.t.n_nt;
   if (total == 0) return cudaSuccess;
   const int grid = (int)(total < num_sms() ? total : num_sms());
 
