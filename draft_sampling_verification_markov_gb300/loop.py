@@ -1,0 +1,107 @@
+"""Device-resident draft -> verify loop.
+
+One iteration is the whole token-level hot path of "[DeepSeek-6] DSpark": the Markov head's
+serial proposal (section 3 and section 4 "Markov Head"), the target normalisers, the TV
+confidence labels and their prefix survival (section 5, section 6), the hardware-aware prefix
+scheduler's lengths (section 6), and lossless rejection verification of the scheduled prefixes
+(speculative sampling with the residual / bonus draw). The token each request emits at the end
+of iteration t (its residual or bonus draw) is the anchor x_0 of iteration t + 1; iteration t
+reads slice t of the pre-drawn uniforms. The logit tensors stay fixed across iterations (the
+models that would produce new logits are outside this library).
+
+Every step is a call into libspecmarkov (argument marshalling only), and the iterations can be
+captured into one CUDA graph so that no host round trip separates them.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import spec as S
+
+
+class SpecLoop:
+    """`iterations` chained draft -> verify iterations over fixed logits.
+
+    U [R, gamma, V] and target [R, gamma + 1, V] (bf16 or fp32), W1 / W2 [V, rank], anchors0
+    [R] int32, uniforms u_draft / u_accept [iters, R, gamma] and u_resid [iters, R] fp32,
+    sps [Bmax + 1] fp64 (index = batch size B). With schedule=False every request verifies
+    all gamma positions (no confidence pass, no scheduler)."""
+
+    def __init__(self, U, target, W1, W2, anchors0, u_draft, u_accept, u_resid, temperature,
+                 sps=None, *, iterations=None, schedule=True):
+        R, gamma, V = U.shape
+        self.R, self.gamma, self.V = R, gamma, V
+        self.iters = int(iterations if iterations is not None else u_draft.shape[0])
+        self.U, self.target, self.W1, self.W2 = U, target, W1, W2
+        self.u_draft, self.u_accept, self.u_resid = u_draft, u_accept, u_resid
+        self.temperature = float(temperature)
+        self.sps = sps
+        self.schedule = bool(schedule) and sps is not None
+        self.rank = 0 if W1 is None else int(W1.shape[1])
+        dev = U.device
+        i32 = dict(dtype=torch.int32, device=dev)
+        f32 = dict(dtype=torch.float32, device=dev)
+        n = self.iters
+        self.anchors = torch.empty(n + 1, R, **i32)
+        self.anchors[0].copy_(anchors0)
+        self.draft_tokens = torch.empty(n, R, gamma, **i32)
+        self.draft_logp = torch.empty(R, gamma, **f32)
+        self.draft_stats = torch.empty(R, gamma, 2, **f32)
+        self.target_stats = torch.empty(R * (gamma + 1), 2, **f32)
+        self.conf = torch.empty(n, R, gamma, **f32)
+        self.survival = torch.empty(n, R, gamma, **f32)
+        self.lengths = torch.empty(n, R, **i32)
+        self.batch = torch.empty(n, **i32)
+        self.theta = torch.empty(n, dtype=torch.float64, device=dev)
+        self.accept_len = torch.empty(n, R, **i32)
+        self.out_tokens = torch.empty(n, R, gamma + 1, **i32)
+        # one workspace large enough for every step, reserved before any capture
+        self.ws = S.Workspace(device=dev)
+        self.ws.reserve(int(S.lib().spec_workspace_bytes(S.SPEC_OP_ALL, R, gamma, V, self.rank)))
+        self.graph = None
+
+    def iteration(self, t: int, stream=None):
+        """Enqueue iteration t on `stream` (the current stream by default)."""
+        ws, T = self.ws, self.temperature
+        a_t = self.anchors[t]
+        S.spec_markov_propose(self.U, self.W1, self.W2, a_t, self.u_draft[t], T,
+                              draft_tokens=self.draft_tokens[t], draft_logp=self.draft_logp,
+                              draft_stats=self.draft_stats, workspace=ws, stream=stream)
+        S.spec_target_stats(self.target, T, stats=self.target_stats, workspace=ws, stream=stream)
+        lengths = None
+        if self.schedule:
+            S.spec_tv_confidence(self.U, self.target, self.W1, self.W2, a_t,
+                                 self.draft_tokens[t], T, draft_stats=self.draft_stats,
+                                 target_stats=self.target_stats, conf=self.conf[t],
+                                 survival=self.survival[t], workspace=ws, stream=stream)
+            S.spec_schedule_prefix(self.survival[t], self.sps, lengths=self.lengths[t],
+                                   B_out=self.batch[t:t + 1], theta_out=self.theta[t:t + 1],
+                                   workspace=ws, stream=stream)
+            lengths = self.lengths[t]
+        S.spec_verify_rejection(self.target, self.U, self.W1, self.W2, a_t, self.draft_tokens[t],
+                                self.draft_logp, self.draft_stats, self.u_accept[t],
+                                self.u_resid[t], T, lengths, target_stats=self.target_stats,
+                                accept_len=self.accept_len[t], out_tokens=self.out_tokens[t],
+                                next_anchor=self.anchors[t + 1], workspace=ws, stream=stream)
+
+    def run(self, stream=None):
+        """All iterations, enqueued eagerly."""
+        for t in range(self.iters):
+            self.iteration(t, stream)
+
+    def capture(self):
+        """Record all iterations into one CUDA graph (replay with replay())."""
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.run()
+        self.graph = g
+        return g
+
+    def replay(self):
+        if self.graph is None:
+            self.capture()
+        self.graph.replay()
+
+    def emitted_tokens(self) -> torch.Tensor:
+        """Tokens emitted per iteration and request: the accepted prefix plus one draw."""
+        return self.accept_len + 1

@@ -1,0 +1,106 @@
+"""The device-resident draft -> verify loop (accepted prefix + emitted token; the emitted token
+is the next iteration's anchor) against the oracle, iteration by iteration.
+
+Each iteration is checked given the GPU's own state entering it (its anchors), so a sampled
+token that legitimately differs at a CDF near-tie does not make the rest of the chain
+incomparable: proposals, confidences, survival, scheduler lengths and verification outputs of
+iteration t are compared with the oracle run on the GPU's anchors, draft tokens, survival and
+lengths of iteration t."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from draft_sampling_verification_markov_gb300 import workloads as W
+from gpu_util import assert_conf_close, compare_proposals
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def spec():
+    import __graft_entry__
+    __graft_entry__.build()
+    from draft_sampling_verification_markov_gb300 import spec as s
+    return s
+
+
+def _loop(spec, wl, schedule=True):
+    from draft_sampling_verification_markov_gb300.loop import SpecLoop
+    g = {k: v.cuda() for k, v in wl.tensors().items()}
+    return SpecLoop(g["U"], g["target"], g["W1"], g["W2"], g["anchors"], g["u_draft"],
+                    g["u_accept"], g["u_resid"], wl.temperature, g.get("sps"),
+                    schedule=schedule)
+
+
+def check_iteration(lp, wl, t, sample=None, report=None):
+    """Teacher-forced oracle check of iteration t on the requests in `sample` (all by default)."""
+    R = wl.R
+    sample = list(range(R)) if sample is None else list(sample)
+    sl = lambda x: x[sample].cpu()
+    a_t = lp.anchors[t][sample].cpu()
+    toks = lp.draft_tokens[t][sample].cpu()
+    ref = oracle.markov_propose(sl(wl.U), wl.W1.cpu(), wl.W2.cpu(), a_t, sl(wl.u_draft[t]),
+                                wl.temperature)
+    # propose writes draft_logp / draft_stats only for the last iteration run; compare tokens
+    # (margin rule) here and the probabilities through the confidence pass below
+    compare_proposals(toks, None, None, ref, report=report)
+    tv = oracle.tv_confidence(sl(wl.U), sl(wl.target), wl.W1.cpu(), wl.W2.cpu(), a_t, toks,
+                              wl.temperature)
+    if lp.schedule:
+        assert_conf_close(lp.conf[t][sample], tv["conf"])
+        assert_conf_close(lp.survival[t][sample], tv["survival"], "survival")
+        # the scheduler sees every request: bit-exact on the GPU's survival
+        sch = oracle.schedule_prefix(lp.survival[t].cpu(), wl.sps.cpu().numpy())
+        np.testing.assert_array_equal(lp.lengths[t].cpu().numpy(), sch["lengths"])
+        assert int(lp.batch[t].item()) == sch["B"]
+        assert float(lp.theta[t].item()) == sch["theta"]
+        lengths = lp.lengths[t][sample].cpu()
+    else:
+        lengths = None
+    rv = oracle.verify_rejection(sl(wl.target), sl(wl.U), wl.W1.cpu(), wl.W2.cpu(), a_t, toks,
+                                 sl(wl.u_accept[t]), sl(wl.u_resid[t]), wl.temperature, lengths)
+    n = lp.accept_len[t][sample].cpu().numpy()
+    o = lp.out_tokens[t][sample].cpu().numpy()
+    nxt = lp.anchors[t + 1][sample].cpu().numpy()
+    amb = (np.nan_to_num(rv["accept_margin"], nan=1.0) < 1e-6).any(axis=1) | (
+        rv["resid_margin"] < 1e-6)
+    diff = (n != rv["accept_len"]) | (o != rv["out_tokens"]).any(axis=1) | (
+        nxt != rv["next_anchor"])
+    assert not (diff & ~amb).any(), f"iteration {t}: verify differs for {np.nonzero(diff & ~amb)}"
+    # the emitted token is the next anchor
+    np.testing.assert_array_equal(nxt, o[np.arange(len(sample)), n])
+    if report is not None:
+        report["verify_margin_cases"] = report.get("verify_margin_cases", 0) + int((diff & amb).sum())
+
+
+@pytest.mark.parametrize("schedule", [True, False])
+def test_loop_matches_oracle_iteration_by_iteration(spec, schedule):
+    wl = W.full_loop("cpu", R=6, gamma=4, V=1040, rank=64, iterations=3, seed=31)
+    lp = _loop(spec, wl, schedule)
+    lp.run()
+    torch.cuda.synchronize()
+    assert lp.ws.status() == 0
+    report = {}
+    for t in range(wl.iterations):
+        check_iteration(lp, wl, t, report=report)
+    if not schedule:
+        assert (lp.accept_len <= wl.gamma).all()
+
+
+def test_loop_graph_replay_equals_eager(spec):
+    wl = W.full_loop("cpu", R=70, gamma=5, V=2048, rank=128, iterations=4, seed=32)
+    eager = _loop(spec, wl)
+    eager.run()
+    graph = _loop(spec, wl)
+    graph.capture()
+    graph.replay()
+    torch.cuda.synchronize()
+    for name in ("anchors", "draft_tokens", "conf", "survival", "lengths", "accept_len",
+                 "out_tokens", "theta"):
+        assert torch.equal(getattr(eager, name), getattr(graph, name)), name
+    first = graph.out_tokens.clone()
+    graph.replay()                       # replays start again from anchors[0]
+    torch.cuda.synchronize()
+    assert torch.equal(first, graph.out_tokens)
+    assert eager.ws.status() == 0 and graph.ws.status() == 0
