@@ -137,8 +137,8 @@ class ClockSampler:
 # ----------------------------------------------------------------------------- profile traffic
 
 def recorded_traffic(kernel_class):
-    """DRAM bytes per launch of the dominant kernel from the committed ncu summary
-    (profiles/traffic.json), or None if absent or taken on a different kernel source."""
+    """DRAM bytes per launch of the dominant kernel class from the committed ncu summary
+    (profiles/traffic.json), or None if absent or taken on different kernel sources."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
@@ -148,11 +148,13 @@ def recorded_traffic(kernel_class):
         return None
     if not rec:
         return None
-    src = os.path.join(ROOT, rec.get("source", ""))
-    if not os.path.exists(src):
-        return None
-    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    if h != rec.get("source_sha256_16"):
+    blob = b""
+    for src in rec.get("sources", []):
+        f = os.path.join(ROOT, src)
+        if not os.path.exists(f):
+            return None
+        blob += open(f, "rb").read()
+    if hashlib.sha256(blob).hexdigest()[:16] != rec.get("sources_sha256_16"):
         return None
     return rec.get("dram_bytes_per_launch")
 
