@@ -53,6 +53,26 @@ def dist_env():
     return rank, world, local
 
 
+def replica_seed(base, rank):
+    """Each replica (one rank per GPU) draws its own workload of the same shape."""
+    return base + 100 * rank
+
+
+def max_over_ranks(x, dist=None, device="cpu"):
+    """The maximum of a per-rank time over all ranks (the timing rule for N > 1)."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_step, steps, world, ms):
+    """Units of all ranks per second of the slowest rank."""
+    return units_per_step * steps * world / (ms / 1e3)
+
+
 def config_dict(extra=None):
     c = {"workload": "markov_rejection: Markov-head sampling + rejection verify, R=256 gamma=7 "
                      "V=129280 rank=256 bf16 T=1",
@@ -246,7 +266,8 @@ def main():
 
     W = WORKLOAD
     wl = workloads.markov_rejection("cuda", R=W["R"], gamma=W["gamma"], V=W["V"], rank=W["rank"],
-                                    seed=W["seed"] + 100 * rank, temperature=W["temperature"])
+                                    seed=replica_seed(W["seed"], rank),
+                                    temperature=W["temperature"])
     R, g, V = W["R"], W["gamma"], W["V"]
     T = W["temperature"]
     stream = torch.cuda.Stream(device=dev)
@@ -321,14 +342,10 @@ def main():
     counts = {kc: spec.lib().spec_trace_count(kc) for kc in range(4)}
     for kc in range(4):
         spec.lib().spec_trace_events(kc, None, None, 0)
-    ms = t_start.elapsed_time(t_end)
-    if pg:
-        t = torch.tensor([ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(t_start.elapsed_time(t_end), pg, dev)
     assert ws.status() == 0, "device status word set during the timed region"
     rows_per_step = R * (2 * g + 1)
-    value = rows_per_step * args.steps * world / (ms / 1e3)
+    value = whole_job_rate(rows_per_step, args.steps, world, ms)
 
     # dominant kernel class by total device time over the timed region
     totals = {}
@@ -386,12 +403,8 @@ def main():
                 e2e_step()
         b.record(stream)
         torch.cuda.synchronize()
-        e_ms = a.elapsed_time(b)
-        if pg:
-            t = torch.tensor([e_ms], device=dev)
-            pg.all_reduce(t, op=pg.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = {"value": rows_per_step * args.e2e_steps * world / (e_ms / 1e3), "unit": UNIT,
+        e_ms = max_over_ranks(a.elapsed_time(b), pg, dev)
+        e2e = {"value": whole_job_rate(rows_per_step, args.e2e_steps, world, e_ms), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e_ms / args.e2e_steps}
 
