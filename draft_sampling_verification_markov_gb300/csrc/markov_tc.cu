@@ -520,10 +520,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     // start streaming logit rows once the first A block is in tensor memory: the W1 gather is
     // latency-bound and must not queue behind this stream
     bool ok = u_begin >= u_end || mbar_wait(&a_full[0], 0, abort, status);
-    int mp = mp_first, nt = nt_first;
+    int mp = mp_first, nt = nt_first, rows_mp = -1;
+    // gathered row indices of the pair's two row blocks (lane g: rows 4g..4g+3), loaded once
+    // per pair: rows past R and the U rows of bonus rows point at row 0 and are ignored
+    int trA[4] = {}, urA[4] = {}, trB[4] = {}, urB[4] = {};
     for (long long u = u_begin; u < u_end && ok; ++u) {
       const int n0 = nt * BN;
       const int nb = 2 * mp + 1 < n_mt ? 2 : 1;
+      if constexpr (GATHER) {
+        if (mp != rows_mp) {
+          rows_mp = mp;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int ra = (2 * mp) * kBM + 4 * lane + e, rb = ra + kBM;
+            trA[e] = urA[e] = trB[e] = urB[e] = 0;
+            if (ra < j.R) {
+              const int n = j.final_n[ra];
+              trA[e] = ra * (j.gamma + 1) + n;
+              if (j.final_kind[ra]) urA[e] = ra * j.gamma + n;
+            }
+            if (nb == 2 && rb < j.R) {
+              const int n = j.final_n[rb];
+              trB[e] = rb * (j.gamma + 1) + n;
+              if (j.final_kind[rb]) urB[e] = rb * j.gamma + n;
+            }
+          }
+        }
+      }
       for (int sb = 0; sb < nb && ok; ++sb) {
         const int mt = 2 * mp + sb;
         ok = mbar_wait(&u_empty[us], uph ^ 1, abort, status);
@@ -545,27 +568,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         } else {
           // final rows of rejection verification, four rows per tile::gather4 (lane g loads
-          // rows 4g..4g+3); rows past R and the U rows of bonus rows point at row 0 and are
-          // ignored
+          // rows 4g..4g+3 of the row block)
           static_assert(C::kBoxes == 1, "gathered tiles are one box wide");
-          int tr4[4], ur4[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int r = mt * kBM + 4 * lane + e;
-            tr4[e] = 0;
-            ur4[e] = 0;
-            if (r < j.R) {
-              const int n = j.final_n[r];
-              tr4[e] = r * (j.gamma + 1) + n;
-              if (j.final_kind[r]) ur4[e] = r * j.gamma + n;
-            }
-          }
           if (lane == 0) mbar_arrive_expect_tx(&u_full[us], 2u * C::kTileBytes);
           __syncwarp();
-          tma_gather4(dt + lane * 512, &map_t, n0, tr4[0], tr4[1], tr4[2], tr4[3], &u_full[us],
-                      pol_stream);
-          tma_gather4(du + lane * 512, &map_u, n0, ur4[0], ur4[1], ur4[2], ur4[3], &u_full[us],
-                      pol_stream);
+          if (sb == 0) {
+            tma_gather4(dt + lane * 512, &map_t, n0, trA[0], trA[1], trA[2], trA[3], &u_full[us],
+                        pol_stream);
+            tma_gather4(du + lane * 512, &map_u, n0, urA[0], urA[1], urA[2], urA[3], &u_full[us],
+                        pol_stream);
+          } else {
+            tma_gather4(dt + lane * 512, &map_t, n0, trB[0], trB[1], trB[2], trB[3], &u_full[us],
+                        pol_stream);
+            tma_gather4(du + lane * 512, &map_u, n0, urB[0], urB[1], urB[2], urB[3], &u_full[us],
+                        pol_stream);
+          }
         }
         if (++us == KU) { us = 0; uph ^= 1; }
       }
@@ -796,7 +813,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const Norm dn = sb ? dn1 : dn0, tn = sb ? tn1 : tn0;
           const bool resid = sb ? rs1 : rs0;
           if (live) {
-            float sum = 0.0f;
+            // branch-free: every column's two probabilities are computed, then selected, so
+            // that the exponentials of all columns overlap; four partial sums
+            float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            const int vb = n0 + col0;
 #pragma unroll
             for (int c = 0; c < kHalf / 8; ++c) {
               float uv[8], tv[8];
@@ -804,18 +824,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               unpack_bf16x8(uw[c], uv);
 #pragma unroll
               for (int e = 0; e < 8; ++e) {
-                const int v = n0 + col0 + c * 8 + e;
-                if (tail && v >= j.V) continue;
                 const float pt = prob_of(tv[e] * j.scale, tn);
-                if (MODE == MODE_RESID && !resid) {
-                  sum += pt;
-                  continue;
-                }
                 const float pd = prob_of((uv[e] + __uint_as_float(braw[c * 8 + e])) * j.scale, dn);
-                sum += MODE == MODE_RESID ? fmaxf(pt - pd, 0.0f) : fminf(pt, pd);
+                float x;
+                if constexpr (MODE == MODE_TV) x = fminf(pt, pd);
+                else x = fmaxf(pt - (resid ? pd : 0.0f), 0.0f);  // bonus rows: p_t
+                acc[e & 3] += (!tail || vb + c * 8 + e < j.V) ? x : 0.0f;
               }
             }
-            P.ps[o] = sum;
+            P.ps[o] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
           }
         }
       }
