@@ -48,16 +48,16 @@ constexpr uint32_t kBoxBytes = kBM * 128;         // one TMA box: 128 rows x 64 
 
 // Per pass mode. Shared memory (A lives in tensor memory):
 //   MODE_STATS: N = 128: B 2 x 64 KB + U 3 x 32 KB          = 224 KB; TMEM 2 x 128 + 2 x 128 cols
-//   MODE_TV / MODE_RESID: N = 64: B 3 x 32 KB + (U + T) 3 x 2 x 16 KB = 192 KB; TMEM 4 x 64 + 2 x 128
+//   MODE_TV / MODE_RESID: N = 64: B 2 x 32 KB + (U + T) 4 x 2 x 16 KB = 192 KB; TMEM 4 x 64 + 2 x 128
 template <int MODE>
 struct Cfg {
   static constexpr int kBN = MODE == MODE_STATS ? 128 : 64;  // vocabulary columns per tile
   static constexpr int kBoxes = kBN / 64;                     // 64-column boxes per logit tile
   static constexpr uint32_t kBAtomBytes = kBN * 128;          // kBN W2 rows x 64 K
   static constexpr uint32_t kBStageBytes = 4 * kBAtomBytes;   // K <= 256
-  static constexpr int kBStages = MODE == MODE_STATS ? 2 : 3;
+  static constexpr int kBStages = 2;
   static constexpr uint32_t kTileBytes = kBoxes * kBoxBytes;
-  static constexpr int kUStages = 3;
+  static constexpr int kUStages = MODE == MODE_STATS ? 3 : 4;
   static constexpr int kAccStages = MODE == MODE_STATS ? 2 : 4;  // accumulator stages in TMEM
   static constexpr int kAccCols = kAccStages * kBN;
   static constexpr int kACols = 128;                          // one A block (rank <= 256)
@@ -174,6 +174,20 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)),
       "l"(policy)
       : "memory");
+}
+
+// 16 bytes global -> shared, asynchronous; src_bytes 0 writes zeros without reading.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+
+// Arrive on `bar` once this thread's earlier cp.async copies have landed (no pending-count
+// increment: the barrier's expected count includes this thread).
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
 }
 
 __device__ __forceinline__ void fence_async_smem() {
@@ -436,6 +450,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* drain = a_empty + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // gathered modes: T and U row indices of the pair's two row blocks, [block][row]
+  int* row_t = reinterpret_cast<int*>(tail + 256);
+  int* row_u = row_t + 2 * kBM;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint32_t* status = j.status;
@@ -455,7 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&b_empty[s], 1);
     }
     for (int s = 0; s < KU; ++s) {
-      mbar_init(&u_full[s], 1);
+      mbar_init(&u_full[s], GATHER ? 32 : 1);  // gathered rows: one arrival per producer lane
       mbar_init(&u_empty[s], kEpiWarps);
     }
     for (int s = 0; s < KA; ++s) {
@@ -521,30 +538,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     // latency-bound and must not queue behind this stream
     bool ok = u_begin >= u_end || mbar_wait(&a_full[0], 0, abort, status);
     int mp = mp_first, nt = nt_first, rows_mp = -1;
-    // gathered row indices of the pair's two row blocks (lane g: rows 4g..4g+3), loaded once
-    // per pair: rows past R and the U rows of bonus rows point at row 0 and are ignored
-    int trA[4] = {}, urA[4] = {}, trB[4] = {}, urB[4] = {};
+    // gathered row indices of the pair's two row blocks, loaded once per pair into a table
+    // (rows past R and the U rows of bonus rows point at row 0 and are ignored)
     for (long long u = u_begin; u < u_end && ok; ++u) {
       const int n0 = nt * BN;
       const int nb = 2 * mp + 1 < n_mt ? 2 : 1;
       if constexpr (GATHER) {
         if (mp != rows_mp) {
           rows_mp = mp;
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int ra = (2 * mp) * kBM + 4 * lane + e, rb = ra + kBM;
-            trA[e] = urA[e] = trB[e] = urB[e] = 0;
-            if (ra < j.R) {
-              const int n = j.final_n[ra];
-              trA[e] = ra * (j.gamma + 1) + n;
-              if (j.final_kind[ra]) urA[e] = ra * j.gamma + n;
+          for (int q = lane; q < 2 * kBM; q += 32) {
+            const int r = 2 * mp * kBM + q;  // q / kBM is the block of the pair
+            int tr = 0, ur = 0;
+            if (r < j.R && q / kBM < nb) {
+              const int n = j.final_n[r];
+              tr = r * (j.gamma + 1) + n;
+              if (j.final_kind[r]) ur = r * j.gamma + n;
             }
-            if (nb == 2 && rb < j.R) {
-              const int n = j.final_n[rb];
-              trB[e] = rb * (j.gamma + 1) + n;
-              if (j.final_kind[rb]) urB[e] = rb * j.gamma + n;
-            }
+            row_t[q] = tr;
+            row_u[q] = ur;
           }
+          __syncwarp();
         }
       }
       for (int sb = 0; sb < nb && ok; ++sb) {
@@ -567,22 +580,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         } else {
-          // final rows of rejection verification, four rows per tile::gather4 (lane g loads
-          // rows 4g..4g+3 of the row block)
+          // final rows of rejection verification: per instruction, 8 lanes copy one row's 128
+          // bytes (16 each) of T and of U, so a warp moves 4 whole rows; pieces land in the
+          // 128-byte swizzled layout, and columns past V are zero-filled without a read
           static_assert(C::kBoxes == 1, "gathered tiles are one box wide");
-          if (lane == 0) mbar_arrive_expect_tx(&u_full[us], 2u * C::kTileBytes);
-          __syncwarp();
-          if (sb == 0) {
-            tma_gather4(dt + lane * 512, &map_t, n0, trA[0], trA[1], trA[2], trA[3], &u_full[us],
-                        pol_stream);
-            tma_gather4(du + lane * 512, &map_u, n0, urA[0], urA[1], urA[2], urA[3], &u_full[us],
-                        pol_stream);
-          } else {
-            tma_gather4(dt + lane * 512, &map_t, n0, trB[0], trB[1], trB[2], trB[3], &u_full[us],
-                        pol_stream);
-            tma_gather4(du + lane * 512, &map_u, n0, urB[0], urB[1], urB[2], urB[3], &u_full[us],
-                        pol_stream);
+          const unsigned short* Tb = static_cast<const unsigned short*>(j.T);
+          const unsigned short* Ub = static_cast<const unsigned short*>(j.U);
+          const uint32_t st_base = smem_u32(dt), su_base = smem_u32(du);
+          const int c = lane & 7;
+          const uint32_t nb16 = n0 + 8 * c < j.V ? 16u : 0u;
+#pragma unroll 4
+          for (int k = 0; k < kBM / 4; ++k) {
+            const int i = 4 * k + (lane >> 3);  // row within the block
+            const long long tro = (long long)row_t[sb * kBM + i] * j.V + n0 + 8 * c;
+            const long long uro = (long long)row_u[sb * kBM + i] * j.V + n0 + 8 * c;
+            const uint32_t so = i * 128 + ((c ^ (i & 7)) << 4);
+            cp_async16(st_base + so, Tb + (nb16 ? tro : 0), nb16);
+            cp_async16(su_base + so, Ub + (nb16 ? uro : 0), nb16);
           }
+          cp_async_arrive(&u_full[us]);
         }
         if (++us == KU) { us = 0; uph ^= 1; }
       }
@@ -882,11 +898,17 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims
 }
 
 template <int MODE>
-size_t smem_bytes() {
+constexpr size_t smem_bytes() {
   using C = Cfg<MODE>;
   return 1024 + C::kBStages * C::kBStageBytes +
-         (MODE != MODE_STATS ? 2 : 1) * C::kUStages * C::kTileBytes + 512;
+         (MODE != MODE_STATS ? 2 : 1) * C::kUStages * C::kTileBytes + 512 +
+         (MODE != MODE_STATS ? 4 * kBM * 4 : 0);  // gathered row table (pair modes)
 }
+
+// the largest dynamic shared memory a CTA may opt into (227 KB)
+static_assert(smem_bytes<MODE_STATS>() <= 232448 && smem_bytes<MODE_TV>() <= 232448 &&
+                  smem_bytes<MODE_RESID>() <= 232448,
+              "shared-memory budget");
 
 template <int MODE, bool ARGMAX, bool GATHER>
 cudaError_t launch_t(const TcParams& p, const CUtensorMap& w2, const CUtensorMap& u,
