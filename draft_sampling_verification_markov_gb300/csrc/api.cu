@@ -41,7 +41,8 @@ void trace_begin(int kclass, cudaStream_t s) {
   __atomic_fetch_add(&g_launches, 1ull, __ATOMIC_RELAXED);
   TraceState& t = g_trace[kclass];
   if (t.count < t.capacity) {
-    cudaEventRecord(t.begin[t.count], s);
+    // external records stay timing events when the launch is captured into a CUDA graph
+    cudaEventRecordWithFlags(t.begin[t.count], s, cudaEventRecordExternal);
     t.open = t.count;
   }
 }
@@ -49,7 +50,7 @@ void trace_begin(int kclass, cudaStream_t s) {
 void trace_end(int kclass, cudaStream_t s) {
   TraceState& t = g_trace[kclass];
   if (t.open >= 0) {
-    cudaEventRecord(t.end[t.open], s);
+    cudaEventRecordWithFlags(t.end[t.open], s, cudaEventRecordExternal);
     t.open = -1;
     ++t.count;
   }

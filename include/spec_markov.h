@@ -277,8 +277,10 @@ unsigned long long spec_launch_count(void);
 /*
  * Attach caller-created CUDA events (cudaEvent_t handles created with timing enabled) to one
  * kernel class: the i-th launch of that class after this call records begin_events[i] before
- * and end_events[i] after itself on the launch stream, for i < capacity. Pass capacity 0 to
- * detach. The events stay owned by the caller. Process-global state; not thread-safe.
+ * and end_events[i] after itself on the launch stream, for i < capacity. The records are
+ * external (cudaEventRecordExternal), so a launch captured into a CUDA graph keeps them as timing
+ * records at each replay. Pass capacity 0 to detach. The events stay owned by the caller.
+ * Process-global state; not thread-safe.
  */
 int spec_trace_events(int kclass, void* const* begin_events, void* const* end_events,
                       int capacity);
