@@ -37,12 +37,21 @@ unsigned long long g_launches = 0;
 
 }  // namespace
 
+// Inside a stream capture a record must be external to stay a timing record of the graph;
+// outside a capture the external flag is not accepted.
+static void record(cudaEvent_t e, cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(e, s, cudaEventRecordExternal);
+  else
+    cudaEventRecord(e, s);
+}
+
 void trace_begin(int kclass, cudaStream_t s) {
   __atomic_fetch_add(&g_launches, 1ull, __ATOMIC_RELAXED);
   TraceState& t = g_trace[kclass];
   if (t.count < t.capacity) {
-    // external records stay timing events when the launch is captured into a CUDA graph
-    cudaEventRecordWithFlags(t.begin[t.count], s, cudaEventRecordExternal);
+    record(t.begin[t.count], s);
     t.open = t.count;
   }
 }
@@ -50,7 +59,7 @@ void trace_begin(int kclass, cudaStream_t s) {
 void trace_end(int kclass, cudaStream_t s) {
   TraceState& t = g_trace[kclass];
   if (t.open >= 0) {
-    cudaEventRecordWithFlags(t.end[t.open], s, cudaEventRecordExternal);
+    record(t.end[t.open], s);
     t.open = -1;
     ++t.count;
   }
@@ -332,6 +341,10 @@ int spec_markov_propose(const void* U, int u_dtype, const void* W1, const void* 
     const bool pf = rank > 0 && k < gamma && aligned16(W2) && w2_bytes % 16 == 0;
     o.l2_prefetch = pf ? W2 : nullptr;
     o.l2_prefetch_bytes = pf ? w2_bytes : 0;
+    // ... and the W1 row of each drawn token, which the next position gathers
+    const int w1_row = rank * (int)esize(wdt);
+    o.w1 = rank > 0 && k < gamma && aligned16(W1) && w1_row % 16 == 0 ? W1 : nullptr;
+    o.w1_row_bytes = w1_row;
     launch_select(j, u_dtype, wdt, seg, nseg, w.pm, w.ps, greedy ? w.pi : nullptr, o, s);
   }
   return finish();
@@ -414,8 +427,11 @@ int spec_verify_rejection(const void* target, const void* U, int l_dtype, const 
     target_stats_pass(target, l_dtype, scale, R, gamma, V, lengths, w.tstats, w, s);
     tstats = w.tstats;
   }
+  const int w1_row = rank * (int)esize(w_dtype);
+  const RowPrefetch pf = {rank > 0 && aligned16(W1) && w1_row % 16 == 0 ? W1 : nullptr, w1_row,
+                          anchors};
   launch_accept(l_dtype, R, gamma, V, scale, target, tstats, draft_tokens, draft_logp, u_accept,
-                lengths, w.final_n, w.final_kind, accept_len, out_tokens, w.status, s);
+                lengths, w.final_n, w.final_kind, accept_len, out_tokens, w.status, pf, s);
 
   RowJob j;
   memset(&j, 0, sizeof j);

@@ -27,6 +27,18 @@ struct SelectOut {
   // latency-bound kernel runs; 16-byte aligned, a multiple of 16 bytes
   const void* l2_prefetch;
   unsigned long long l2_prefetch_bytes;
+  // optional: the Markov embedding; the row of each drawn token (w1_row_bytes, a multiple of
+  // 16) is pulled into L2 for the next position's A-operand gather
+  const void* w1;
+  int w1_row_bytes;
+};
+
+// Optional L2 prefetch of the W1 rows that the residual pass will gather (the previous token
+// of each request's final row); w1 == nullptr disables it.
+struct RowPrefetch {
+  const void* w1;
+  int row_bytes;
+  const int32_t* anchors;
 };
 
 void launch_stream_partials(const RowJob& j, int dtype, int seg, int nseg, bool vec, bool sum,
@@ -49,7 +61,7 @@ void launch_accept(int dtype, int R, int gamma, int V, float scale, const void* 
                    const float* tstats, const int32_t* tokens, const float* dlogp,
                    const float* u_accept, const int32_t* lengths, int32_t* final_n,
                    int32_t* final_kind, int32_t* accept_len, int32_t* out_tokens,
-                   uint32_t* status, cudaStream_t s);
+                   uint32_t* status, RowPrefetch pf, cudaStream_t s);
 void launch_tv_finalize(int R, int gamma, int nseg, const float* ps, float* conf, float* survival,
                         cudaStream_t s);
 cudaError_t launch_schedule(const float* survival, const double* sps, int Bmax, int R, int gamma,

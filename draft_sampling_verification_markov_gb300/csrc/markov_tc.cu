@@ -18,8 +18,8 @@
 //      evict-first policy (read once), 64-column boxes in the 128-byte-swizzled layout; rows
 //      that are not equally spaced (the final rows of rejection verification) come four at a
 //      time with tile::gather4 into the same layout.
-// The logit stream starts only once the first A block is in tensor memory, so that the W1
-// row gather is not queued behind it.
+// The W1 rows of the A gather are prefetched into L2 by the kernel that drew the tokens, so
+// the logit stream starts at once.
 // Warp roles (352 threads, one CTA per SM, persistent over a contiguous range of units):
 //   warp 0  W2 (B operand) TMA producer;  warp 1  TMEM allocator + single-thread MMA issuer;
 //   warp 2  U / T tile producer;  warps 3..10  epilogue: warp w reads TMEM lanes 32*(w%4)..
@@ -534,9 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t pol_stream = policy_evict_first();
     int us = 0;
     uint32_t uph = 0;
-    // start streaming logit rows once the first A block is in tensor memory: the W1 gather is
-    // latency-bound and must not queue behind this stream
-    bool ok = u_begin >= u_end || mbar_wait(&a_full[0], 0, abort, status);
+    bool ok = true;
     int mp = mp_first, nt = nt_first, rows_mp = -1;
     // gathered row indices of the pair's two row blocks, loaded once per pair into a table
     // (rows past R and the U rows of bonus rows point at row 0 and are ignored)

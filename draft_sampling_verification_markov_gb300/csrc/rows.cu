@@ -476,6 +476,11 @@ __device__ __forceinline__ void l2_prefetch_share(const void* base, unsigned lon
   }
 }
 
+// Bulk prefetch of [p, p + bytes) into L2 (16-byte aligned, a multiple of 16 bytes).
+__device__ __forceinline__ void l2_prefetch_bytes(const void* p, unsigned bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // One block (256 threads) per row.
 //   kind 0 (MODE_STATS partials): greedy argmax, or inverse-CDF draw from the softmax;
 //   kind 1 (MODE_RESID partials): inverse-CDF draw from the residual / bonus distribution.
@@ -751,6 +756,8 @@ __global__ void __launch_bounds__(256) select_kernel(RowJob j, int seg, int nseg
     if (!resid) {
       const size_t q = (size_t)row * j.gamma + (j.k - 1);
       o.tokens[q] = x;
+      if (o.w1) l2_prefetch_bytes(static_cast<const char*>(o.w1) + (size_t)x * o.w1_row_bytes,
+                                  o.w1_row_bytes);
       if (o.logp) {
         const int zv0 = sh_zv0;
         const float zx = (zv0 >= 0 && x >= zv0 && x < zv0 + 64) ? zs[x - zv0]
@@ -837,7 +844,7 @@ __global__ void accept_kernel(int R, int gamma, int V, float scale, const void* 
                               const float* tstats, const int32_t* tokens, const float* dlogp,
                               const float* u_accept, const int32_t* lengths, int32_t* final_n,
                               int32_t* final_kind, int32_t* accept_len, int32_t* out_tokens,
-                              uint32_t* status) {
+                              uint32_t* status, RowPrefetch pf) {
   const int lane = threadIdx.x & 31;
   const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (r >= R) return;
@@ -873,6 +880,12 @@ __global__ void accept_kernel(int R, int gamma, int V, float scale, const void* 
     final_n[r] = n;
     final_kind[r] = n < l ? 1 : 0;
     accept_len[r] = n;
+    if (pf.w1) {  // the residual pass gathers W1 of the final row's previous token
+      const int prev = n == 0 ? pf.anchors[r] : tokens[(size_t)r * gamma + n - 1];
+      if (prev >= 0 && prev < V)
+        l2_prefetch_bytes(static_cast<const char*>(pf.w1) + (size_t)prev * pf.row_bytes,
+                          pf.row_bytes);
+    }
   }
   if (out_tokens) {
     int32_t* o = out_tokens + (size_t)r * (gamma + 1);
@@ -1014,17 +1027,17 @@ void launch_accept(int dtype, int R, int gamma, int V, float scale, const void* 
                    const float* tstats, const int32_t* tokens, const float* dlogp,
                    const float* u_accept, const int32_t* lengths, int32_t* final_n,
                    int32_t* final_kind, int32_t* accept_len, int32_t* out_tokens,
-                   uint32_t* status, cudaStream_t s) {
+                   uint32_t* status, RowPrefetch pf, cudaStream_t s) {
   TraceScope ts(SPEC_KCLASS_OTHER, s);
   const int grid = (R + 7) / 8;  // one warp per request, 8 warps per block
   if (dtype == SPEC_BF16)
     accept_kernel<SPEC_BF16><<<grid, 256, 0, s>>>(R, gamma, V, scale, T, tstats, tokens, dlogp,
                                                   u_accept, lengths, final_n, final_kind,
-                                                  accept_len, out_tokens, status);
+                                                  accept_len, out_tokens, status, pf);
   else
     accept_kernel<SPEC_F32><<<grid, 256, 0, s>>>(R, gamma, V, scale, T, tstats, tokens, dlogp,
                                                  u_accept, lengths, final_n, final_kind,
-                                                 accept_len, out_tokens, status);
+                                                 accept_len, out_tokens, status, pf);
 }
 
 void launch_tv_finalize(int R, int gamma, int nseg, const float* ps, float* conf, float* survival,
