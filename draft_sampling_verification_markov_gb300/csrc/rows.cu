@@ -522,13 +522,16 @@ __global__ void __launch_bounds__(256) select_kernel(RowJob j, int seg, int nseg
   float M = -INFINITY;
   int gidx = 0x7fffffff;
   if (!resid) {
+    // only the row maximum and its first index are needed here (Z comes from the weights
+    // below): a max / min-index reduction, no exponentials
     const int* rpi = pi ? pi + (size_t)row * nseg : nullptr;
-    StatsAcc a = stats_empty();
-    for (int cb = c0; cb < c1; cb += kPer) {
+    float lmax = -INFINITY;
+    int lidx = 0x7fffffff;
+    if (in_regs) {
       int li[kPer];
 #pragma unroll
       for (int k = 0; k < kPer; ++k) {
-        const int c = cb + k;
+        const int c = c0 + k;
         lm[k] = -INFINITY;
         ls[k] = 0.0f;
         li[k] = 0x7fffffff;
@@ -539,11 +542,47 @@ __global__ void __launch_bounds__(256) select_kernel(RowJob j, int seg, int nseg
         }
       }
 #pragma unroll
-      for (int k = 0; k < kPer; ++k) a = stats_merge(a, {lm[k], ls[k], li[k]});
+      for (int k = 0; k < kPer; ++k) lmax = fmaxf(lmax, lm[k]);
+      if (rpi) {
+#pragma unroll
+        for (int k = 0; k < kPer; ++k)
+          if (lm[k] == lmax && li[k] < lidx) lidx = li[k];
+      }
+    } else {
+      for (int c = c0; c < c1; ++c) {
+        const float v = rpm[c];
+        const int ix = rpi ? rpi[c] : 0x7fffffff;
+        if (v > lmax || (v == lmax && ix < lidx)) {
+          lmax = v;
+          lidx = ix;
+        }
+      }
     }
-    a = block_merge(a);
-    M = a.m;
-    gidx = a.idx;
+    // warp, then block: larger maximum wins, equal maxima keep the lower index
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float om = __shfl_xor_sync(0xffffffffu, lmax, off);
+      const int oi = __shfl_xor_sync(0xffffffffu, lidx, off);
+      if (om > lmax || (om == lmax && oi < lidx)) {
+        lmax = om;
+        lidx = oi;
+      }
+    }
+    __shared__ float sh_wm[32];
+    __shared__ int sh_wi[32];
+    if (lane == 0) {
+      sh_wm[warp] = lmax;
+      sh_wi[warp] = lidx;
+    }
+    __syncthreads();
+    for (int w = 0; w < nwarps; ++w) {
+      const float om = sh_wm[w];
+      const int oi = sh_wi[w];
+      if (om > M || (om == M && oi < gidx)) {
+        M = om;
+        gidx = oi;
+      }
+    }
   }
   // 2. segment weights (each partial's share of Z, fp32); run sums, an inclusive warp scan of
   // them and the warp totals as double-float pairs; Z and every warp's offset are sums of the
