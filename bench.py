@@ -391,6 +391,8 @@ def main():
                 "peak_source": peak_src,
                 "launch_ms": 1e3 * dur_s,
                 "step_hbm_frac": algorithmic_bytes_per_step() * args.steps / (ms / 1e3) / 1e9 / peak,
+                "step_hbm_frac_of_8tbs_nominal":
+                    algorithmic_bytes_per_step() * args.steps / (ms / 1e3) / 1e9 / 8000.0,
                 "class_ms_per_step": {names[k]: totals[k][0] / args.steps for k in totals}}
 
     # end to end through the C ABI from pinned host buffers (weights stay resident)
@@ -438,6 +440,7 @@ def main():
                 for k, v in wl.tensors().items()}
         v_cpu, dt = cpu_baseline_run(wl_h, n_req)
         cpu = {"value": v_cpu, "unit": UNIT, "cores": min(threads, n_req), "kind": "oracle",
+               "host_cores_available": len(os.sched_getaffinity(0)),
                "sample": f"{n_req} of {R} requests (all {g} positions, full V) of the same "
                          f"seeded bytes, {dt:.1f} s"}
 

@@ -474,6 +474,13 @@ int spec_verify_rejection(const void* target, const void* U, int l_dtype, const 
   o.uni = u_resid;
   o.uni_stride = 1;
   o.uni_offset = 0;
+  // a decoding loop proposes next from the emitted tokens: have L2 fetch W2 and their W1 rows
+  const size_t w2_bytes = (size_t)V * rank * esize(wdt);
+  const bool next_pf = rank > 0 && aligned16(W2) && w2_bytes % 16 == 0;
+  o.l2_prefetch = next_pf ? W2 : nullptr;
+  o.l2_prefetch_bytes = next_pf ? w2_bytes : 0;
+  o.w1 = next_pf && aligned16(W1) && (rank * esize(wdt)) % 16 == 0 ? W1 : nullptr;
+  o.w1_row_bytes = rank * (int)esize(wdt);
   launch_select(j, l_dtype, wdt, seg, nseg, w.pm, w.ps, nullptr, o, s);
   return finish();
 }

@@ -811,6 +811,8 @@ __global__ void __launch_bounds__(256) select_kernel(RowJob j, int seg, int nseg
       const int n = j.final_n[row];
       o.tokens[(size_t)row * (j.gamma + 1) + n] = x;
       if (o.next_anchor) o.next_anchor[row] = x;
+      if (o.w1) l2_prefetch_bytes(static_cast<const char*>(o.w1) + (size_t)x * o.w1_row_bytes,
+                                  o.w1_row_bytes);
     }
   }
 }
