@@ -478,7 +478,9 @@ def main():
                                                  "events around each library launch"}),
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": int(launches), "clocks": clocks,
-                "tokens_per_s": float(n_acc.sum().item() + R) * args.steps * world / (ms / 1e3)}
+                "tokens_per_s": float(n_acc.sum().item() + R) * args.steps * world / (ms / 1e3),
+                "mean_accept_len": float(n_acc.float().mean().item()),
+                "mean_emitted_per_request": float(n_acc.float().mean().item()) + 1.0}
         print(json.dumps(line), flush=True)
     if pg:
         pg.destroy_process_group()

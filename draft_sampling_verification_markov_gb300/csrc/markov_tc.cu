@@ -394,7 +394,8 @@ struct TcParams {
   float* pm;
   float* ps;
   int* pi;
-  int nseg;  // partial segments per row (row-major partial arrays)
+  int nseg;   // partial segments per row (row-major partial arrays)
+  int stall;  // test of the bounded waits: the first W2 tile is never loaded
 };
 
 // Per-row normalisers of the pair modes for one row (loaded once per row block).
@@ -518,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int ka = 0; ka < ka_n; ++ka) tma_prefetch_2d(&map_w2, ka * 64, pf * BN, pol_keep);
       if (u + kPrefetch < u_end && ++pf == n_nt) pf = 0;
       ok = mbar_wait(&b_empty[bs], bph ^ 1, abort, status);
-      if (ok && lane == 0) {
+      if (ok && lane == 0 && !(P.stall && u == u_begin)) {
         mbar_arrive_expect_tx(&b_full[bs], ka_n * C::kBAtomBytes);
         for (int ka = 0; ka < ka_n; ++ka)
           tma_load_2d(sB + bs * C::kBStageBytes + ka * C::kBAtomBytes, &map_w2, ka * 64, n0,
@@ -937,6 +938,8 @@ bool markov_tc_supported(int udt, int wdt, int rank, int V, const void* U, const
   return tc::encode_fn() != nullptr;
 }
 
+int g_stall_next = 0;  // spec_test_stall_next_markov
+
 cudaError_t launch_markov_tc(const RowJob& j, float* pm, float* ps, int* pi, bool argmax,
                              cudaStream_t s) {
   using namespace tc;
@@ -953,6 +956,7 @@ cudaError_t launch_markov_tc(const RowJob& j, float* pm, float* ps, int* pi, boo
   p.t.n_mt = j.map == MAP_ALL_POS ? rb * j.gamma : rb;
   p.t.n_nt = (j.V + BN - 1) / BN;
   p.nseg = (j.V + BN / 2 - 1) / (BN / 2);
+  p.stall = __atomic_exchange_n(&g_stall_next, 0, __ATOMIC_RELAXED);
   // work units: one column tile against a pair of row blocks
   const long long total = (long long)((p.t.n_mt + 1) / 2) * p.t.n_nt;
   if (total == 0) return cudaSuccess;
@@ -996,3 +1000,8 @@ cudaError_t launch_markov_tc(const RowJob& j, float* pm, float* ps, int* pi, boo
 }
 
 }  // namespace spec
+
+extern "C" int spec_test_stall_next_markov(void) {
+  __atomic_store_n(&spec::g_stall_next, 1, __ATOMIC_RELAXED);
+  return SPEC_OK;
+}

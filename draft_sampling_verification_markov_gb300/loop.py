@@ -84,16 +84,19 @@ class SpecLoop:
                                 accept_len=self.accept_len[t], out_tokens=self.out_tokens[t],
                                 next_anchor=self.anchors[t + 1], workspace=ws, stream=stream)
 
-    def run(self, stream=None):
-        """All iterations, enqueued eagerly."""
-        for t in range(self.iters):
+    def run(self, first: int = 0, last: int | None = None, stream=None):
+        """Iterations first..last-1, enqueued eagerly. The loop state is anchors[first] and the
+        iteration index (which selects the uniform slice), so a loop stopped after iteration t
+        resumes exactly with run(t + 1, ...), given the same anchors and uniforms."""
+        last = self.iters if last is None else last
+        for t in range(first, last):
             self.iteration(t, stream)
 
-    def capture(self):
-        """Record all iterations into one CUDA graph (replay with replay())."""
+    def capture(self, first: int = 0, last: int | None = None):
+        """Record iterations first..last-1 into one CUDA graph (replay with replay())."""
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            self.run()
+            self.run(first, last)
         self.graph = g
         return g
 

@@ -259,6 +259,16 @@ int spec_verify_greedy_noalloc(const void* target, int t_dtype, const int32_t* d
                                uint32_t* device_status, void* stream);
 
 /*
+ * Test support for the bounded waits (no counterpart on the pages). The next tensor-core
+ * Markov pass launched by this process never receives its first W2 tile, so its MMA thread's
+ * wait expires (after about 2 s of SM clock): the kernel sets SPEC_DEV_TIMEOUT in the device
+ * status word, abandons its work (its partials, and the outputs built from them, are
+ * invalid), drains its copies, frees its tensor memory and returns; the CUDA context stays
+ * usable. Nothing faults or hangs.
+ */
+int spec_test_stall_next_markov(void);
+
+/*
  * Tracing (no counterpart on the pages; instrumentation of this library).
  * Kernel classes: SPEC_KCLASS_MARKOV (the Markov producer: tensor-core GEMM fused with the
  * softmax / residual / TV epilogue, or its CUDA-core form), SPEC_KCLASS_STREAM (rank-0 streaming

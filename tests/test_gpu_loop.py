@@ -104,3 +104,23 @@ def test_loop_graph_replay_equals_eager(spec):
     torch.cuda.synchronize()
     assert torch.equal(first, graph.out_tokens)
     assert eager.ws.status() == 0 and graph.ws.status() == 0
+
+
+def test_loop_resumes_from_an_iteration(spec):
+    """Stopping after iteration 1 and resuming at iteration 2 (from the stored anchors) gives the
+    same outputs as one uninterrupted run."""
+    wl = W.full_loop("cpu", R=9, gamma=3, V=1040, rank=64, iterations=4, seed=33)
+    whole = _loop(spec, wl)
+    whole.run()
+    split = _loop(spec, wl)
+    split.run(0, 2)
+    torch.cuda.synchronize()
+    resumed = _loop(spec, wl)
+    resumed.anchors[2].copy_(split.anchors[2])          # the saved loop state
+    resumed.run(2, 4)
+    torch.cuda.synchronize()
+    for name in ("draft_tokens", "accept_len", "out_tokens", "lengths"):
+        a, b, c = getattr(whole, name), getattr(split, name), getattr(resumed, name)
+        assert torch.equal(a[:2], b[:2]), name
+        assert torch.equal(a[2:], c[2:]), name
+    assert torch.equal(whole.anchors[4], resumed.anchors[4])

@@ -1,0 +1,50 @@
+"""Failure detection on the GPU without a fault: every wait of the tensor-core Markov kernel is
+bounded. A test hook makes one wait run out (the first W2 tile of the next Markov pass is never
+loaded); the kernel must report SPEC_DEV_TIMEOUT through the device status word, return, and
+leave the CUDA context usable, so that the next call gives correct results."""
+import time
+
+import pytest
+import torch
+
+from draft_sampling_verification_markov_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+SPEC_DEV_TIMEOUT = 0x10
+
+
+@pytest.fixture(scope="module")
+def spec():
+    import __graft_entry__
+    __graft_entry__.build()
+    from draft_sampling_verification_markov_gb300 import spec as s
+    return s
+
+
+def test_expired_wait_reports_timeout_and_context_survives(spec):
+    wl = W.markov_rejection("cuda", R=130, gamma=2, V=4096, rank=128, seed=41)
+    run = lambda ws: spec.spec_markov_propose(wl.U, wl.W1, wl.W2, wl.anchors, None, 0.0,
+                                              workspace=ws)
+    ref_ws = spec.Workspace(device="cuda")
+    ref = [x.clone() for x in run(ref_ws)]
+    torch.cuda.synchronize()
+    assert ref_ws.status() == 0
+
+    ws = spec.Workspace(device="cuda")
+    run(ws)                              # sizes the workspace
+    torch.cuda.synchronize()
+    assert spec.lib().spec_test_stall_next_markov() == 0
+    t0 = time.time()
+    run(ws)                              # position 1's Markov pass waits in vain, then returns
+    torch.cuda.synchronize()             # no CUDA error: the kernels completed
+    waited = time.time() - t0
+    status = ws.status(clear=True)
+    assert status & SPEC_DEV_TIMEOUT, f"status {status:#x}"
+    assert 0.5 < waited < 30.0
+
+    again = run(ws)                      # the context and the workspace are usable
+    torch.cuda.synchronize()
+    assert ws.status() == 0
+    for a, b in zip(again, ref):
+        assert torch.equal(a, b)
