@@ -467,8 +467,9 @@ __device__ __forceinline__ void l2_prefetch_share(const void* base, unsigned lon
   const unsigned long long b1 = b0 + share < bytes ? b0 + share : bytes;
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
-  for (unsigned long long off = b0; off < b1; off += 65536) {
-    const unsigned n = (unsigned)(b1 - off < 65536 ? b1 - off : 65536);
+  // one instruction per block: issuing is the slow part, not the size
+  for (unsigned long long off = b0; off < b1; off += (1ull << 30)) {
+    const unsigned n = (unsigned)(b1 - off < (1ull << 30) ? b1 - off : (1ull << 30));
     asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(
                      reinterpret_cast<const char*>(base) + off),
                  "r"(n), "l"(pol)
