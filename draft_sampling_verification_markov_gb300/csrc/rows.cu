@@ -235,7 +235,7 @@ __device__ __forceinline__ void row_word(const float (&x)[8], int v, float c, fl
     }
     mx = g;
   }
-  if (STATS) {
+  if (STATS && mx > -INFINITY) {  // words with no finite value so far add nothing (and no NaN)
     const unsigned long long nm = pk2(-mx, -mx), c2 = pk2(c, c);
 #pragma unroll
     for (int i = 0; i < 8; i += 2) {

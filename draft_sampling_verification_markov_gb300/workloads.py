@@ -16,6 +16,8 @@ Workloads (names describe what they are; sizes are the defaults):
   confidence_scheduling  R=512, gamma=16, V=129280, rank 256, bf16, T=1, SPS table to B=8704
   full_loop              R=1024, gamma=16, V=129280, rank 256, bf16, Zipf(1.1) prior, T=0.7,
                          20 chained iterations, SPS table to B=17408
+  sparse_targets         markov_rejection's shapes on a vocab-shuffled Zipf(1.1) prior, with
+                         top-k or top-p truncated target rows (-inf outside the nucleus)
 """
 from __future__ import annotations
 
@@ -172,6 +174,56 @@ def zipf_prior(V, s=1.1, device="cpu"):
     return -s * torch.log(torch.arange(V, device=device, dtype=torch.float32) + 1.0)
 
 
+def shuffled_zipf_prior(V, s=1.1, seed=7, device="cpu"):
+    """Zipf(s) prior -s * ln(rank + 1) with the frequency ranks dealt to token ids by a seeded
+    random permutation (so frequent tokens are scattered over the vocabulary)."""
+    rank = torch.randperm(V, generator=_gen(device, seed), device=device).to(torch.float32)
+    return -s * torch.log(rank + 1.0)
+
+
+def truncate_rows(logits, top_k=None, top_p=None):
+    """Target-side truncation of each row's distribution (the row's own softmax at T = 1): keep
+    the top_k largest logits, or the smallest set of largest logits whose probability reaches
+    top_p, and set every other logit to -inf. Computed with torch in fp64 on a sorted copy;
+    ties at the cut keep the lower token ids."""
+    x = logits.double()
+    flat = x.reshape(-1, x.shape[-1])
+    # stable descending order: larger logit first, lower id first among equals
+    order = torch.sort(flat, dim=-1, descending=True, stable=True).indices
+    keep = torch.zeros_like(flat, dtype=torch.bool)
+    if top_k is not None:
+        keep.scatter_(1, order[:, :top_k], True)
+    else:
+        srt = torch.gather(flat, 1, order)
+        p = torch.softmax(srt, dim=-1)
+        before = torch.cumsum(p, dim=-1) - p            # mass of the larger logits
+        keep_sorted = before < top_p                    # includes the one that reaches top_p
+        keep.scatter_(1, order, keep_sorted)
+    out = torch.where(keep, flat, torch.full_like(flat, float("-inf")))
+    return out.reshape(logits.shape).to(logits.dtype).contiguous()
+
+
+def sparse_targets(device="cpu", R=256, gamma=7, V=129280, rank=256, seed=1006,
+                   temperature=1.0, top_k=None, top_p=None, zipf_seed=1106) -> Workload:
+    """Markov sampling + rejection verify on a vocab-shuffled Zipf(1.1) prior (added to U and to
+    the target in fp32 before the bf16 cast) with top-k or top-p truncated target rows (every
+    target row keeps only its nucleus; other target logits are -inf). The draft side is not
+    truncated, so draft tokens outside the nucleus occur and must be rejected."""
+    U, T = _bf16_pair(R, gamma, V, seed, device, prior=shuffled_zipf_prior(V, 1.1, zipf_seed,
+                                                                              device))
+    if top_k is not None or top_p is not None:
+        T = truncate_rows(T, top_k=top_k, top_p=top_p)
+    W1, W2 = _markov_weights(V, rank, 0.02, seed, device, torch.bfloat16)
+    useed = seed + 1000
+    wl = Workload("sparse_targets", R, gamma, V, rank, temperature, U, T, W1, W2,
+                  _anchors(R, V, seed * 10 + 6, device),
+                  u_draft=_uniform((R, gamma), useed * 10 + 1, device),
+                  u_accept=_uniform((R, gamma), useed * 10 + 2, device),
+                  u_resid=_uniform((R,), useed * 10 + 3, device))
+    wl.extra.update(top_k=top_k, top_p=top_p)
+    return wl
+
+
 def full_loop(device="cpu", R=1024, gamma=16, V=129280, rank=256, iterations=20, seed=1005,
               temperature=0.7, Bmax=None) -> Workload:
     """Full draft -> verify loop: bf16 logits with a Zipf(1.1) prior added to U and target,
@@ -203,6 +255,7 @@ BY_NAME = {
     "markov_rejection": markov_rejection,
     "confidence_scheduling": confidence_scheduling,
     "full_loop": full_loop,
+    "sparse_targets": sparse_targets,
 }
 
 

@@ -289,21 +289,28 @@ def _target_for(Tb, M, prefix):
     return rows.to(torch.bfloat16).unsqueeze(0)
 
 
-@pytest.mark.parametrize("gamma", [1, 2, 3])
-def test_rejection_sampling_is_lossless_by_exact_enumeration(orc, gamma):
+@pytest.mark.parametrize("gamma,top_k", [(1, None), (2, None), (3, None), (2, 3), (3, 3)])
+def test_rejection_sampling_is_lossless_by_exact_enumeration(orc, gamma, top_k):
     """Sum exactly over every draft sequence, every accept/reject branch and every final token;
     the emitted block, padded with fresh target draws, must follow the target chain rule
     P(y_1..y_{gamma+1}) = prod_i p_t(y_{i+1} | y_i) (y_0 = anchor). Draft and target are both
     prefix-dependent (a Markov head on the draft side, a transition table on the target side)
-    and share the temperature."""
+    and share the temperature. With top_k, every target row keeps only its 3 largest logits
+    (the others are -inf): draft tokens outside that nucleus must never survive, and the
+    emitted block must still follow the truncated target chain."""
+    from draft_sampling_verification_markov_gb300.workloads import truncate_rows
     U, W1, W2, Tb, M, anchor, T = _enumeration_problem(100 + gamma, gamma)
     V = U.shape[-1]
     # target row i conditioned on the token at window position i
     tp = np.zeros((gamma + 1, V, V))
     for prev in range(V):
         tgt = _target_for(Tb, M, [prev] * (gamma + 1))
+        if top_k is not None:
+            tgt = truncate_rows(tgt, top_k=top_k)
         for i in range(gamma + 1):
             tp[i, prev] = orc.target_probs(tgt, 0, i, T)
+            if top_k is not None:
+                assert np.count_nonzero(tp[i, prev]) == top_k
     # draft position k conditioned on the previous token
     pd = np.zeros((gamma + 1, V, V))
     for k in range(1, gamma + 1):
