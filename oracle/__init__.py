@@ -72,19 +72,20 @@ def _load():
         lib.oracle_residual.argtypes = [c_dp, c_dp, i, c_dp]
         lib.oracle_residual.restype = ctypes.c_double
         lib.oracle_draft_probs.argtypes = [vp, i, vp, vp, i, i, i, i, i, i, i, ctypes.c_int32,
-                                           f, c_dp, c_dp, c_dp]
+                                           f, c_dp, c_dp, c_dp, vp]
         lib.oracle_draft_probs.restype = i
         lib.oracle_target_probs.argtypes = [vp, i, i, i, i, i, i, f, c_dp]
         lib.oracle_target_probs.restype = i
         lib.oracle_markov_propose.argtypes = [vp, i, vp, vp, i, i, vp, vp, f, i, i, i, vp, vp, vp,
-                                              vp]
+                                              vp, vp]
         lib.oracle_markov_propose.restype = i
         lib.oracle_verify_greedy.argtypes = [vp, i, vp, vp, i, i, i, vp, vp, vp]
         lib.oracle_verify_greedy.restype = i
         lib.oracle_verify_rejection.argtypes = [vp, vp, i, vp, vp, i, i, vp, vp, vp, vp, f, vp, i,
-                                                i, i, vp, vp, vp, vp, vp]
+                                                i, i, vp, vp, vp, vp, vp, vp]
         lib.oracle_verify_rejection.restype = i
-        lib.oracle_tv_confidence.argtypes = [vp, vp, i, vp, vp, i, i, vp, vp, f, i, i, i, vp, vp]
+        lib.oracle_tv_confidence.argtypes = [vp, vp, i, vp, vp, i, i, vp, vp, f, i, i, i, vp, vp,
+                                             vp]
         lib.oracle_tv_confidence.restype = i
         lib.oracle_schedule_prefix.argtypes = [vp, vp, i, i, i, vp, vp, vp]
         lib.oracle_schedule_prefix.restype = i
@@ -144,6 +145,18 @@ def _dp(a):
     return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
 
 
+def _mask(a, R, V):
+    """Allowed-token bitmask [R, ceil(V/32)] as uint32 words, or None."""
+    a = _np(a)
+    if a is None:
+        return None
+    a = np.ascontiguousarray(a).view(np.uint32) if a.dtype.itemsize == 4 else a
+    a = np.ascontiguousarray(a, dtype=np.uint32)
+    if a.shape != (R, (V + 31) // 32):
+        raise ValueError(f"mask must be [R, ceil(V/32)] = {(R, (V + 31) // 32)}, got {a.shape}")
+    return a
+
+
 def _check(rc, what):
     if rc != 0:
         raise OracleError(f"{what} returned status {rc}")
@@ -190,8 +203,9 @@ def residual(pt, pd):
     return q, float(z)
 
 
-def draft_probs(U, W1, W2, r, k, prev, temperature, rank=None):
-    """p_d at draft position k (1-based) of request r after token prev."""
+def draft_probs(U, W1, W2, r, k, prev, temperature, rank=None, mask=None):
+    """p_d at draft position k (1-based) of request r after token prev (mask: allowed-token
+    bitmask [R, ceil(V/32)] or None)."""
     U, ud = _logits(U)
     W1, wd = _logits(W1)
     W2, _ = _logits(W2)
@@ -202,7 +216,7 @@ def draft_probs(U, W1, W2, r, k, prev, temperature, rank=None):
     lz = ctypes.c_double()
     rc = _load().oracle_draft_probs(_p(U), ud, _p(W1), _p(W2), wd, rank, R, gamma, V, r, k,
                                     int(prev), float(temperature), _dp(p), ctypes.byref(m),
-                                    ctypes.byref(lz))
+                                    ctypes.byref(lz), _p(_mask(mask, R, V)))
     _check(rc, "oracle_draft_probs")
     return p, m.value, lz.value
 
@@ -218,7 +232,7 @@ def target_probs(target, r, i, temperature):
 
 # ----------------------------------------------------------------------------- the five steps
 
-def markov_propose(U, W1, W2, anchors, u_draft, temperature, rank=None):
+def markov_propose(U, W1, W2, anchors, u_draft, temperature, rank=None, mask=None):
     """Draft proposal. Returns dict(tokens [R,g] i32, logp [R,g], stats [R,g,2], margin [R,g])."""
     U, ud = _logits(U)
     W1, wd = _logits(W1)
@@ -235,7 +249,7 @@ def markov_propose(U, W1, W2, anchors, u_draft, temperature, rank=None):
     margin = np.empty((R, gamma), dtype=np.float64)
     rc = _load().oracle_markov_propose(_p(U), ud, _p(W1), _p(W2), wd, rank, _p(anchors),
                                        _p(u_draft), float(temperature), R, gamma, V, _p(tokens),
-                                       _p(logp), _p(stats), _p(margin))
+                                       _p(logp), _p(stats), _p(margin), _p(_mask(mask, R, V)))
     _check(rc, "oracle_markov_propose")
     return dict(tokens=tokens, logp=logp, stats=stats, margin=margin)
 
@@ -256,7 +270,7 @@ def verify_greedy(target, draft_tokens, lengths=None):
 
 
 def verify_rejection(target, U, W1, W2, anchors, draft_tokens, u_accept, u_resid, temperature,
-                     lengths=None, rank=None):
+                     lengths=None, rank=None, mask=None):
     T, td = _logits(target)
     U, ud = _logits(U)
     if td != ud:
@@ -274,13 +288,14 @@ def verify_rejection(target, U, W1, W2, anchors, draft_tokens, u_accept, u_resid
                                          _p(_i32(anchors)), _p(_i32(draft_tokens)),
                                          _p(_f32(u_accept)), _p(_f32(u_resid)),
                                          float(temperature), _p(_i32(lengths)), R, gamma, V,
-                                         _p(n), _p(out), _p(nxt), _p(am), _p(rm))
+                                         _p(n), _p(out), _p(nxt), _p(am), _p(rm),
+                                         _p(_mask(mask, R, V)))
     _check(rc, "oracle_verify_rejection")
     return dict(accept_len=n, out_tokens=out, next_anchor=nxt, accept_margin=am,
                 resid_margin=rm)
 
 
-def tv_confidence(U, target, W1, W2, anchors, draft_tokens, temperature, rank=None):
+def tv_confidence(U, target, W1, W2, anchors, draft_tokens, temperature, rank=None, mask=None):
     U, ud = _logits(U)
     T, td = _logits(target)
     if td != ud:
@@ -293,7 +308,8 @@ def tv_confidence(U, target, W1, W2, anchors, draft_tokens, temperature, rank=No
     surv = np.empty((R, gamma), dtype=np.float64)
     rc = _load().oracle_tv_confidence(_p(U), _p(T), ud, _p(W1), _p(W2), wd, rank,
                                       _p(_i32(anchors)), _p(_i32(draft_tokens)),
-                                      float(temperature), R, gamma, V, _p(conf), _p(surv))
+                                      float(temperature), R, gamma, V, _p(conf), _p(surv),
+                                      _p(_mask(mask, R, V)))
     _check(rc, "oracle_tv_confidence")
     return dict(conf=conf, survival=surv)
 

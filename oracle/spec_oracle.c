@@ -47,6 +47,11 @@
  *       Theta(K) = double(R * 2^32 + S_K) * SPS[R + K]; K ranges over
  *       [0, min(R*gamma, Bmax - R)]; K* is the smallest K reaching the maximum; l_r is the
  *       number of selected candidates of request r.
+ *   R11 Grammar-masked drafting: an optional per-request bitmask of ceil(V/32) words (bit
+ *       v%32 of word v/32 set = token v may be proposed) restricts the draft distribution of
+ *       every position to the allowed tokens (their logits are -inf otherwise); argmax,
+ *       sampling, log p_d and (m, log Z), the residual and the TV label all use that
+ *       restricted p_d. The target distribution is never masked.
  *
  * Arithmetic is fp64 except where R1 fixes fp32. Requests are independent in every function
  * but the scheduler; OpenMP spreads requests over host threads and nothing else.
@@ -179,10 +184,13 @@ typedef struct {
   int w_dtype;
   int rank;
   int gamma, V;
+  const uint32_t* mask; /* allowed draft tokens [R, ceil(V/32)] (bit v%32 of word v/32), or NULL */
 } DraftSide;
 
 /* Pre-temperature draft scores s(v) of request r at draft position k (1-based) given the
- * previous token prev (DSpark sections 3-4, readings R1 and the anchor-first layout). */
+ * previous token prev (DSpark sections 3-4, readings R1 and the anchor-first layout). A
+ * disallowed token of a masked request scores -inf (grammar-masked drafting, "Module
+ * deepseek_v4_mtp", Forward: the draft argmax is grammar-masked; reading R11). */
 static void draft_scores(const DraftSide* d, int r, int k, int32_t prev, double* s) {
   const size_t row = ((size_t)r * d->gamma + (size_t)(k - 1)) * (size_t)d->V;
   const int rk = d->rank;
@@ -205,17 +213,23 @@ static void draft_scores(const DraftSide* d, int r, int k, int32_t prev, double*
       s[v] = (double)u + b;
     }
   }
+  if (d->mask) {
+    const uint32_t* mrow = d->mask + (size_t)r * (size_t)((d->V + 31) / 32);
+    for (int v = 0; v < d->V; ++v)
+      if (!((mrow[v / 32] >> (v % 32)) & 1u)) s[v] = -INFINITY;
+  }
 }
 
 /* p_d at draft position k of request r after previous token prev, at inverse temperature
  * invT. Exposed for the exact-enumeration pin. */
 int oracle_draft_probs(const void* U, int u_dtype, const void* W1, const void* W2, int w_dtype,
                        int rank, int R, int gamma, int V, int r, int k, int32_t prev,
-                       float temperature, double* p_out, double* m_out, double* logz_out) {
+                       float temperature, double* p_out, double* m_out, double* logz_out,
+                       const uint32_t* mask) {
   if (!U || !p_out || r < 0 || r >= R || k < 1 || k > gamma || V < 1 || rank < 0)
     return ORACLE_ERR_INVALID_ARG;
   if (rank > 0 && (!W1 || !W2 || prev < 0 || prev >= V)) return ORACLE_ERR_INVALID_ARG;
-  DraftSide d = {U, u_dtype, W1, W2, w_dtype, rank, gamma, V};
+  DraftSide d = {U, u_dtype, W1, W2, w_dtype, rank, gamma, V, mask};
   double* s = (double*)malloc(sizeof(double) * (size_t)V);
   if (!s) return ORACLE_ERR_NO_MEMORY;
   draft_scores(&d, r, k, prev, s);
@@ -261,7 +275,8 @@ int oracle_target_probs(const void* target, int t_dtype, int R, int rows_per_req
 int oracle_markov_propose(const void* U, int u_dtype, const void* W1, const void* W2,
                           int w_dtype, int rank, const int32_t* anchors, const float* u_draft,
                           float temperature, int R, int gamma, int V, int32_t* draft_tokens,
-                          double* draft_logp, double* draft_stats, double* margin) {
+                          double* draft_logp, double* draft_stats, double* margin,
+                          const uint32_t* mask) {
   if (R < 0 || gamma < 0 || V < 1 || rank < 0 || !dtype_ok(u_dtype))
     return R < 0 || gamma < 0 || V < 1 || rank < 0 ? ORACLE_ERR_INVALID_ARG
                                                   : ORACLE_ERR_UNSUPPORTED_DTYPE;
@@ -271,7 +286,7 @@ int oracle_markov_propose(const void* U, int u_dtype, const void* W1, const void
     return ORACLE_ERR_INVALID_ARG;
   const int greedy = (u_draft == NULL) || (temperature == 0.0f);
   const double invT = greedy ? 1.0 : (double)(1.0f / temperature);
-  DraftSide d = {U, u_dtype, W1, W2, w_dtype, rank, gamma, V};
+  DraftSide d = {U, u_dtype, W1, W2, w_dtype, rank, gamma, V, mask};
   int status = ORACLE_OK;
 
 #pragma omp parallel for schedule(dynamic, 1)
@@ -384,7 +399,8 @@ int oracle_verify_rejection(const void* target, const void* U, int l_dtype, cons
                             const int32_t* draft_tokens, const float* u_accept,
                             const float* u_resid, float temperature, const int32_t* lengths,
                             int R, int gamma, int V, int32_t* accept_len, int32_t* out_tokens,
-                            int32_t* next_anchor, double* accept_margin, double* resid_margin) {
+                            int32_t* next_anchor, double* accept_margin, double* resid_margin,
+                            const uint32_t* mask) {
   if (R < 0 || gamma < 0 || V < 1 || rank < 0) return ORACLE_ERR_INVALID_ARG;
   if (!dtype_ok(l_dtype)) return ORACLE_ERR_UNSUPPORTED_DTYPE;
   if (R == 0) return ORACLE_OK;
@@ -393,7 +409,7 @@ int oracle_verify_rejection(const void* target, const void* U, int l_dtype, cons
   if (gamma > 0 && (!draft_tokens || !u_accept)) return ORACLE_ERR_INVALID_ARG;
   if (rank > 0 && (!W1 || !W2 || !anchors || !dtype_ok(w_dtype))) return ORACLE_ERR_INVALID_ARG;
   const double invT = (double)(1.0f / temperature);
-  DraftSide d = {U, l_dtype, W1, W2, w_dtype, rank, gamma, V};
+  DraftSide d = {U, l_dtype, W1, W2, w_dtype, rank, gamma, V, mask};
   int status = ORACLE_OK;
 
 #pragma omp parallel for schedule(dynamic, 1)
@@ -467,7 +483,7 @@ int oracle_verify_rejection(const void* target, const void* U, int l_dtype, cons
 int oracle_tv_confidence(const void* U, const void* target, int l_dtype, const void* W1,
                          const void* W2, int w_dtype, int rank, const int32_t* anchors,
                          const int32_t* draft_tokens, float temperature, int R, int gamma,
-                         int V, double* conf, double* survival) {
+                         int V, double* conf, double* survival, const uint32_t* mask) {
   if (R < 0 || gamma < 0 || V < 1 || rank < 0) return ORACLE_ERR_INVALID_ARG;
   if (!dtype_ok(l_dtype)) return ORACLE_ERR_UNSUPPORTED_DTYPE;
   if (R == 0 || gamma == 0) return ORACLE_OK;
@@ -475,7 +491,7 @@ int oracle_tv_confidence(const void* U, const void* target, int l_dtype, const v
     return ORACLE_ERR_INVALID_ARG;
   if (rank > 0 && (!W1 || !W2 || !anchors || !dtype_ok(w_dtype))) return ORACLE_ERR_INVALID_ARG;
   const double invT = (double)(1.0f / temperature);
-  DraftSide d = {U, l_dtype, W1, W2, w_dtype, rank, gamma, V};
+  DraftSide d = {U, l_dtype, W1, W2, w_dtype, rank, gamma, V, mask};
   int status = ORACLE_OK;
 #pragma omp parallel for schedule(dynamic, 1)
   for (int r = 0; r < R; ++r) {

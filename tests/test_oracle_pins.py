@@ -503,3 +503,122 @@ def test_scheduler_special_cases(orc):
     sps = np.array([0, 1.0, 1.0, 1.0, 0.0])
     out = orc.schedule_prefix(eq2, sps)
     assert list(out["lengths"]) == [2]
+
+
+# ----------------------------------------------------------------------------- grammar masks
+
+def _bits(allowed_rows, V):
+    """bool [R, V] -> uint32 words [R, ceil(V/32)], bit v%32 of word v/32."""
+    R = len(allowed_rows)
+    words = np.zeros((R, (V + 31) // 32), dtype=np.uint32)
+    for r, row in enumerate(allowed_rows):
+        for v in np.nonzero(row)[0]:
+            words[r, v // 32] |= np.uint32(1 << (v % 32))
+    return words
+
+
+def test_masked_draft_is_the_renormalised_restriction(orc):
+    g = torch.Generator().manual_seed(21)
+    R, gamma, V, rank = 2, 2, 70, 8
+    U = torch.randn(R, gamma, V, generator=g).mul(2).to(torch.bfloat16)
+    W1 = torch.randn(V, rank, generator=g).mul(0.3).to(torch.bfloat16)
+    W2 = torch.randn(V, rank, generator=g).mul(0.3).to(torch.bfloat16)
+    allowed = np.random.default_rng(3).random((R, V)) < 0.4
+    mask = _bits(allowed, V)
+    for r in range(R):
+        for k in (1, 2):
+            p, _, _ = orc.draft_probs(U, W1, W2, r, k, 5, 0.8)
+            pm, _, _ = orc.draft_probs(U, W1, W2, r, k, 5, 0.8, mask=mask)
+            want = np.where(allowed[r], p, 0.0)
+            np.testing.assert_allclose(pm, want / want.sum(), rtol=1e-12, atol=1e-300)
+    ones = _bits(np.ones((R, V), bool), V)
+    p1, _, _ = orc.draft_probs(U, W1, W2, 1, 2, 7, 0.8, mask=ones)
+    p0, _, _ = orc.draft_probs(U, W1, W2, 1, 2, 7, 0.8)
+    assert np.array_equal(p1, p0)
+
+
+def test_masked_greedy_is_argmax_over_allowed_tokens(orc):
+    """Small-integer fp32 values: the scores are the exact integer matrix product, so the
+    masked argmax is checked by brute force (ties to the lowest allowed id)."""
+    rng = np.random.default_rng(8)
+    R, gamma, V, rank = 3, 4, 40, 6
+    U = rng.integers(-6, 6, (R, gamma, V)).astype(np.float32)
+    W1 = rng.integers(-2, 3, (V, rank)).astype(np.float32)
+    W2 = rng.integers(-2, 3, (V, rank)).astype(np.float32)
+    anchors = rng.integers(0, V, R).astype(np.int32)
+    allowed = rng.random((R, V)) < 0.3
+    allowed[:, 0] = True
+    ref = orc.markov_propose(U, W1, W2, anchors, None, 0.0, mask=_bits(allowed, V))
+    for r in range(R):
+        prev = anchors[r]
+        for k in range(gamma):
+            s = U[r, k] + W1[prev] @ W2.T
+            s = np.where(allowed[r], s, -np.inf)
+            x = int(np.argmax(s))                     # numpy: first maximum
+            assert ref["tokens"][r, k] == x
+            prev = x
+
+
+def test_masked_sampling_stays_in_the_allowed_set(orc):
+    g = torch.Generator().manual_seed(5)
+    R, gamma, V, rank = 64, 3, 50, 8
+    U = torch.randn(R, gamma, V, generator=g).mul(2).to(torch.bfloat16)
+    W1 = torch.randn(V, rank, generator=g).mul(0.3).to(torch.bfloat16)
+    W2 = torch.randn(V, rank, generator=g).mul(0.3).to(torch.bfloat16)
+    anchors = torch.randint(0, V, (R,), generator=g, dtype=torch.int32)
+    u = torch.rand(R, gamma, generator=g)
+    allowed = np.random.default_rng(9).random((R, V)) < 0.2
+    allowed[:, 3] = True
+    ref = orc.markov_propose(U, W1, W2, anchors, u, 0.9, mask=_bits(allowed, V))
+    assert all(allowed[r, ref["tokens"][r, k]] for r in range(R) for k in range(gamma))
+
+
+def test_masked_draft_rejection_is_lossless_by_exact_enumeration(orc):
+    """The enumeration of the lossless pin with a draft restricted to 5 of 8 tokens: tokens the
+    draft cannot propose still reach the output through the residual, and the emitted block
+    follows the (unmasked) target chain."""
+    gamma = 2
+    U, W1, W2, Tb, M, anchor, T = _enumeration_problem(202, gamma)
+    V = U.shape[-1]
+    allowed = np.array([[1, 0, 1, 1, 0, 1, 0, 1]], bool)
+    mask = _bits(allowed, V)
+    tp = np.zeros((gamma + 1, V, V))
+    for prev in range(V):
+        tgt = _target_for(Tb, M, [prev] * (gamma + 1))
+        for i in range(gamma + 1):
+            tp[i, prev] = orc.target_probs(tgt, 0, i, T)
+    pd = np.zeros((gamma + 1, V, V))
+    for k in range(1, gamma + 1):
+        for prev in range(V):
+            pd[k, prev] = orc.draft_probs(U, W1, W2, 0, k, prev, T, mask=mask)[0]
+            assert np.all(pd[k, prev][~allowed[0]] == 0)
+
+    def pad_after(L, y):
+        if L == gamma + 1:
+            return np.array(1.0)
+        return np.stack([tp[L, y, v] * pad_after(L + 1, v) for v in range(V)])
+
+    P = np.zeros((V,) * (gamma + 1))
+    for x in itertools.product(range(V), repeat=gamma):
+        prefix = (anchor,) + x
+        reach = 1.0
+        for k in range(1, gamma + 1):
+            reach *= pd[k, prefix[k - 1], x[k - 1]]
+        if reach == 0:
+            continue
+        for n in range(gamma + 1):
+            if n < gamma:
+                p_t, p_d = tp[n, prefix[n]], pd[n + 1, prefix[n]]
+                alpha = orc.accept_prob(p_d[x[n]], p_t[x[n]])
+                q, _ = orc.residual(p_t, p_d)
+                w = reach * (1.0 - alpha)
+                reach *= alpha
+            else:
+                q, w = tp[gamma, prefix[gamma]], reach
+            if w <= 0:
+                continue
+            for y in range(V):
+                if q[y] > 0:
+                    P[x[:n] + (y,)] += w * q[y] * pad_after(n + 1, y)
+    want = pad_after(0, anchor)
+    assert np.max(np.abs(P - want)) <= 1e-12
