@@ -277,11 +277,11 @@ int spec_device_status(void* ws, size_t ws_bytes, void* stream, uint32_t* status
   return SPEC_OK;
 }
 
-int spec_markov_propose(const void* U, int u_dtype, const void* W1, const void* W2, int w_dtype,
-                        int rank, const int32_t* anchors, const float* u_draft,
-                        float temperature, int R, int gamma, int V, int32_t* draft_tokens,
-                        float* draft_logp, float* draft_stats, void* ws, size_t ws_bytes,
-                        void* stream) {
+static int markov_propose_impl(const void* U, int u_dtype, const void* W1, const void* W2,
+                               int w_dtype, int rank, const int32_t* anchors, const float* u_draft,
+                               float temperature, int R, int gamma, int V, int32_t* draft_tokens,
+                               float* draft_logp, float* draft_stats, void* ws, size_t ws_bytes,
+                               void* stream, const uint32_t* mask) {
   if (!sizes_ok(R, gamma, V) || rank < 0 || rank > 1024) return SPEC_ERR_INVALID_ARG;
   if (!dtype_ok(u_dtype) || (rank > 0 && !dtype_ok(w_dtype))) return SPEC_ERR_UNSUPPORTED_DTYPE;
   if (!(temperature >= 0.0f) || !isfinite(temperature)) return SPEC_ERR_INVALID_ARG;
@@ -311,6 +311,8 @@ int spec_markov_propose(const void* U, int u_dtype, const void* W1, const void* 
   j.anchors = anchors;
   j.tokens = draft_tokens;
   j.status = w.status;
+  j.mask = mask;
+  j.mask_words = (V + 31) / 32;
 
   SelectOut o;
   memset(&o, 0, sizeof o);
@@ -399,14 +401,14 @@ int spec_target_stats(const void* target, int t_dtype, float temperature, int ro
   return finish();
 }
 
-int spec_verify_rejection(const void* target, const void* U, int l_dtype, const void* W1,
-                          const void* W2, int w_dtype, int rank, const int32_t* anchors,
-                          const int32_t* draft_tokens, const float* draft_logp,
-                          const float* draft_stats, const float* target_stats,
-                          const float* u_accept, const float* u_resid, float temperature,
-                          const int32_t* lengths, int R, int gamma, int V, int32_t* accept_len,
-                          int32_t* out_tokens, int32_t* next_anchor, void* ws, size_t ws_bytes,
-                          void* stream) {
+static int verify_rejection_impl(const void* target, const void* U, int l_dtype, const void* W1,
+                                 const void* W2, int w_dtype, int rank, const int32_t* anchors,
+                                 const int32_t* draft_tokens, const float* draft_logp,
+                                 const float* draft_stats, const float* target_stats,
+                                 const float* u_accept, const float* u_resid, float temperature,
+                                 const int32_t* lengths, int R, int gamma, int V,
+                                 int32_t* accept_len, int32_t* out_tokens, int32_t* next_anchor,
+                                 void* ws, size_t ws_bytes, void* stream, const uint32_t* mask) {
   if (!sizes_ok(R, gamma, V) || rank < 0 || rank > 1024) return SPEC_ERR_INVALID_ARG;
   if (!dtype_ok(l_dtype) || (rank > 0 && !dtype_ok(w_dtype))) return SPEC_ERR_UNSUPPORTED_DTYPE;
   if (!(temperature > 0.0f) || !isfinite(temperature)) return SPEC_ERR_INVALID_ARG;
@@ -455,6 +457,8 @@ int spec_verify_rejection(const void* target, const void* U, int l_dtype, const 
   j.final_n = w.final_n;
   j.final_kind = w.final_kind;
   j.status = w.status;
+  j.mask = mask;
+  j.mask_words = (V + 31) / 32;
   const int wdt = rank > 0 ? w_dtype : l_dtype;
   int seg, nseg;
   if (rank == 0) {
@@ -485,11 +489,12 @@ int spec_verify_rejection(const void* target, const void* U, int l_dtype, const 
   return finish();
 }
 
-int spec_tv_confidence(const void* U, const void* target, int l_dtype, const void* W1,
-                       const void* W2, int w_dtype, int rank, const int32_t* anchors,
-                       const int32_t* draft_tokens, const float* draft_stats,
-                       const float* target_stats, float temperature, int R, int gamma, int V,
-                       float* conf, float* survival, void* ws, size_t ws_bytes, void* stream) {
+static int tv_confidence_impl(const void* U, const void* target, int l_dtype, const void* W1,
+                              const void* W2, int w_dtype, int rank, const int32_t* anchors,
+                              const int32_t* draft_tokens, const float* draft_stats,
+                              const float* target_stats, float temperature, int R, int gamma, int V,
+                              float* conf, float* survival, void* ws, size_t ws_bytes, void* stream,
+                              const uint32_t* mask) {
   if (!sizes_ok(R, gamma, V) || rank < 0 || rank > 1024) return SPEC_ERR_INVALID_ARG;
   if (!dtype_ok(l_dtype) || (rank > 0 && !dtype_ok(w_dtype))) return SPEC_ERR_UNSUPPORTED_DTYPE;
   if (!(temperature > 0.0f) || !isfinite(temperature)) return SPEC_ERR_INVALID_ARG;
@@ -527,6 +532,8 @@ int spec_tv_confidence(const void* U, const void* target, int l_dtype, const voi
   j.T = target;
   j.tstats = tstats;
   j.status = w.status;
+  j.mask = mask;
+  j.mask_words = (V + 31) / 32;
   const bool vec = vec_ok(U, target, l_dtype, V);
   const float* dstats = draft_stats;
   if (!dstats) {
@@ -574,6 +581,79 @@ int spec_schedule_prefix(const float* survival, const double* sps, int Bmax, int
                                         static_cast<uint32_t*>(ws),
                                         static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+// The plain entry points are the no-mask case of the grammar-masked ones.
+
+int spec_markov_propose(const void* U, int u_dtype, const void* W1, const void* W2, int w_dtype,
+                        int rank, const int32_t* anchors, const float* u_draft,
+                        float temperature, int R, int gamma, int V, int32_t* draft_tokens,
+                        float* draft_logp, float* draft_stats, void* ws, size_t ws_bytes,
+                        void* stream) {
+  return markov_propose_impl(U, u_dtype, W1, W2, w_dtype, rank, anchors, u_draft, temperature, R,
+                             gamma, V, draft_tokens, draft_logp, draft_stats, ws, ws_bytes,
+                             stream, nullptr);
+}
+
+int spec_markov_propose_masked(const void* U, int u_dtype, const void* W1, const void* W2,
+                               int w_dtype, int rank, const int32_t* anchors,
+                               const float* u_draft, float temperature, int R, int gamma, int V,
+                               int32_t* draft_tokens, float* draft_logp, float* draft_stats,
+                               const uint32_t* allowed, void* ws, size_t ws_bytes,
+                               void* stream) {
+  return markov_propose_impl(U, u_dtype, W1, W2, w_dtype, rank, anchors, u_draft, temperature, R,
+                             gamma, V, draft_tokens, draft_logp, draft_stats, ws, ws_bytes,
+                             stream, allowed);
+}
+
+int spec_verify_rejection(const void* target, const void* U, int l_dtype, const void* W1,
+                          const void* W2, int w_dtype, int rank, const int32_t* anchors,
+                          const int32_t* draft_tokens, const float* draft_logp,
+                          const float* draft_stats, const float* target_stats,
+                          const float* u_accept, const float* u_resid, float temperature,
+                          const int32_t* lengths, int R, int gamma, int V, int32_t* accept_len,
+                          int32_t* out_tokens, int32_t* next_anchor, void* ws, size_t ws_bytes,
+                          void* stream) {
+  return verify_rejection_impl(target, U, l_dtype, W1, W2, w_dtype, rank, anchors, draft_tokens,
+                               draft_logp, draft_stats, target_stats, u_accept, u_resid,
+                               temperature, lengths, R, gamma, V, accept_len, out_tokens,
+                               next_anchor, ws, ws_bytes, stream, nullptr);
+}
+
+int spec_verify_rejection_masked(const void* target, const void* U, int l_dtype, const void* W1,
+                                 const void* W2, int w_dtype, int rank, const int32_t* anchors,
+                                 const int32_t* draft_tokens, const float* draft_logp,
+                                 const float* draft_stats, const float* target_stats,
+                                 const float* u_accept, const float* u_resid, float temperature,
+                                 const int32_t* lengths, int R, int gamma, int V,
+                                 int32_t* accept_len, int32_t* out_tokens, int32_t* next_anchor,
+                                 const uint32_t* allowed, void* ws, size_t ws_bytes,
+                                 void* stream) {
+  return verify_rejection_impl(target, U, l_dtype, W1, W2, w_dtype, rank, anchors, draft_tokens,
+                               draft_logp, draft_stats, target_stats, u_accept, u_resid,
+                               temperature, lengths, R, gamma, V, accept_len, out_tokens,
+                               next_anchor, ws, ws_bytes, stream, allowed);
+}
+
+int spec_tv_confidence(const void* U, const void* target, int l_dtype, const void* W1,
+                       const void* W2, int w_dtype, int rank, const int32_t* anchors,
+                       const int32_t* draft_tokens, const float* draft_stats,
+                       const float* target_stats, float temperature, int R, int gamma, int V,
+                       float* conf, float* survival, void* ws, size_t ws_bytes, void* stream) {
+  return tv_confidence_impl(U, target, l_dtype, W1, W2, w_dtype, rank, anchors, draft_tokens,
+                            draft_stats, target_stats, temperature, R, gamma, V, conf, survival,
+                            ws, ws_bytes, stream, nullptr);
+}
+
+int spec_tv_confidence_masked(const void* U, const void* target, int l_dtype, const void* W1,
+                              const void* W2, int w_dtype, int rank, const int32_t* anchors,
+                              const int32_t* draft_tokens, const float* draft_stats,
+                              const float* target_stats, float temperature, int R, int gamma,
+                              int V, float* conf, float* survival, const uint32_t* allowed,
+                              void* ws, size_t ws_bytes, void* stream) {
+  return tv_confidence_impl(U, target, l_dtype, W1, W2, w_dtype, rank, anchors, draft_tokens,
+                            draft_stats, target_stats, temperature, R, gamma, V, conf, survival,
+                            ws, ws_bytes, stream, allowed);
 }
 
 }  // extern "C"

@@ -265,7 +265,16 @@ struct RowJob {
   const int32_t* final_n;  // [R] n_r (MAP_FINAL)
   const int32_t* final_kind;  // [R] 1 = residual, 0 = bonus (MAP_FINAL)
   uint32_t* status;
+  // grammar-masked drafting: allowed draft tokens [R, mask_words] (bit v%32 of word v/32), or
+  // null for no mask; a disallowed token has draft logit -inf
+  const uint32_t* mask;
+  int mask_words;
 };
+
+// Whether request r may propose token v.
+__device__ __forceinline__ bool draft_allowed(const RowJob& j, int r, int v) {
+  return !j.mask || ((j.mask[(size_t)r * j.mask_words + (v >> 5)] >> (v & 31)) & 1u);
+}
 
 struct RowInfo {
   int active;   // 0: the row is not needed (beyond the verified length)

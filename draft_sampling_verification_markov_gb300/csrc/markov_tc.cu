@@ -732,6 +732,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const TileRow tr = tile_row(j, P.t, 2 * mp + sb, i);
         const bool live = tr.valid && n0 + col0 < j.V;
         const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + as * BN + col0;
+        // allowed-token bits of this thread's columns (grammar-masked drafting), loaded before
+        // the waits so that the load is in flight meanwhile
+        uint32_t mlo = ~0u, mhi = ~0u;
+        if (j.mask && live) {
+          const uint32_t* mr = j.mask + (size_t)tr.r * j.mask_words + ((n0 + col0) >> 5);
+          mlo = mr[0];
+          if (kHalf == 64) mhi = n0 + col0 + 32 < j.V ? mr[1] : 0u;
+        }
         ok = mbar_wait(&acc_full[as], accph[as], abort, status);
         if (!ok) break;
         tc_fence_after();
@@ -785,6 +793,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int e = 0; e < 64; ++e)
               if (n0 + col0 + e >= j.V) z[e] = -INFINITY;
+          }
+          if (j.mask) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              if (!((mlo >> e) & 1u)) z[e] = -INFINITY;
+              if (!((mhi >> e) & 1u)) z[32 + e] = -INFINITY;
+            }
           }
           // maximum (3-input tree) and, for greedy, its first position
           float t22[22];
@@ -840,7 +855,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int e = 0; e < 8; ++e) {
                 const float pt = prob_of(tv[e] * j.scale, tn);
-                const float pd = prob_of((uv[e] + __uint_as_float(braw[c * 8 + e])) * j.scale, dn);
+                float pd = prob_of((uv[e] + __uint_as_float(braw[c * 8 + e])) * j.scale, dn);
+                if (!((mlo >> (c * 8 + e)) & 1u)) pd = 0.0f;  // disallowed draft token
                 float x;
                 if constexpr (MODE == MODE_TV) x = fminf(pt, pd);
                 else x = fmaxf(pt - (resid ? pd : 0.0f), 0.0f);  // bonus rows: p_t

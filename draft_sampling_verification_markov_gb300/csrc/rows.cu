@@ -27,6 +27,7 @@ namespace spec {
 // in the canonical fp32 chain acc = fma(W1[prev][i], W2[v][i], acc), i ascending.
 template <int UDT, int WDT>
 __device__ __forceinline__ float draft_logit(const RowJob& j, const RowInfo& ri, int v) {
+  if (!draft_allowed(j, ri.r, v)) return -INFINITY;
   float acc = 0.0f;
   if (j.rank > 0) {
     const size_t a = (size_t)ri.prev * j.rank, b = (size_t)v * j.rank;
@@ -135,6 +136,7 @@ __global__ void __launch_bounds__(256) stream_partials_kernel(RowJob j, int seg,
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             x[b][i] = __fmul_rn(x[b][i], j.scale);
+            if (draft && j.mask && !draft_allowed(j, ri.r, v + i)) x[b][i] = -INFINITY;
             if (ARGMAX && x[b][i] > acc.m && x[b][i] > g) acc.idx = v + i;  // first maximum
             g = fmaxf(g, x[b][i]);
           }
@@ -176,7 +178,9 @@ __global__ void __launch_bounds__(256) stream_partials_kernel(RowJob j, int seg,
               acc += pt;
               continue;
             }
-            const float pd = prob_of(__fmul_rn(xd[b][i], j.scale), dn);
+            const float pd = draft_allowed(j, ri.r, base + b * step + i)
+                                 ? prob_of(__fmul_rn(xd[b][i], j.scale), dn)
+                                 : 0.0f;
             acc += MODE == MODE_RESID ? fmaxf(pt - pd, 0.0f) : fminf(pt, pd);
           }
         }
@@ -452,7 +456,7 @@ __device__ void segment_logits(const RowJob& j, const RowInfo& ri, int v0, int n
     for (int off = tpc / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (col < n && part == 0) {
       const float s = __fadd_rn(ld_elem<UDT>(j.U, (size_t)ri.urow * j.V + v), acc);
-      zs[col] = __fmul_rn(s, j.scale);
+      zs[col] = draft_allowed(j, ri.r, v) ? __fmul_rn(s, j.scale) : -INFINITY;
     }
   } else {
     if (tid < n) zs[tid] = draft_logit<UDT, WDT>(j, ri, v0 + tid);

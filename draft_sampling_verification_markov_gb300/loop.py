@@ -25,10 +25,12 @@ class SpecLoop:
     U [R, gamma, V] and target [R, gamma + 1, V] (bf16 or fp32), W1 / W2 [V, rank], anchors0
     [R] int32, uniforms u_draft / u_accept [iters, R, gamma] and u_resid [iters, R] fp32,
     sps [Bmax + 1] fp64 (index = batch size B). With schedule=False every request verifies
-    all gamma positions (no confidence pass, no scheduler)."""
+    all gamma positions (no confidence pass, no scheduler). `allowed` (optional, [R, ceil(V/32)]
+    32-bit words) restricts every draft position to the allowed tokens (grammar-masked
+    drafting), in the proposal, the confidence pass and the residual alike."""
 
     def __init__(self, U, target, W1, W2, anchors0, u_draft, u_accept, u_resid, temperature,
-                 sps=None, *, iterations=None, schedule=True):
+                 sps=None, *, iterations=None, schedule=True, allowed=None):
         R, gamma, V = U.shape
         self.R, self.gamma, self.V = R, gamma, V
         self.iters = int(iterations if iterations is not None else u_draft.shape[0])
@@ -36,6 +38,7 @@ class SpecLoop:
         self.u_draft, self.u_accept, self.u_resid = u_draft, u_accept, u_resid
         self.temperature = float(temperature)
         self.sps = sps
+        self.allowed = allowed
         self.schedule = bool(schedule) and sps is not None
         self.rank = 0 if W1 is None else int(W1.shape[1])
         dev = U.device
@@ -66,14 +69,16 @@ class SpecLoop:
         a_t = self.anchors[t]
         S.spec_markov_propose(self.U, self.W1, self.W2, a_t, self.u_draft[t], T,
                               draft_tokens=self.draft_tokens[t], draft_logp=self.draft_logp,
-                              draft_stats=self.draft_stats, workspace=ws, stream=stream)
+                              draft_stats=self.draft_stats, workspace=ws, stream=stream,
+                              allowed=self.allowed)
         S.spec_target_stats(self.target, T, stats=self.target_stats, workspace=ws, stream=stream)
         lengths = None
         if self.schedule:
             S.spec_tv_confidence(self.U, self.target, self.W1, self.W2, a_t,
                                  self.draft_tokens[t], T, draft_stats=self.draft_stats,
                                  target_stats=self.target_stats, conf=self.conf[t],
-                                 survival=self.survival[t], workspace=ws, stream=stream)
+                                 survival=self.survival[t], workspace=ws, stream=stream,
+                                 allowed=self.allowed)
             S.spec_schedule_prefix(self.survival[t], self.sps, lengths=self.lengths[t],
                                    B_out=self.batch[t:t + 1], theta_out=self.theta[t:t + 1],
                                    workspace=ws, stream=stream)
@@ -82,7 +87,8 @@ class SpecLoop:
                                 self.draft_logp, self.draft_stats, self.u_accept[t],
                                 self.u_resid[t], T, lengths, target_stats=self.target_stats,
                                 accept_len=self.accept_len[t], out_tokens=self.out_tokens[t],
-                                next_anchor=self.anchors[t + 1], workspace=ws, stream=stream)
+                                next_anchor=self.anchors[t + 1], workspace=ws, stream=stream,
+                                allowed=self.allowed)
 
     def run(self, first: int = 0, last: int | None = None, stream=None):
         """Iterations first..last-1, enqueued eagerly. The loop state is anchors[first] and the

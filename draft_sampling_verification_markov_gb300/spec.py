@@ -63,6 +63,13 @@ def lib():
                                          vp, vp, sz, vp]
         L.spec_schedule_prefix.argtypes = [vp, vp, i, i, i, vp, vp, vp, vp, sz, vp]
         L.spec_verify_greedy_noalloc.argtypes = [vp, i, vp, vp, i, i, i, vp, vp, vp, vp, vp]
+        L.spec_markov_propose_masked.argtypes = [vp, i, vp, vp, i, i, vp, vp, f, i, i, i, vp, vp,
+                                                 vp, vp, vp, sz, vp]
+        L.spec_verify_rejection_masked.argtypes = [vp, vp, i, vp, vp, i, i, vp, vp, vp, vp, vp,
+                                                   vp, vp, f, vp, i, i, i, vp, vp, vp, vp, vp,
+                                                   sz, vp]
+        L.spec_tv_confidence_masked.argtypes = [vp, vp, i, vp, vp, i, i, vp, vp, vp, vp, f, i, i,
+                                                i, vp, vp, vp, vp, sz, vp]
         L.spec_launch_count.restype = ctypes.c_ulonglong
         L.spec_trace_events.argtypes = [i, vp, vp, i]
         L.spec_trace_events.restype = i
@@ -71,7 +78,8 @@ def lib():
         for name in ("spec_workspace_init", "spec_device_status", "spec_markov_propose",
                      "spec_verify_greedy", "spec_target_stats", "spec_verify_rejection",
                      "spec_tv_confidence", "spec_schedule_prefix",
-                     "spec_verify_greedy_noalloc"):
+                     "spec_verify_greedy_noalloc", "spec_markov_propose_masked",
+                     "spec_verify_rejection_masked", "spec_tv_confidence_masked"):
             getattr(L, name).restype = i
         _lib = L
     return _lib
@@ -100,6 +108,13 @@ def _ptr(t):
 def _stream(stream):
     s = stream if stream is not None else torch.cuda.current_stream()
     return ctypes.c_void_p(s.cuda_stream)
+
+
+def _mask(allowed, R, V):
+    """Allowed-token bitmask [R, ceil(V/32)] of 32-bit words on the device."""
+    if tuple(allowed.shape) != (R, (V + 31) // 32) or allowed.element_size() != 4:
+        raise ValueError(f"allowed must be [R, ceil(V/32)] = {(R, (V + 31) // 32)} 32-bit words")
+    return allowed
 
 
 def _check(fn, rc):
@@ -172,9 +187,10 @@ def _rank_of(W1, rank):
 
 def spec_markov_propose(U, W1, W2, anchors, u_draft, temperature, *, rank=None,
                         draft_tokens=None, draft_logp=None, draft_stats=None, workspace=None,
-                        stream=None, want_stats=True):
-    """Draft proposal (greedy when u_draft is None or temperature == 0).
-    Returns (draft_tokens [R,g] int32, draft_logp [R,g] fp32, draft_stats [R,g,2] fp32)."""
+                        stream=None, want_stats=True, allowed=None):
+    """Draft proposal (greedy when u_draft is None or temperature == 0); `allowed` is an
+    optional allowed-token bitmask [R, ceil(V/32)] (int32 / uint32 words) for grammar-masked
+    drafting. Returns (draft_tokens [R,g] int32, draft_logp [R,g] fp32, draft_stats [R,g,2])."""
     R, gamma, V = U.shape
     rank = _rank_of(W1, rank)
     dev = U.device
@@ -187,10 +203,14 @@ def spec_markov_propose(U, W1, W2, anchors, u_draft, temperature, *, rank=None,
     ws = workspace or default_workspace(dev)
     wp, wn = ws.for_op(SPEC_OP_PROPOSE, R, gamma, V, rank, stream)
     wdt = _dt(W1) if W1 is not None else SPEC_BF16
-    rc = lib().spec_markov_propose(_ptr(U), _dt(U), _ptr(W1), _ptr(W2), wdt, rank, _ptr(anchors),
-                                   _ptr(u_draft), float(temperature), R, gamma, V,
-                                   _ptr(draft_tokens), _ptr(draft_logp), _ptr(draft_stats), wp,
-                                   wn, _stream(stream))
+    args = (_ptr(U), _dt(U), _ptr(W1), _ptr(W2), wdt, rank, _ptr(anchors), _ptr(u_draft),
+            float(temperature), R, gamma, V, _ptr(draft_tokens), _ptr(draft_logp),
+            _ptr(draft_stats))
+    if allowed is None:
+        rc = lib().spec_markov_propose(*args, wp, wn, _stream(stream))
+    else:
+        rc = lib().spec_markov_propose_masked(*args, _ptr(_mask(allowed, R, V)), wp, wn,
+                                              _stream(stream))
     _check("spec_markov_propose", rc)
     return draft_tokens, draft_logp, draft_stats
 
@@ -255,7 +275,7 @@ def spec_target_stats(target, temperature, *, stats=None, workspace=None, stream
 def spec_verify_rejection(target, U, W1, W2, anchors, draft_tokens, draft_logp, draft_stats,
                           u_accept, u_resid, temperature, lengths=None, *, rank=None,
                           target_stats=None, accept_len=None, out_tokens=None, next_anchor=None,
-                          workspace=None, stream=None):
+                          workspace=None, stream=None, allowed=None):
     R, gamma, V = U.shape
     rank = _rank_of(W1, rank)
     dev = U.device
@@ -268,19 +288,22 @@ def spec_verify_rejection(target, U, W1, W2, anchors, draft_tokens, draft_logp, 
     ws = workspace or default_workspace(dev)
     wp, wn = ws.for_op(SPEC_OP_VERIFY_REJECTION, R, gamma, V, rank, stream)
     wdt = _dt(W1) if W1 is not None else SPEC_BF16
-    rc = lib().spec_verify_rejection(_ptr(target), _ptr(U), _dt(U), _ptr(W1), _ptr(W2), wdt, rank,
-                                     _ptr(anchors), _ptr(draft_tokens), _ptr(draft_logp),
-                                     _ptr(draft_stats), _ptr(target_stats), _ptr(u_accept),
-                                     _ptr(u_resid), float(temperature), _ptr(lengths), R, gamma,
-                                     V, _ptr(accept_len), _ptr(out_tokens), _ptr(next_anchor),
-                                     wp, wn, _stream(stream))
+    args = (_ptr(target), _ptr(U), _dt(U), _ptr(W1), _ptr(W2), wdt, rank, _ptr(anchors),
+            _ptr(draft_tokens), _ptr(draft_logp), _ptr(draft_stats), _ptr(target_stats),
+            _ptr(u_accept), _ptr(u_resid), float(temperature), _ptr(lengths), R, gamma, V,
+            _ptr(accept_len), _ptr(out_tokens), _ptr(next_anchor))
+    if allowed is None:
+        rc = lib().spec_verify_rejection(*args, wp, wn, _stream(stream))
+    else:
+        rc = lib().spec_verify_rejection_masked(*args, _ptr(_mask(allowed, R, V)), wp, wn,
+                                                _stream(stream))
     _check("spec_verify_rejection", rc)
     return accept_len, out_tokens, next_anchor
 
 
 def spec_tv_confidence(U, target, W1, W2, anchors, draft_tokens, temperature, *, rank=None,
                        draft_stats=None, target_stats=None, conf=None, survival=None,
-                       workspace=None, stream=None):
+                       workspace=None, stream=None, allowed=None):
     R, gamma, V = U.shape
     rank = _rank_of(W1, rank)
     dev = U.device
@@ -291,10 +314,14 @@ def spec_tv_confidence(U, target, W1, W2, anchors, draft_tokens, temperature, *,
     ws = workspace or default_workspace(dev)
     wp, wn = ws.for_op(SPEC_OP_TV_CONFIDENCE, R, gamma, V, rank, stream)
     wdt = _dt(W1) if W1 is not None else SPEC_BF16
-    rc = lib().spec_tv_confidence(_ptr(U), _ptr(target), _dt(U), _ptr(W1), _ptr(W2), wdt, rank,
-                                  _ptr(anchors), _ptr(draft_tokens), _ptr(draft_stats),
-                                  _ptr(target_stats), float(temperature), R, gamma, V,
-                                  _ptr(conf), _ptr(survival), wp, wn, _stream(stream))
+    args = (_ptr(U), _ptr(target), _dt(U), _ptr(W1), _ptr(W2), wdt, rank, _ptr(anchors),
+            _ptr(draft_tokens), _ptr(draft_stats), _ptr(target_stats), float(temperature), R,
+            gamma, V, _ptr(conf), _ptr(survival))
+    if allowed is None:
+        rc = lib().spec_tv_confidence(*args, wp, wn, _stream(stream))
+    else:
+        rc = lib().spec_tv_confidence_masked(*args, _ptr(_mask(allowed, R, V)), wp, wn,
+                                             _stream(stream))
     _check("spec_tv_confidence", rc)
     return conf, survival
 

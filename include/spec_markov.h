@@ -211,6 +211,40 @@ int spec_tv_confidence(const void* U, const void* target, int l_dtype, const voi
                        float* conf, float* survival, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * Grammar-masked drafting.
+ * Defines: "Module deepseek_v4_mtp", Forward (the draft argmax is grammar-masked when a mask is
+ *   given). Reading: `allowed` is a per-request bitmask [R, ceil(V/32)] uint32 (bit v%32 of
+ *   word v/32 set = token v may be proposed; NULL = every token). The draft distribution of
+ *   every position of request r is the softmax restricted to its allowed tokens (the others
+ *   have logit -inf): argmax, sampling, draft_logp and draft_stats, the rejection residual
+ *   norm(max(0, p_t - p_d)) and the TV label all use that restricted p_d. The target is never
+ *   masked, so rejection verification stays lossless. A request with no allowed token sets
+ *   SPEC_DEV_NONFINITE. Arguments otherwise as the unmasked entry points; a proposal made with
+ *   a mask must be verified and scored with the same mask.
+ */
+int spec_markov_propose_masked(const void* U, int u_dtype, const void* W1, const void* W2,
+                               int w_dtype, int rank, const int32_t* anchors,
+                               const float* u_draft, float temperature, int R, int gamma, int V,
+                               int32_t* draft_tokens, float* draft_logp, float* draft_stats,
+                               const uint32_t* allowed, void* ws, size_t ws_bytes,
+                               void* stream);
+int spec_verify_rejection_masked(const void* target, const void* U, int l_dtype, const void* W1,
+                                 const void* W2, int w_dtype, int rank, const int32_t* anchors,
+                                 const int32_t* draft_tokens, const float* draft_logp,
+                                 const float* draft_stats, const float* target_stats,
+                                 const float* u_accept, const float* u_resid, float temperature,
+                                 const int32_t* lengths, int R, int gamma, int V,
+                                 int32_t* accept_len, int32_t* out_tokens, int32_t* next_anchor,
+                                 const uint32_t* allowed, void* ws, size_t ws_bytes,
+                                 void* stream);
+int spec_tv_confidence_masked(const void* U, const void* target, int l_dtype, const void* W1,
+                              const void* W2, int w_dtype, int rank, const int32_t* anchors,
+                              const int32_t* draft_tokens, const float* draft_stats,
+                              const float* target_stats, float temperature, int R, int gamma,
+                              int V, float* conf, float* survival, const uint32_t* allowed,
+                              void* ws, size_t ws_bytes, void* stream);
+
+/*
  * Hardware-aware prefix scheduler.
  * Defines: "[DeepSeek-6] DSpark", section 6: maximise Theta = tau * SPS(B) with
  *   B = sum_r (1 + l_r) and tau = sum_r (1 + sum_{j<=l_r} a_{r,j}), queueing every candidate
