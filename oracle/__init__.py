@@ -89,6 +89,8 @@ def _load():
         lib.oracle_tv_confidence.restype = i
         lib.oracle_schedule_prefix.argtypes = [vp, vp, i, i, i, vp, vp, vp]
         lib.oracle_schedule_prefix.restype = i
+        lib.oracle_schedule_topk.argtypes = [vp, vp, i, i, i, i, vp, vp, vp]
+        lib.oracle_schedule_topk.restype = i
         del c_i32p
         _lib = lib
     return _lib
@@ -325,4 +327,20 @@ def schedule_prefix(survival, sps):
                                         ctypes.cast(ctypes.byref(B), ctypes.c_void_p),
                                         ctypes.cast(ctypes.byref(theta), ctypes.c_void_p))
     _check(rc, "oracle_schedule_prefix")
+    return dict(lengths=lengths, B=int(B.value), theta=float(theta.value))
+
+
+def schedule_topk(survival, sps, capacity):
+    """Dynamic top-K (DSpark section 7): the batch size `capacity` is given (from an earlier
+    step's confidences); the first K = capacity - R candidates of the current queue are taken."""
+    a = _f32(survival)
+    R, gamma = a.shape
+    sps = np.ascontiguousarray(sps, dtype=np.float64)
+    lengths = np.empty(R, dtype=np.int32)
+    B = ctypes.c_int32()
+    theta = ctypes.c_double()
+    rc = _load().oracle_schedule_topk(_p(a), _p(sps), sps.size - 1, R, gamma, int(capacity),
+                                      _p(lengths), ctypes.cast(ctypes.byref(B), ctypes.c_void_p),
+                                      ctypes.cast(ctypes.byref(theta), ctypes.c_void_p))
+    _check(rc, "oracle_schedule_topk")
     return dict(lengths=lengths, B=int(B.value), theta=float(theta.value))

@@ -545,8 +545,15 @@ static int candidate_cmp(const void* pa, const void* pb) {
  * Exactness per reading R7. survival [R, gamma] must hold finite values in [0, 1];
  * sps[B] for B = 0..Bmax.
  */
-int oracle_schedule_prefix(const float* survival, const double* sps, int Bmax, int R, int gamma,
-                           int32_t* lengths, int32_t* B_out, double* theta_out) {
+/*
+ * Prefix scheduler (DSpark section 6). With capacity < 0 the batch size B = R + K is the
+ * Theta-maximising one (smallest K on ties). With capacity >= 0 it is the dynamic top-K of
+ * DSpark section 7: the capacity B comes from confidences of an earlier step, and the current
+ * candidates are taken in the same queue order up to K = min(capacity - R, R*gamma, Bmax - R)
+ * (clamped at 0); theta_out is Theta at that K.
+ */
+static int schedule_impl(const float* survival, const double* sps, int Bmax, int R, int gamma,
+                         int capacity, int32_t* lengths, int32_t* B_out, double* theta_out) {
   if (R < 0 || gamma < 0 || Bmax < R || !sps) return ORACLE_ERR_INVALID_ARG;
   if (R > 0 && (!lengths || (gamma > 0 && !survival))) return ORACLE_ERR_INVALID_ARG;
   const size_t n = (size_t)R * (size_t)gamma;
@@ -573,12 +580,19 @@ int oracle_schedule_prefix(const float* survival, const double* sps, int Bmax, i
   uint64_t S = 0;
   size_t best_K = 0;
   double best = (double)base * sps[R];
-  for (size_t K = 1; K <= Kmax; ++K) {
-    S += (uint64_t)nearbyint((double)c[K - 1].a * two32);
-    const double theta = (double)(base + S) * sps[R + K];
-    if (theta > best) {
-      best = theta;
-      best_K = K;
+  if (capacity >= 0) { /* fixed capacity: take the first K candidates of the queue */
+    const long long want = (long long)capacity - R;
+    best_K = want <= 0 ? 0 : ((size_t)want < Kmax ? (size_t)want : Kmax);
+    for (size_t K = 1; K <= best_K; ++K) S += (uint64_t)nearbyint((double)c[K - 1].a * two32);
+    best = (double)(base + S) * sps[R + best_K];
+  } else {
+    for (size_t K = 1; K <= Kmax; ++K) {
+      S += (uint64_t)nearbyint((double)c[K - 1].a * two32);
+      const double theta = (double)(base + S) * sps[R + K];
+      if (theta > best) {
+        best = theta;
+        best_K = K;
+      }
     }
   }
   for (int r = 0; r < R; ++r) lengths[r] = 0;
@@ -587,4 +601,15 @@ int oracle_schedule_prefix(const float* survival, const double* sps, int Bmax, i
   if (theta_out) *theta_out = best / two32; /* tau * SPS(B) in natural units */
   free(c);
   return ORACLE_OK;
+}
+
+int oracle_schedule_prefix(const float* survival, const double* sps, int Bmax, int R, int gamma,
+                           int32_t* lengths, int32_t* B_out, double* theta_out) {
+  return schedule_impl(survival, sps, Bmax, R, gamma, -1, lengths, B_out, theta_out);
+}
+
+int oracle_schedule_topk(const float* survival, const double* sps, int Bmax, int R, int gamma,
+                         int capacity, int32_t* lengths, int32_t* B_out, double* theta_out) {
+  if (capacity < 0) return ORACLE_ERR_INVALID_ARG;
+  return schedule_impl(survival, sps, Bmax, R, gamma, capacity, lengths, B_out, theta_out);
 }

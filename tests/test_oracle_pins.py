@@ -622,3 +622,31 @@ def test_masked_draft_rejection_is_lossless_by_exact_enumeration(orc):
                     P[x[:n] + (y,)] += w * q[y] * pad_after(n + 1, y)
     want = pad_after(0, anchor)
     assert np.max(np.abs(P - want)) <= 1e-12
+
+
+# ----------------------------------------------------------------------------- dynamic top-K
+
+@pytest.mark.parametrize("seed", range(4))
+def test_topk_takes_the_k_largest_survivals_prefix_closed(orc, seed):
+    """Dynamic top-K (DSpark section 7): with capacity B the selected candidates are exactly the
+    B - R largest survivals in queue order (a desc, r asc, j asc), prefix-closed per request;
+    with the Theta-optimal B it reproduces the Theta scheduler."""
+    rng = np.random.default_rng(50 + seed)
+    R, gamma = 6, 5
+    a = np.sort(rng.uniform(0.05, 1.0, (R, gamma)), axis=1)[:, ::-1].astype(np.float32)
+    if seed == 3:
+        a[:, :] = a[:, :1]                                  # ties: queue order decides
+    sps = np.random.default_rng(seed).uniform(0.5, 1.0, R * (gamma + 1) + 1)
+    order = sorted(((-float(a[r, j]), r, j) for r in range(R) for j in range(gamma)))
+    for cap in (R - 3, R, R + 1, R + 7, R + R * gamma, R + R * gamma + 9):
+        out = orc.schedule_topk(a, sps, cap)
+        K = max(0, min(cap - R, R * gamma))
+        want = np.zeros(R, dtype=np.int32)
+        for _, r, j in order[:K]:
+            want[r] += 1
+        np.testing.assert_array_equal(out["lengths"], want)
+        assert out["B"] == R + K
+    opt = orc.schedule_prefix(a, sps)
+    same = orc.schedule_topk(a, sps, opt["B"])
+    np.testing.assert_array_equal(same["lengths"], opt["lengths"])
+    assert same["theta"] == opt["theta"]
