@@ -193,9 +193,11 @@ bool vec_ok(const void* a, const void* b, int dtype, int V) {
   return aligned16(a) && (b == nullptr || aligned16(b)) && ((size_t)V * esize(dtype)) % 16 == 0;
 }
 
-// Target row stats (m, log Z) of all R*(gamma+1) rows into `out` (rows beyond `lengths` skipped).
+// Target row stats (m, log Z) of all R*(gamma+1) rows into `out` (rows beyond `lengths`, or
+// past toff[R] in the flattened layout, skipped).
 void target_stats_pass(const void* target, int dtype, float scale, int R, int gamma, int V,
-                       const int32_t* lengths, float* out, const Ws& w, cudaStream_t s) {
+                       const int32_t* lengths, float* out, const Ws& w, cudaStream_t s,
+                       const int32_t* toff = nullptr) {
   RowJob j;
   memset(&j, 0, sizeof j);
   j.rows = R * (gamma + 1);
@@ -207,6 +209,7 @@ void target_stats_pass(const void* target, int dtype, float scale, int R, int ga
   j.scale = scale;
   j.T = target;
   j.lengths = lengths;
+  j.toff = toff;
   j.status = w.status;
   launch_row_stats(j, dtype, vec_ok(target, nullptr, dtype, V), out, nullptr, s);
 }
@@ -352,10 +355,10 @@ static int markov_propose_impl(const void* U, int u_dtype, const void* W1, const
   return finish();
 }
 
-int spec_verify_greedy(const void* target, int t_dtype, const int32_t* draft_tokens,
-                       const int32_t* lengths, int R, int gamma, int V, int32_t* accept_len,
-                       int32_t* out_tokens, int32_t* next_anchor, void* ws, size_t ws_bytes,
-                       void* stream) {
+static int verify_greedy_impl(const void* target, int t_dtype, const int32_t* draft_tokens,
+                              const int32_t* lengths, const int32_t* toff, int R, int gamma,
+                              int V, int32_t* accept_len, int32_t* out_tokens,
+                              int32_t* next_anchor, void* ws, size_t ws_bytes, void* stream) {
   if (!sizes_ok(R, gamma, V)) return SPEC_ERR_INVALID_ARG;
   if (!dtype_ok(t_dtype)) return SPEC_ERR_UNSUPPORTED_DTYPE;
   Layout L;
@@ -376,10 +379,58 @@ int spec_verify_greedy(const void* target, int t_dtype, const int32_t* draft_tok
   j.scale = 1.0f;
   j.T = target;
   j.lengths = lengths;
+  j.toff = toff;
   j.status = w.status;
   launch_row_stats(j, t_dtype, vec_ok(target, nullptr, t_dtype, V), nullptr, w.pi, s);
-  launch_greedy_scan(R, gamma, w.pi, draft_tokens, lengths, accept_len, out_tokens, next_anchor,
-                     w.status, s);
+  launch_greedy_scan(R, gamma, w.pi, draft_tokens, lengths, toff, accept_len, out_tokens,
+                     next_anchor, w.status, s);
+  return finish();
+}
+
+int spec_verify_greedy(const void* target, int t_dtype, const int32_t* draft_tokens,
+                       const int32_t* lengths, int R, int gamma, int V, int32_t* accept_len,
+                       int32_t* out_tokens, int32_t* next_anchor, void* ws, size_t ws_bytes,
+                       void* stream) {
+  return verify_greedy_impl(target, t_dtype, draft_tokens, lengths, nullptr, R, gamma, V,
+                            accept_len, out_tokens, next_anchor, ws, ws_bytes, stream);
+}
+
+int spec_verify_greedy_flat(const void* target, int t_dtype, const int32_t* draft_tokens,
+                            const int32_t* lengths, const int32_t* offsets, int R, int gamma,
+                            int V, int32_t* accept_len, int32_t* out_tokens,
+                            int32_t* next_anchor, void* ws, size_t ws_bytes, void* stream) {
+  if (R > 0 && (!lengths || !offsets)) return SPEC_ERR_INVALID_ARG;
+  return verify_greedy_impl(target, t_dtype, draft_tokens, lengths, offsets, R, gamma, V,
+                            accept_len, out_tokens, next_anchor, ws, ws_bytes, stream);
+}
+
+int spec_flat_layout(const int32_t* lengths, int R, int gamma, int32_t* offsets,
+                     int32_t* row_req, int32_t* row_pos, void* ws, size_t ws_bytes,
+                     void* stream) {
+  if (R < 0 || gamma < 0 || (long long)R * (gamma + 1) > (1LL << 30)) return SPEC_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < kHeader || (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0)
+    return SPEC_ERR_INVALID_ARG;
+  if (!offsets || (R > 0 && !lengths)) return SPEC_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  TraceScope ts(SPEC_KCLASS_OTHER, s);
+  launch_flat_layout(lengths, R, gamma, offsets, row_req, row_pos, static_cast<uint32_t*>(ws), s);
+  return finish();
+}
+
+int spec_target_stats_flat(const void* target, int t_dtype, float temperature, int R, int gamma,
+                           int V, const int32_t* offsets, float* stats, void* ws,
+                           size_t ws_bytes, void* stream) {
+  if (!sizes_ok(R, gamma, V)) return SPEC_ERR_INVALID_ARG;
+  if (!dtype_ok(t_dtype)) return SPEC_ERR_UNSUPPORTED_DTYPE;
+  if (!(temperature > 0.0f) || !isfinite(temperature)) return SPEC_ERR_INVALID_ARG;
+  Layout L;
+  int rc = check_ws(ws, ws_bytes, SPEC_OP_TARGET_STATS, R, gamma, V, 0, &L);
+  if (rc != SPEC_OK) return rc;
+  if (R == 0) return SPEC_OK;
+  if (!target || !stats || !offsets) return SPEC_ERR_INVALID_ARG;
+  const Ws w = carve(ws, L);
+  target_stats_pass(target, t_dtype, 1.0f / temperature, R, gamma, V, nullptr, stats, w,
+                    static_cast<cudaStream_t>(stream), offsets);
   return finish();
 }
 
@@ -408,7 +459,8 @@ static int verify_rejection_impl(const void* target, const void* U, int l_dtype,
                                  const float* u_accept, const float* u_resid, float temperature,
                                  const int32_t* lengths, int R, int gamma, int V,
                                  int32_t* accept_len, int32_t* out_tokens, int32_t* next_anchor,
-                                 void* ws, size_t ws_bytes, void* stream, const uint32_t* mask) {
+                                 void* ws, size_t ws_bytes, void* stream, const uint32_t* mask,
+                                 const int32_t* toff = nullptr) {
   if (!sizes_ok(R, gamma, V) || rank < 0 || rank > 1024) return SPEC_ERR_INVALID_ARG;
   if (!dtype_ok(l_dtype) || (rank > 0 && !dtype_ok(w_dtype))) return SPEC_ERR_UNSUPPORTED_DTYPE;
   if (!(temperature > 0.0f) || !isfinite(temperature)) return SPEC_ERR_INVALID_ARG;
@@ -426,14 +478,14 @@ static int verify_rejection_impl(const void* target, const void* U, int l_dtype,
 
   const float* tstats = target_stats;
   if (!tstats) {
-    target_stats_pass(target, l_dtype, scale, R, gamma, V, lengths, w.tstats, w, s);
+    target_stats_pass(target, l_dtype, scale, R, gamma, V, lengths, w.tstats, w, s, toff);
     tstats = w.tstats;
   }
   const int w1_row = rank * (int)esize(w_dtype);
   const RowPrefetch pf = {rank > 0 && aligned16(W1) && w1_row % 16 == 0 ? W1 : nullptr, w1_row,
                           anchors};
   launch_accept(l_dtype, R, gamma, V, scale, target, tstats, draft_tokens, draft_logp, u_accept,
-                lengths, w.final_n, w.final_kind, accept_len, out_tokens, w.status, pf, s);
+                lengths, toff, w.final_n, w.final_kind, accept_len, out_tokens, w.status, pf, s);
 
   RowJob j;
   memset(&j, 0, sizeof j);
@@ -459,6 +511,7 @@ static int verify_rejection_impl(const void* target, const void* U, int l_dtype,
   j.status = w.status;
   j.mask = mask;
   j.mask_words = (V + 31) / 32;
+  j.toff = toff;
   const int wdt = rank > 0 ? w_dtype : l_dtype;
   int seg, nseg;
   if (rank == 0) {
@@ -566,9 +619,10 @@ static int tv_confidence_impl(const void* U, const void* target, int l_dtype, co
   return finish();
 }
 
-int spec_schedule_prefix(const float* survival, const double* sps, int Bmax, int R, int gamma,
-                         int32_t* lengths, int32_t* B_out, double* theta_out, void* ws,
-                         size_t ws_bytes, void* stream) {
+static int schedule_impl(const float* survival, const double* sps, int Bmax, int R, int gamma,
+                         const int32_t* capacity, int32_t* lengths, int32_t* B_out,
+                         double* theta_out, int32_t* B_opt_out, void* ws, size_t ws_bytes,
+                         void* stream) {
   if (R < 0 || gamma < 0 || Bmax < R) return SPEC_ERR_INVALID_ARG;
   if ((long long)R * gamma > SPEC_SCHEDULE_MAX_CANDIDATES || R > SPEC_SCHEDULE_MAX_CANDIDATES)
     return SPEC_ERR_INVALID_ARG;
@@ -577,10 +631,26 @@ int spec_schedule_prefix(const float* survival, const double* sps, int Bmax, int
   if (!sps || !B_out || !theta_out || (R > 0 && !lengths) || (R * gamma > 0 && !survival))
     return SPEC_ERR_INVALID_ARG;
   TraceScope ts(SPEC_KCLASS_OTHER, static_cast<cudaStream_t>(stream));
-  const cudaError_t e = launch_schedule(survival, sps, Bmax, R, gamma, lengths, B_out, theta_out,
-                                        static_cast<uint32_t*>(ws),
+  const cudaError_t e = launch_schedule(survival, sps, Bmax, R, gamma, capacity, lengths, B_out,
+                                        theta_out, B_opt_out, static_cast<uint32_t*>(ws),
                                         static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+int spec_schedule_prefix(const float* survival, const double* sps, int Bmax, int R, int gamma,
+                         int32_t* lengths, int32_t* B_out, double* theta_out, void* ws,
+                         size_t ws_bytes, void* stream) {
+  return schedule_impl(survival, sps, Bmax, R, gamma, nullptr, lengths, B_out, theta_out,
+                       nullptr, ws, ws_bytes, stream);
+}
+
+int spec_schedule_topk(const float* survival, const double* sps, int Bmax, int R, int gamma,
+                       const int32_t* capacity, int32_t* lengths, int32_t* B_out,
+                       double* theta_out, int32_t* B_opt_out, void* ws, size_t ws_bytes,
+                       void* stream) {
+  if (!capacity) return SPEC_ERR_INVALID_ARG;
+  return schedule_impl(survival, sps, Bmax, R, gamma, capacity, lengths, B_out, theta_out,
+                       B_opt_out, ws, ws_bytes, stream);
 }
 
 // The plain entry points are the no-mask case of the grammar-masked ones.
@@ -633,6 +703,22 @@ int spec_verify_rejection_masked(const void* target, const void* U, int l_dtype,
                                draft_logp, draft_stats, target_stats, u_accept, u_resid,
                                temperature, lengths, R, gamma, V, accept_len, out_tokens,
                                next_anchor, ws, ws_bytes, stream, allowed);
+}
+
+int spec_verify_rejection_flat(const void* target, const void* U, int l_dtype, const void* W1,
+                               const void* W2, int w_dtype, int rank, const int32_t* anchors,
+                               const int32_t* draft_tokens, const float* draft_logp,
+                               const float* draft_stats, const float* target_stats,
+                               const float* u_accept, const float* u_resid, float temperature,
+                               const int32_t* lengths, const int32_t* offsets, int R, int gamma,
+                               int V, int32_t* accept_len, int32_t* out_tokens,
+                               int32_t* next_anchor, const uint32_t* allowed, void* ws,
+                               size_t ws_bytes, void* stream) {
+  if (R > 0 && (!lengths || !offsets)) return SPEC_ERR_INVALID_ARG;
+  return verify_rejection_impl(target, U, l_dtype, W1, W2, w_dtype, rank, anchors, draft_tokens,
+                               draft_logp, draft_stats, target_stats, u_accept, u_resid,
+                               temperature, lengths, R, gamma, V, accept_len, out_tokens,
+                               next_anchor, ws, ws_bytes, stream, allowed, offsets);
 }
 
 int spec_tv_confidence(const void* U, const void* target, int l_dtype, const void* W1,

@@ -269,7 +269,28 @@ struct RowJob {
   // null for no mask; a disallowed token has draft logit -inf
   const uint32_t* mask;
   int mask_words;
+  // flattened verify batch: target rows of request r are toff[r] .. toff[r+1]-1 of a packed
+  // [*, V] array (toff[R] rows in all), or null for the padded [R, gamma+1, V] layout
+  const int32_t* toff;
 };
+
+// Row of target position i (0..gamma) of request r in a target array of R*(gamma+1) rows,
+// padded (toff null) or flattened. A flattened row outside the array (offsets that do not
+// match the lengths) is flagged and read as row 0, so no access leaves the array.
+__device__ __forceinline__ long long target_row(const int32_t* toff, int R, int gamma, int r,
+                                                int i, uint32_t* status) {
+  const long long g1 = (long long)gamma + 1;
+  if (!toff) return (long long)r * g1 + i;
+  const long long t = (long long)toff[r] + i;
+  if (t < 0 || t >= (long long)R * g1) {
+    atomicOr(status, SPEC_DEV_BAD_LENGTH);
+    return 0;
+  }
+  return t;
+}
+__device__ __forceinline__ long long target_row(const RowJob& j, int r, int i) {
+  return target_row(j.toff, j.R, j.gamma, r, i, j.status);
+}
 
 // Whether request r may propose token v.
 __device__ __forceinline__ bool draft_allowed(const RowJob& j, int r, int v) {
@@ -323,14 +344,14 @@ __device__ __forceinline__ RowInfo row_info(const RowJob& j, int m) {
       const int r = m / g, k = m % g + 1;
       o.r = r;
       o.urow = m;
-      o.trow = (long long)r * (g + 1) + (k - 1);
+      o.trow = target_row(j, r, k - 1);
       if (j.rank > 0) o.prev = checked_token(j, k == 1 ? j.anchors[r] : j.tokens[(size_t)m - 1]);
       break;
     }
     case MAP_FINAL: {
       const int r = m, n = j.final_n[r];
       o.r = r;
-      o.trow = (long long)r * (g + 1) + n;
+      o.trow = target_row(j, r, n);
       o.resid = j.final_kind[r];
       if (o.resid) {
         o.urow = (long long)r * g + n;
@@ -340,9 +361,14 @@ __device__ __forceinline__ RowInfo row_info(const RowJob& j, int m) {
       break;
     }
     default: {  // MAP_TARGET
+      o.trow = m;
+      if (j.toff) {  // flattened: the first toff[R] rows are the batch
+        o.r = 0;      // target rows have no draft side
+        o.active = m < j.toff[j.R];
+        break;
+      }
       const int r = m / (g + 1), i = m % (g + 1);
       o.r = r;
-      o.trow = m;
       if (j.lengths) o.active = i <= checked_length(j, r);
       break;
     }

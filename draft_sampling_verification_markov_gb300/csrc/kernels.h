@@ -52,22 +52,27 @@ void launch_finalize_stats(int rows, int nseg, const float* pm, const float* ps,
                            const int32_t* lengths, int rows_per_req, uint32_t* status,
                            cudaStream_t s);
 void launch_greedy_scan(int R, int gamma, const int* amax, const int32_t* tokens,
-                        const int32_t* lengths, int32_t* accept_len, int32_t* out_tokens,
-                        int32_t* next_anchor, uint32_t* status, cudaStream_t s);
+                        const int32_t* lengths, const int32_t* toff, int32_t* accept_len,
+                        int32_t* out_tokens, int32_t* next_anchor, uint32_t* status,
+                        cudaStream_t s);
 // Per-row (m, log Z) and/or first argmax of target rows (MAP_TARGET job), one block per row.
 void launch_row_stats(const RowJob& j, int dtype, bool vec, float* stats, int* argmax,
                       cudaStream_t s);
 void launch_accept(int dtype, int R, int gamma, int V, float scale, const void* T,
                    const float* tstats, const int32_t* tokens, const float* dlogp,
-                   const float* u_accept, const int32_t* lengths, int32_t* final_n,
-                   int32_t* final_kind, int32_t* accept_len, int32_t* out_tokens,
-                   uint32_t* status, RowPrefetch pf, cudaStream_t s);
+                   const float* u_accept, const int32_t* lengths, const int32_t* toff,
+                   int32_t* final_n, int32_t* final_kind, int32_t* accept_len,
+                   int32_t* out_tokens, uint32_t* status, RowPrefetch pf, cudaStream_t s);
 void launch_tv_finalize(int R, int gamma, int nseg, const float* ps, float* conf, float* survival,
                         cudaStream_t s);
 cudaError_t launch_schedule(const float* survival, const double* sps, int Bmax, int R, int gamma,
-                            int32_t* lengths, int32_t* B_out, double* theta_out, uint32_t* status,
+                            const int32_t* b_cap, int32_t* lengths, int32_t* B_out,
+                            double* theta_out, int32_t* B_opt_out, uint32_t* status,
                             cudaStream_t s);
 size_t schedule_smem_bytes(int R, int gamma);
+// Flattened verify batch layout from per-request lengths (offsets [R+1], optional row markers).
+void launch_flat_layout(const int32_t* lengths, int R, int gamma, int32_t* offsets,
+                        int32_t* row_req, int32_t* row_pos, uint32_t* status, cudaStream_t s);
 
 // tcgen05 Markov producer (markov_tc.cu). Returns false when the shape is not supported
 // (the caller then uses the CUDA-core producer).

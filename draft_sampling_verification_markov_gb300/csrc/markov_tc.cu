@@ -407,12 +407,12 @@ __device__ __forceinline__ void row_norms_tc(const RowJob& j, const TileRow& tr,
   resid = true;
   if (!tr.valid) return;
   if constexpr (MODE == MODE_TV) {
-    tn = load_norm(j.tstats, (long long)tr.r * (j.gamma + 1) + (tr.k - 1));
+    tn = load_norm(j.tstats, target_row(j, tr.r, tr.k - 1));
     dn = load_norm(j.dstats, (long long)tr.r * j.gamma + (tr.k - 1));
   } else {
     const int n = j.final_n[tr.r];
     resid = j.final_kind[tr.r] != 0;
-    tn = load_norm(j.tstats, (long long)tr.r * (j.gamma + 1) + n);
+    tn = load_norm(j.tstats, target_row(j, tr.r, n));
     if (resid) dn = load_norm(j.dstats, (long long)tr.r * j.gamma + n);
   }
 }
@@ -550,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int tr = 0, ur = 0;
             if (r < j.R && q / kBM < nb) {
               const int n = j.final_n[r];
-              tr = r * (j.gamma + 1) + n;
+              tr = (int)target_row(j, r, n);
               if (j.final_kind[r]) ur = r * j.gamma + n;
             }
             row_t[q] = tr;

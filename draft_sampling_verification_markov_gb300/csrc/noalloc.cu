@@ -95,8 +95,8 @@ extern "C" int spec_verify_greedy_noalloc(const void* target, int t_dtype,
   j.lengths = lengths;
   j.status = status;
   launch_row_stats(j, t_dtype, vec_loads(target, t_dtype, V), nullptr, amax, s);
-  launch_greedy_scan(R, gamma, amax, draft_tokens, lengths, accept_len, out_tokens, next_anchor,
-                     status, s);
+  launch_greedy_scan(R, gamma, amax, draft_tokens, lengths, nullptr, accept_len, out_tokens,
+                     next_anchor, status, s);
   if (device_status &&
       cudaMemcpyAsync(device_status, status, sizeof(uint32_t), cudaMemcpyDeviceToDevice, s) !=
           cudaSuccess)

@@ -854,8 +854,9 @@ __global__ void finalize_stats_kernel(int rows, int nseg, const float* pm, const
 
 // Greedy longest-prefix match + bonus, one thread per request, from per-row target argmaxes.
 __global__ void greedy_scan_kernel(int R, int gamma, const int* amax, const int32_t* tokens,
-                                   const int32_t* lengths, int32_t* accept_len,
-                                   int32_t* out_tokens, int32_t* next_anchor, uint32_t* status) {
+                                   const int32_t* lengths, const int32_t* toff,
+                                   int32_t* accept_len, int32_t* out_tokens,
+                                   int32_t* next_anchor, uint32_t* status) {
   const int r = blockIdx.x * blockDim.x + threadIdx.x;
   if (r >= R) return;
   int l = gamma;
@@ -868,7 +869,7 @@ __global__ void greedy_scan_kernel(int R, int gamma, const int* amax, const int3
   }
   int n = 0, y = 0;
   for (int i = 0; i <= l; ++i) {
-    y = amax[(size_t)r * (gamma + 1) + i];
+    y = amax[target_row(toff, R, gamma, r, i, status)];
     if (i == l || tokens[(size_t)r * gamma + i] != y) break;
     n = i + 1;
   }
@@ -888,9 +889,10 @@ __global__ void greedy_scan_kernel(int R, int gamma, const int* amax, const int3
 template <int DT>
 __global__ void accept_kernel(int R, int gamma, int V, float scale, const void* T,
                               const float* tstats, const int32_t* tokens, const float* dlogp,
-                              const float* u_accept, const int32_t* lengths, int32_t* final_n,
-                              int32_t* final_kind, int32_t* accept_len, int32_t* out_tokens,
-                              uint32_t* status, RowPrefetch pf) {
+                              const float* u_accept, const int32_t* lengths,
+                              const int32_t* toff, int32_t* final_n, int32_t* final_kind,
+                              int32_t* accept_len, int32_t* out_tokens, uint32_t* status,
+                              RowPrefetch pf) {
   const int lane = threadIdx.x & 31;
   const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (r >= R) return;
@@ -912,7 +914,7 @@ __global__ void accept_kernel(int R, int gamma, int V, float scale, const void* 
         atomicOr(status, SPEC_DEV_BAD_TOKEN);
         reject = true;  // an invalid proposal is rejected
       } else {
-        const long long trow = (long long)r * (gamma + 1) + k;
+        const long long trow = target_row(toff, R, gamma, r, k, status);
         const float t = __fmul_rn(ld_elem<DT>(T, (size_t)trow * V + x), scale);
         const float pt = prob_of(t, load_norm(tstats, trow));
         const float pd = fast_exp2(dlogp[(size_t)r * gamma + k] * kLog2e);  // exp(log p_d)
@@ -1062,27 +1064,28 @@ void launch_finalize_stats(int rows, int nseg, const float* pm, const float* ps,
 }
 
 void launch_greedy_scan(int R, int gamma, const int* amax, const int32_t* tokens,
-                        const int32_t* lengths, int32_t* accept_len, int32_t* out_tokens,
-                        int32_t* next_anchor, uint32_t* status, cudaStream_t s) {
+                        const int32_t* lengths, const int32_t* toff, int32_t* accept_len,
+                        int32_t* out_tokens, int32_t* next_anchor, uint32_t* status,
+                        cudaStream_t s) {
   TraceScope ts(SPEC_KCLASS_OTHER, s);
-  greedy_scan_kernel<<<(R + 127) / 128, 128, 0, s>>>(R, gamma, amax, tokens, lengths, accept_len,
-                                                     out_tokens, next_anchor, status);
+  greedy_scan_kernel<<<(R + 127) / 128, 128, 0, s>>>(R, gamma, amax, tokens, lengths, toff,
+                                                     accept_len, out_tokens, next_anchor, status);
 }
 
 void launch_accept(int dtype, int R, int gamma, int V, float scale, const void* T,
                    const float* tstats, const int32_t* tokens, const float* dlogp,
-                   const float* u_accept, const int32_t* lengths, int32_t* final_n,
-                   int32_t* final_kind, int32_t* accept_len, int32_t* out_tokens,
-                   uint32_t* status, RowPrefetch pf, cudaStream_t s) {
+                   const float* u_accept, const int32_t* lengths, const int32_t* toff,
+                   int32_t* final_n, int32_t* final_kind, int32_t* accept_len,
+                   int32_t* out_tokens, uint32_t* status, RowPrefetch pf, cudaStream_t s) {
   TraceScope ts(SPEC_KCLASS_OTHER, s);
   const int grid = (R + 7) / 8;  // one warp per request, 8 warps per block
   if (dtype == SPEC_BF16)
     accept_kernel<SPEC_BF16><<<grid, 256, 0, s>>>(R, gamma, V, scale, T, tstats, tokens, dlogp,
-                                                  u_accept, lengths, final_n, final_kind,
+                                                  u_accept, lengths, toff, final_n, final_kind,
                                                   accept_len, out_tokens, status, pf);
   else
     accept_kernel<SPEC_F32><<<grid, 256, 0, s>>>(R, gamma, V, scale, T, tstats, tokens, dlogp,
-                                                 u_accept, lengths, final_n, final_kind,
+                                                 u_accept, lengths, toff, final_n, final_kind,
                                                  accept_len, out_tokens, status, pf);
 }
 

@@ -13,6 +13,12 @@
 //   4. l_r = number of selected candidates of request r.
 // The integer prefix sums and the single IEEE multiply make the result independent of the
 // summation order, so it is bit-identical to any implementation of the same definition.
+//
+// Dynamic top-K (section 7): with a device-resident capacity B_cap (a batch size decided from an
+// earlier step's confidences) the selection is K = clamp(B_cap - R, 0, Kmax), the first K
+// candidates of the current queue, and Theta(K) is reported for that K. The search of step 3 still
+// runs on the same sorted queue, and its optimum R + K* can be written out as the capacity of a
+// later step, so one sort serves both.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -26,8 +32,10 @@ constexpr int kSchedThreads = 1024;
 __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float* survival,
                                                                  const double* sps, int Bmax,
                                                                  int R, int gamma, int npow2,
+                                                                 const int32_t* b_cap,
                                                                  int32_t* lengths, int32_t* B_out,
                                                                  double* theta_out,
+                                                                 int32_t* B_opt_out,
                                                                  uint32_t* status) {
   extern __shared__ __align__(16) unsigned char smem[];
   unsigned long long* key = reinterpret_cast<unsigned long long*>(smem);  // [npow2]
@@ -35,6 +43,7 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float* su
   __shared__ unsigned long long warp_tot[32];
   __shared__ double best_theta[32];
   __shared__ int best_k[32];
+  __shared__ double fixed_theta;
 
   const int n = R * gamma;
   const int tid = threadIdx.x;
@@ -110,17 +119,26 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float* su
   // 3. Theta(K) for K in [0, Kmax]; thread t evaluates K = slot + 1 for its slots (and K = 0)
   const int Kmax = min(n, Bmax - R);
   const unsigned long long base = (unsigned long long)R << 32;
+  int Kcap = -1;  // fixed K of the dynamic top-K, -1 for the Theta search
+  if (b_cap) {
+    const int cap = *b_cap;
+    if (cap < 0 && tid == 0) atomicOr(status, SPEC_DEV_BAD_LENGTH);
+    const long long want = (long long)cap - R;
+    Kcap = want <= 0 ? 0 : (want < Kmax ? (int)want : Kmax);
+  }
   double bt = -1.0;
   int bk = 0x7fffffff;
   if (tid == 0) {
     bt = (double)base * sps[R];
     bk = 0;
+    if (Kcap == 0) fixed_theta = bt;
   }
   for (int s = s0; s < s1; ++s) {
     S += q_of(s);
     const int K = s + 1;
     if (K > Kmax) break;
     const double th = (double)(base + S) * sps[R + K];
+    if (K == Kcap) fixed_theta = th;  // exactly one thread holds slot Kcap - 1
     if (th > bt) {  // slots ascend, so the first maximum in this run has the smallest K
       bt = th;
       bk = K;
@@ -161,17 +179,19 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float* su
   }
   __syncthreads();
   const int Kstar = best_k[0];
+  const int Ksel = Kcap >= 0 ? Kcap : Kstar;
 
   // 4. lengths
-  for (int s = tid; s < Kstar; s += blockDim.x) {
+  for (int s = tid; s < Ksel; s += blockDim.x) {
     const int idx = (int)(key[s] & 0xffffffffull);
     atomicAdd(&len[idx / gamma], 1);
   }
   __syncthreads();
   for (int r = tid; r < R; r += blockDim.x) lengths[r] = len[r];
   if (tid == 0) {
-    *B_out = R + Kstar;
-    *theta_out = best_theta[0] / 4294967296.0;
+    *B_out = R + Ksel;
+    *theta_out = (Kcap >= 0 ? fixed_theta : best_theta[0]) / 4294967296.0;
+    if (B_opt_out) *B_opt_out = R + Kstar;
   }
 }
 
@@ -182,7 +202,8 @@ size_t schedule_smem_bytes(int R, int gamma) {
 }
 
 cudaError_t launch_schedule(const float* survival, const double* sps, int Bmax, int R, int gamma,
-                            int32_t* lengths, int32_t* B_out, double* theta_out, uint32_t* status,
+                            const int32_t* b_cap, int32_t* lengths, int32_t* B_out,
+                            double* theta_out, int32_t* B_opt_out, uint32_t* status,
                             cudaStream_t s) {
   int n = R * gamma, p = 1;
   while (p < n) p <<= 1;
@@ -191,9 +212,80 @@ cudaError_t launch_schedule(const float* survival, const double* sps, int Bmax, 
   cudaError_t e = cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  schedule_kernel<<<1, kSchedThreads, smem, s>>>(survival, sps, Bmax, R, gamma, p, lengths, B_out,
-                                                 theta_out, status);
+  schedule_kernel<<<1, kSchedThreads, smem, s>>>(survival, sps, Bmax, R, gamma, p, b_cap, lengths,
+                                                 B_out, theta_out, B_opt_out, status);
   return cudaGetLastError();
+}
+
+// Flattened verify batch ("[DeepSeek-6] DSpark", section 7: physical execution decoupled from
+// the logical sequences, with a marker tensor carrying the per-sequence structure): request r
+// owns the 1 + l_r packed target rows offsets[r] .. offsets[r+1]-1 (positions 0..l_r), and the
+// markers give each packed row its request and position (-1 past the batch). One CTA: every
+// thread sums a contiguous run of requests, a block scan gives each run its first row.
+__global__ void __launch_bounds__(kSchedThreads) flat_layout_kernel(const int32_t* lengths, int R,
+                                                                    int gamma, int32_t* offsets,
+                                                                    int32_t* row_req,
+                                                                    int32_t* row_pos,
+                                                                    uint32_t* status) {
+  __shared__ int warp_tot[32];
+  __shared__ int total;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  auto len = [&](int r) {
+    int l = lengths[r];
+    if (l < 0 || l > gamma) {
+      atomicOr(status, SPEC_DEV_BAD_LENGTH);
+      l = l < 0 ? 0 : gamma;
+    }
+    return l;
+  };
+  const int per = (R + blockDim.x - 1) / blockDim.x;
+  const int r0 = min(R, tid * per), r1 = min(R, r0 + per);
+  int local = 0;
+  for (int r = r0; r < r1; ++r) local += 1 + len(r);
+  int inc = local;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, inc, off);
+    if (lane >= off) inc += y;
+  }
+  if (lane == 31) warp_tot[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = blockDim.x >> 5;
+    const int w = lane < nw ? warp_tot[lane] : 0;
+    int wi = w;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, wi, off);
+      if (lane >= off) wi += y;
+    }
+    if (lane < nw) warp_tot[lane] = wi - w;
+    if (lane == 31) total = wi;
+  }
+  __syncthreads();
+  int S = warp_tot[warp] + inc - local;  // first packed row of this thread's requests
+  for (int r = r0; r < r1; ++r) {
+    const int l = len(r);
+    offsets[r] = S;
+    if (row_req)
+      for (int i = 0; i <= l; ++i) row_req[S + i] = r;
+    if (row_pos)
+      for (int i = 0; i <= l; ++i) row_pos[S + i] = i;
+    S += 1 + l;
+  }
+  const int B = total;
+  if (tid == 0) offsets[R] = B;
+  const int cap = R * (gamma + 1);
+  for (int b = B + tid; b < cap; b += blockDim.x) {
+    if (row_req) row_req[b] = -1;
+    if (row_pos) row_pos[b] = -1;
+  }
+}
+
+void launch_flat_layout(const int32_t* lengths, int R, int gamma, int32_t* offsets,
+                        int32_t* row_req, int32_t* row_pos, uint32_t* status, cudaStream_t s) {
+  flat_layout_kernel<<<1, kSchedThreads, 0, s>>>(lengths, R, gamma, offsets, row_req, row_pos,
+                                                 status);
 }
 
 }  // namespace spec

@@ -27,10 +27,17 @@ class SpecLoop:
     sps [Bmax + 1] fp64 (index = batch size B). With schedule=False every request verifies
     all gamma positions (no confidence pass, no scheduler). `allowed` (optional, [R, ceil(V/32)]
     32-bit words) restricts every draft position to the allowed tokens (grammar-masked
-    drafting), in the proposal, the confidence pass and the residual alike."""
+    drafting), in the proposal, the confidence pass and the residual alike.
+
+    async_schedule=True is the production form of the scheduler ("[DeepSeek-6] DSpark",
+    section 7): iteration t still ranks its own candidates by its own survival, but the batch
+    size it fills is the Theta-optimal one of iteration t - 2 (dynamic top-K). The first two
+    iterations have no such history and use their own Theta optimum. One scheduler launch per
+    iteration both selects and records the Theta optimum for iteration t + 2 (batch_opt)."""
 
     def __init__(self, U, target, W1, W2, anchors0, u_draft, u_accept, u_resid, temperature,
-                 sps=None, *, iterations=None, schedule=True, allowed=None):
+                 sps=None, *, iterations=None, schedule=True, allowed=None,
+                 async_schedule=False):
         R, gamma, V = U.shape
         self.R, self.gamma, self.V = R, gamma, V
         self.iters = int(iterations if iterations is not None else u_draft.shape[0])
@@ -40,6 +47,7 @@ class SpecLoop:
         self.sps = sps
         self.allowed = allowed
         self.schedule = bool(schedule) and sps is not None
+        self.async_schedule = self.schedule and bool(async_schedule)
         self.rank = 0 if W1 is None else int(W1.shape[1])
         dev = U.device
         i32 = dict(dtype=torch.int32, device=dev)
@@ -55,6 +63,8 @@ class SpecLoop:
         self.survival = torch.empty(n, R, gamma, **f32)
         self.lengths = torch.empty(n, R, **i32)
         self.batch = torch.empty(n, **i32)
+        # Theta-optimal batch of iteration t >= 2 in async mode (for t < 2 it is batch[t])
+        self.batch_opt = torch.empty(n, **i32)
         self.theta = torch.empty(n, dtype=torch.float64, device=dev)
         self.accept_len = torch.empty(n, R, **i32)
         self.out_tokens = torch.empty(n, R, gamma + 1, **i32)
@@ -79,9 +89,15 @@ class SpecLoop:
                                  target_stats=self.target_stats, conf=self.conf[t],
                                  survival=self.survival[t], workspace=ws, stream=stream,
                                  allowed=self.allowed)
-            S.spec_schedule_prefix(self.survival[t], self.sps, lengths=self.lengths[t],
-                                   B_out=self.batch[t:t + 1], theta_out=self.theta[t:t + 1],
-                                   workspace=ws, stream=stream)
+            out = dict(lengths=self.lengths[t], B_out=self.batch[t:t + 1],
+                       theta_out=self.theta[t:t + 1], workspace=ws, stream=stream)
+            if self.async_schedule and t >= 2:
+                # iterations 0 and 1 chose their own optimum, so it sits in `batch`
+                hist = self.batch if t < 4 else self.batch_opt
+                S.spec_schedule_prefix(self.survival[t], self.sps, capacity=hist[t - 2:t - 1],
+                                       B_opt_out=self.batch_opt[t:t + 1], **out)
+            else:
+                S.spec_schedule_prefix(self.survival[t], self.sps, **out)
             lengths = self.lengths[t]
         S.spec_verify_rejection(self.target, self.U, self.W1, self.W2, a_t, self.draft_tokens[t],
                                 self.draft_logp, self.draft_stats, self.u_accept[t],

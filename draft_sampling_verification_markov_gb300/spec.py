@@ -62,6 +62,7 @@ def lib():
         L.spec_tv_confidence.argtypes = [vp, vp, i, vp, vp, i, i, vp, vp, vp, vp, f, i, i, i, vp,
                                          vp, vp, sz, vp]
         L.spec_schedule_prefix.argtypes = [vp, vp, i, i, i, vp, vp, vp, vp, sz, vp]
+        L.spec_schedule_topk.argtypes = [vp, vp, i, i, i, vp, vp, vp, vp, vp, vp, sz, vp]
         L.spec_verify_greedy_noalloc.argtypes = [vp, i, vp, vp, i, i, i, vp, vp, vp, vp, vp]
         L.spec_markov_propose_masked.argtypes = [vp, i, vp, vp, i, i, vp, vp, f, i, i, i, vp, vp,
                                                  vp, vp, vp, sz, vp]
@@ -70,6 +71,12 @@ def lib():
                                                    sz, vp]
         L.spec_tv_confidence_masked.argtypes = [vp, vp, i, vp, vp, i, i, vp, vp, vp, vp, f, i, i,
                                                 i, vp, vp, vp, vp, sz, vp]
+        L.spec_flat_layout.argtypes = [vp, i, i, vp, vp, vp, vp, sz, vp]
+        L.spec_target_stats_flat.argtypes = [vp, i, f, i, i, i, vp, vp, vp, sz, vp]
+        L.spec_verify_greedy_flat.argtypes = [vp, i, vp, vp, vp, i, i, i, vp, vp, vp, vp, sz, vp]
+        L.spec_verify_rejection_flat.argtypes = [vp, vp, i, vp, vp, i, i, vp, vp, vp, vp, vp, vp,
+                                                 vp, f, vp, vp, i, i, i, vp, vp, vp, vp, vp, sz,
+                                                 vp]
         L.spec_launch_count.restype = ctypes.c_ulonglong
         L.spec_trace_events.argtypes = [i, vp, vp, i]
         L.spec_trace_events.restype = i
@@ -77,9 +84,11 @@ def lib():
         L.spec_trace_count.restype = i
         for name in ("spec_workspace_init", "spec_device_status", "spec_markov_propose",
                      "spec_verify_greedy", "spec_target_stats", "spec_verify_rejection",
-                     "spec_tv_confidence", "spec_schedule_prefix",
+                     "spec_tv_confidence", "spec_schedule_prefix", "spec_schedule_topk",
                      "spec_verify_greedy_noalloc", "spec_markov_propose_masked",
-                     "spec_verify_rejection_masked", "spec_tv_confidence_masked"):
+                     "spec_verify_rejection_masked", "spec_tv_confidence_masked",
+                     "spec_flat_layout", "spec_target_stats_flat", "spec_verify_greedy_flat",
+                     "spec_verify_rejection_flat"):
             getattr(L, name).restype = i
         _lib = L
     return _lib
@@ -327,7 +336,11 @@ def spec_tv_confidence(U, target, W1, W2, anchors, draft_tokens, temperature, *,
 
 
 def spec_schedule_prefix(survival, sps, *, lengths=None, B_out=None, theta_out=None,
-                         workspace=None, stream=None):
+                         workspace=None, stream=None, capacity=None, B_opt_out=None):
+    """Prefix scheduler. With `capacity` (a [1] int32 device tensor holding a batch size,
+    typically the Theta-optimal batch of an earlier step) it is the dynamic top-K selection
+    instead of the Theta search; `B_opt_out` ([1] int32, optional) then receives this step's
+    Theta-optimal batch size."""
     R, gamma = survival.shape
     dev = survival.device
     if lengths is None:
@@ -338,11 +351,133 @@ def spec_schedule_prefix(survival, sps, *, lengths=None, B_out=None, theta_out=N
         theta_out = torch.empty(1, dtype=torch.float64, device=dev)
     ws = workspace or default_workspace(dev)
     ws.reserve(256, stream)
-    rc = lib().spec_schedule_prefix(_ptr(survival), _ptr(sps), sps.numel() - 1, R, gamma,
-                                    _ptr(lengths), _ptr(B_out), _ptr(theta_out), ws.ptr,
-                                    ws.nbytes, _stream(stream))
+    if capacity is None:
+        if B_opt_out is not None:
+            raise ValueError("B_opt_out is an output of the capacity form")
+        rc = lib().spec_schedule_prefix(_ptr(survival), _ptr(sps), sps.numel() - 1, R, gamma,
+                                        _ptr(lengths), _ptr(B_out), _ptr(theta_out), ws.ptr,
+                                        ws.nbytes, _stream(stream))
+    else:
+        if capacity.dtype != torch.int32 or capacity.numel() < 1 or capacity.device != dev:
+            raise ValueError("capacity must be an int32 tensor on the survival's device")
+        if B_opt_out is not None and (B_opt_out.dtype != torch.int32 or B_opt_out.device != dev):
+            raise ValueError("B_opt_out must be an int32 tensor on the survival's device")
+        rc = lib().spec_schedule_topk(_ptr(survival), _ptr(sps), sps.numel() - 1, R, gamma,
+                                      _ptr(capacity), _ptr(lengths), _ptr(B_out),
+                                      _ptr(theta_out),
+                                      None if B_opt_out is None else _ptr(B_opt_out), ws.ptr,
+                                      ws.nbytes, _stream(stream))
     _check("spec_schedule_prefix", rc)
     return lengths, B_out, theta_out
+
+
+# ----------------------------------------------------------------------------- flattened batch
+
+def _i32_on(t, dev, name):
+    if t.dtype != torch.int32 or t.device != dev:
+        raise ValueError(f"{name} must be an int32 tensor on {dev}")
+    return t
+
+
+def spec_flat_layout(lengths, gamma, *, offsets=None, row_req=None, row_pos=None, markers=True,
+                     workspace=None, stream=None):
+    """Packed-row layout of a variable-length verify batch: offsets [R+1] (offsets[R] = B) and,
+    with markers=True, the request / position of each of the R*(gamma+1) packed rows (-1 past
+    B). Returns (offsets, row_req, row_pos)."""
+    R = lengths.shape[0]
+    dev = lengths.device
+    _i32_on(lengths, dev, "lengths")
+    if offsets is None:
+        offsets = torch.empty(R + 1, dtype=torch.int32, device=dev)
+    if markers and row_req is None:
+        row_req = torch.empty(R * (gamma + 1), dtype=torch.int32, device=dev)
+    if markers and row_pos is None:
+        row_pos = torch.empty(R * (gamma + 1), dtype=torch.int32, device=dev)
+    ws = workspace or default_workspace(dev)
+    ws.reserve(256, stream)
+    rc = lib().spec_flat_layout(_ptr(lengths), R, int(gamma), _ptr(offsets), _ptr(row_req),
+                                _ptr(row_pos), ws.ptr, ws.nbytes, _stream(stream))
+    _check("spec_flat_layout", rc)
+    return offsets, row_req, row_pos
+
+
+def spec_target_stats_flat(target, temperature, offsets, gamma, *, stats=None, workspace=None,
+                           stream=None):
+    """(m, log Z) of the packed target rows b < offsets[R]; target [R*(gamma+1), V]."""
+    R = offsets.shape[0] - 1
+    V = target.shape[-1]
+    dev = target.device
+    if target.numel() != R * (gamma + 1) * V:
+        raise ValueError("a packed target holds R*(gamma+1) rows")
+    _i32_on(offsets, dev, "offsets")
+    if stats is None:
+        stats = torch.empty(R * (gamma + 1), 2, dtype=torch.float32, device=dev)
+    ws = workspace or default_workspace(dev)
+    wp, wn = ws.for_op(SPEC_OP_TARGET_STATS, R, gamma, V, 0, stream)
+    rc = lib().spec_target_stats_flat(_ptr(target), _dt(target), float(temperature), R,
+                                      int(gamma), V, _ptr(offsets), _ptr(stats), wp, wn,
+                                      _stream(stream))
+    _check("spec_target_stats_flat", rc)
+    return stats
+
+
+def spec_verify_greedy_flat(target, draft_tokens, lengths, offsets, *, accept_len=None,
+                            out_tokens=None, next_anchor=None, workspace=None, stream=None):
+    """Greedy verify with the target rows packed by spec_flat_layout (target [R*(gamma+1), V])."""
+    R, gamma = draft_tokens.shape
+    V = target.shape[-1]
+    dev = target.device
+    if target.numel() != R * (gamma + 1) * V:
+        raise ValueError("a packed target holds R*(gamma+1) rows")
+    _i32_on(lengths, dev, "lengths")
+    _i32_on(offsets, dev, "offsets")
+    if accept_len is None:
+        accept_len = torch.empty(R, dtype=torch.int32, device=dev)
+    if out_tokens is None:
+        out_tokens = torch.empty(R, gamma + 1, dtype=torch.int32, device=dev)
+    if next_anchor is None:
+        next_anchor = torch.empty(R, dtype=torch.int32, device=dev)
+    ws = workspace or default_workspace(dev)
+    wp, wn = ws.for_op(SPEC_OP_VERIFY_GREEDY, R, gamma, V, 0, stream)
+    rc = lib().spec_verify_greedy_flat(_ptr(target), _dt(target), _ptr(draft_tokens),
+                                       _ptr(lengths), _ptr(offsets), R, gamma, V,
+                                       _ptr(accept_len), _ptr(out_tokens), _ptr(next_anchor),
+                                       wp, wn, _stream(stream))
+    _check("spec_verify_greedy_flat", rc)
+    return accept_len, out_tokens, next_anchor
+
+
+def spec_verify_rejection_flat(target, U, W1, W2, anchors, draft_tokens, draft_logp,
+                               draft_stats, u_accept, u_resid, temperature, lengths, offsets, *,
+                               rank=None, target_stats=None, accept_len=None, out_tokens=None,
+                               next_anchor=None, workspace=None, stream=None, allowed=None):
+    """Rejection verify with the target rows (and target_stats, if given) packed by
+    spec_flat_layout; everything else keeps its per-request layout."""
+    R, gamma, V = U.shape
+    rank = _rank_of(W1, rank)
+    dev = U.device
+    if target.numel() != R * (gamma + 1) * V:
+        raise ValueError("a packed target holds R*(gamma+1) rows")
+    _i32_on(lengths, dev, "lengths")
+    _i32_on(offsets, dev, "offsets")
+    if accept_len is None:
+        accept_len = torch.empty(R, dtype=torch.int32, device=dev)
+    if out_tokens is None:
+        out_tokens = torch.empty(R, gamma + 1, dtype=torch.int32, device=dev)
+    if next_anchor is None:
+        next_anchor = torch.empty(R, dtype=torch.int32, device=dev)
+    ws = workspace or default_workspace(dev)
+    wp, wn = ws.for_op(SPEC_OP_VERIFY_REJECTION, R, gamma, V, rank, stream)
+    wdt = _dt(W1) if W1 is not None else SPEC_BF16
+    mask = None if allowed is None else _mask(allowed, R, V)
+    rc = lib().spec_verify_rejection_flat(
+        _ptr(target), _ptr(U), _dt(U), _ptr(W1), _ptr(W2), wdt, rank, _ptr(anchors),
+        _ptr(draft_tokens), _ptr(draft_logp), _ptr(draft_stats), _ptr(target_stats),
+        _ptr(u_accept), _ptr(u_resid), float(temperature), _ptr(lengths), _ptr(offsets), R,
+        gamma, V, _ptr(accept_len), _ptr(out_tokens), _ptr(next_anchor), _ptr(mask), wp, wn,
+        _stream(stream))
+    _check("spec_verify_rejection_flat", rc)
+    return accept_len, out_tokens, next_anchor
 
 
 def spec_device_status(workspace=None, clear=True, stream=None) -> int:

@@ -265,6 +265,87 @@ int spec_schedule_prefix(const float* survival, const double* sps, int Bmax, int
                          int32_t* lengths, int32_t* B_out, double* theta_out, void* ws,
                          size_t ws_bytes, void* stream);
 
+/*
+ * Dynamic top-K prefix selection.
+ * Defines: "[DeepSeek-6] DSpark", section 7 (asynchronous scheduling): the verify batch size is
+ *   decided from confidences computed steps earlier, and the current step fills that capacity
+ *   with its own highest-survival candidates. With capacity B the first
+ *   K = clamp(B - R, 0, min(R*gamma, Bmax-R)) candidates of the same queue as
+ *   spec_schedule_prefix (a desc, r asc, j asc) are selected, so the selection is prefix-closed
+ *   per request and equals spec_schedule_prefix's whenever B is that scheduler's optimum.
+ * Arguments as spec_schedule_prefix, plus:
+ *   capacity [1] int32 device pointer: the batch size B (typically B_out of an earlier call).
+ *            It is read by the kernel, so it may be written by earlier work on `stream`.
+ *   theta_out receives Theta at the selected K; B_out receives R + K.
+ *   B_opt_out [1] int32 device pointer or NULL: receives the batch size spec_schedule_prefix
+ *            would choose for this survival (R + K*), the capacity of a later step. The same
+ *            sorted queue serves both, so this costs no second sort.
+ * A negative capacity selects K = 0 and sets SPEC_DEV_BAD_LENGTH in the device status word.
+ * Returns SPEC_ERR_INVALID_ARG for a null capacity, otherwise as spec_schedule_prefix.
+ */
+int spec_schedule_topk(const float* survival, const double* sps, int Bmax, int R, int gamma,
+                       const int32_t* capacity, int32_t* lengths, int32_t* B_out,
+                       double* theta_out, int32_t* B_opt_out, void* ws, size_t ws_bytes,
+                       void* stream);
+
+/*
+ * Flattened (variable-length) verify batch.
+ * Defines: "[DeepSeek-6] DSpark", section 7 (production adaptation): padding every request to
+ *   the same query length would spend on padding the verify budget the scheduler just saved,
+ *   so the physical batch is the tokens of all requests flattened into independent rows, and
+ *   the per-sequence structure travels in a marker tensor.
+ * Layout: request r owns the 1 + l_r packed target rows offsets[r] .. offsets[r+1]-1 (its
+ *   verify positions 0..l_r, position l_r being the bonus position); B = offsets[R] is the
+ *   scheduler's batch size sum_r (1 + l_r). A packed target array is allocated for
+ *   R*(gamma+1) rows (the largest batch); only its first B rows are read.
+ *
+ * spec_flat_layout: from lengths [R] int32 in [0, gamma] (device) writes
+ *   offsets  [R+1] int32 (device, required) and the markers
+ *   row_req  [R*(gamma+1)] int32 request of each packed row (optional, -1 past B) and
+ *   row_pos  [R*(gamma+1)] int32 position of each packed row (optional, -1 past B).
+ *   A length outside [0, gamma] is clamped and sets SPEC_DEV_BAD_LENGTH. The workspace is
+ *   used for its status word only (ws_bytes >= 256).
+ */
+int spec_flat_layout(const int32_t* lengths, int R, int gamma, int32_t* offsets,
+                     int32_t* row_req, int32_t* row_pos, void* ws, size_t ws_bytes,
+                     void* stream);
+
+/*
+ * Target normalisers of a flattened batch: stats[b] = (m, log Z) of softmax(target[b,:] / T)
+ * for the packed rows b < offsets[R]; rows past the batch are neither read nor written.
+ * target [R*(gamma+1), V] packed, stats [R*(gamma+1), 2] fp32 (packed like target).
+ */
+int spec_target_stats_flat(const void* target, int t_dtype, float temperature, int R, int gamma,
+                           int V, const int32_t* offsets, float* stats, void* ws,
+                           size_t ws_bytes, void* stream);
+
+/*
+ * Greedy verification of a flattened batch: as spec_verify_greedy with target row (r, i) at
+ * packed row offsets[r] + i. lengths and offsets (from spec_flat_layout of the same lengths)
+ * are required; outputs keep the per-request [R, gamma+1] layout. Offsets that put a row
+ * outside the R*(gamma+1) packed rows set SPEC_DEV_BAD_LENGTH (the row is then read as row 0).
+ */
+int spec_verify_greedy_flat(const void* target, int t_dtype, const int32_t* draft_tokens,
+                            const int32_t* lengths, const int32_t* offsets, int R, int gamma,
+                            int V, int32_t* accept_len, int32_t* out_tokens,
+                            int32_t* next_anchor, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Rejection verification of a flattened batch: as spec_verify_rejection_masked with target
+ * row (r, i) at packed row offsets[r] + i; target_stats (optional) is packed the same way
+ * (spec_target_stats_flat). lengths and offsets are required; `allowed` may be NULL.
+ * U, draft tokens, draft statistics, uniforms and outputs keep their per-request layouts.
+ */
+int spec_verify_rejection_flat(const void* target, const void* U, int l_dtype, const void* W1,
+                               const void* W2, int w_dtype, int rank, const int32_t* anchors,
+                               const int32_t* draft_tokens, const float* draft_logp,
+                               const float* draft_stats, const float* target_stats,
+                               const float* u_accept, const float* u_resid, float temperature,
+                               const int32_t* lengths, const int32_t* offsets, int R, int gamma,
+                               int V, int32_t* accept_len, int32_t* out_tokens,
+                               int32_t* next_anchor, const uint32_t* allowed, void* ws,
+                               size_t ws_bytes, void* stream);
+
 /* Largest R * (gamma + 1) that spec_verify_greedy_noalloc accepts. */
 #define SPEC_NOALLOC_MAX_ROWS 65536
 

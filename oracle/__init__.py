@@ -91,6 +91,8 @@ def _load():
         lib.oracle_schedule_prefix.restype = i
         lib.oracle_schedule_topk.argtypes = [vp, vp, i, i, i, i, vp, vp, vp]
         lib.oracle_schedule_topk.restype = i
+        lib.oracle_flat_layout.argtypes = [vp, i, i, vp, vp, vp]
+        lib.oracle_flat_layout.restype = i
         del c_i32p
         _lib = lib
     return _lib
@@ -344,3 +346,16 @@ def schedule_topk(survival, sps, capacity):
                                       ctypes.cast(ctypes.byref(theta), ctypes.c_void_p))
     _check(rc, "oracle_schedule_topk")
     return dict(lengths=lengths, B=int(B.value), theta=float(theta.value))
+
+
+def flat_layout(lengths, gamma):
+    """Packed-row layout of a variable-length verify batch (DSpark section 7): offsets [R+1],
+    and the request / position of each of the R*(gamma+1) packed rows (-1 past the batch)."""
+    ln = _i32(lengths)
+    R = ln.shape[0]
+    offsets = np.empty(R + 1, dtype=np.int32)
+    row_req = np.empty(R * (gamma + 1), dtype=np.int32)
+    row_pos = np.empty(R * (gamma + 1), dtype=np.int32)
+    _check(_load().oracle_flat_layout(_p(ln), R, int(gamma), _p(offsets), _p(row_req),
+                                      _p(row_pos)), "oracle_flat_layout")
+    return dict(offsets=offsets, row_req=row_req, row_pos=row_pos)

@@ -613,3 +613,28 @@ int oracle_schedule_topk(const float* survival, const double* sps, int Bmax, int
   if (capacity < 0) return ORACLE_ERR_INVALID_ARG;
   return schedule_impl(survival, sps, Bmax, R, gamma, capacity, lengths, B_out, theta_out);
 }
+
+/*
+ * Flattened verify batch (DSpark section 7: tokens of all requests flattened into independent
+ * rows, the sequence structure carried by a marker tensor). Request r's 1 + l_r target rows
+ * (positions 0..l_r) are packed rows offsets[r] .. offsets[r] + l_r, with offsets[0] = 0 and
+ * offsets[r+1] = offsets[r] + 1 + l_r; row_req / row_pos name the request and position of every
+ * packed row, -1 for the R*(gamma+1) - offsets[R] rows past the batch.
+ */
+int oracle_flat_layout(const int32_t* lengths, int R, int gamma, int32_t* offsets,
+                       int32_t* row_req, int32_t* row_pos) {
+  if (R < 0 || gamma < 0) return ORACLE_ERR_INVALID_ARG;
+  for (int r = 0; r < R; ++r)
+    if (lengths[r] < 0 || lengths[r] > gamma) return ORACLE_ERR_INVALID_ARG;
+  long long b = 0;
+  offsets[0] = 0;
+  for (int r = 0; r < R; ++r) {
+    for (int i = 0; i <= lengths[r]; ++i, ++b) {
+      row_req[b] = r;
+      row_pos[b] = i;
+    }
+    offsets[r + 1] = (int32_t)b;
+  }
+  for (long long c = (long long)R * (gamma + 1); b < c; ++b) row_req[b] = row_pos[b] = -1;
+  return ORACLE_OK;
+}

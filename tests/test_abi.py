@@ -89,6 +89,25 @@ def test_validation_rejects_before_launch(cuda_lib):
     # Bmax < R, and too many candidates
     assert sched(bogus, bogus, 3, 4, 2, bogus, bogus, bogus, bogus, 1024, None) == -1
     assert sched(bogus, bogus, 1 << 20, 2048, 16, bogus, bogus, bogus, bogus, 1024, None) == -1
+    topk = cuda_lib.spec_schedule_topk
+    topk.restype = ctypes.c_int
+    topk.argtypes = [vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp, vp, vp, vp, vp,
+                     ctypes.c_size_t, vp]
+    # no capacity, then Bmax < R
+    assert topk(bogus, bogus, 8, 4, 2, None, bogus, bogus, bogus, None, bogus, 1024, None) == -1
+    assert topk(bogus, bogus, 3, 4, 2, bogus, bogus, bogus, bogus, None, bogus, 1024, None) == -1
+    # flattened batch: lengths and offsets are required
+    fl = cuda_lib.spec_flat_layout
+    fl.restype = ctypes.c_int
+    fl.argtypes = [vp, ctypes.c_int, ctypes.c_int, vp, vp, vp, vp, ctypes.c_size_t, vp]
+    assert fl(None, 4, 3, bogus, None, None, bogus, 1024, None) == -1
+    assert fl(bogus, 4, 3, None, None, None, bogus, 1024, None) == -1
+    gf = cuda_lib.spec_verify_greedy_flat
+    gf.restype = ctypes.c_int
+    gf.argtypes = [vp, ctypes.c_int, vp, vp, vp] + [ctypes.c_int] * 3 + [vp] * 4 + [
+        ctypes.c_size_t, vp]
+    assert gf(bogus, 1, bogus, bogus, None, 4, 3, 8, bogus, None, None, bogus, 1 << 20,
+              None) == -1
     # the no-allocation greedy verify: beyond its fixed scratch, then a bad dtype
     na = cuda_lib.spec_verify_greedy_noalloc
     na.restype = ctypes.c_int

@@ -25,12 +25,12 @@ def spec():
     return s
 
 
-def _loop(spec, wl, schedule=True):
+def _loop(spec, wl, schedule=True, async_schedule=False):
     from draft_sampling_verification_markov_gb300.loop import SpecLoop
     g = {k: v.cuda() for k, v in wl.tensors().items()}
     return SpecLoop(g["U"], g["target"], g["W1"], g["W2"], g["anchors"], g["u_draft"],
                     g["u_accept"], g["u_resid"], wl.temperature, g.get("sps"),
-                    schedule=schedule)
+                    schedule=schedule, async_schedule=async_schedule)
 
 
 def check_iteration(lp, wl, t, sample=None, report=None):
@@ -51,7 +51,13 @@ def check_iteration(lp, wl, t, sample=None, report=None):
         assert_conf_close(lp.conf[t][sample], tv["conf"])
         assert_conf_close(lp.survival[t][sample], tv["survival"], "survival")
         # the scheduler sees every request: bit-exact on the GPU's survival
-        sch = oracle.schedule_prefix(lp.survival[t].cpu(), wl.sps.cpu().numpy())
+        sps = wl.sps.cpu().numpy()
+        sch = oracle.schedule_prefix(lp.survival[t].cpu(), sps)
+        if lp.async_schedule and t >= 2:
+            # dynamic top-K: capacity = the Theta optimum of iteration t - 2's survival
+            cap = oracle.schedule_prefix(lp.survival[t - 2].cpu(), sps)["B"]
+            assert int(lp.batch_opt[t].item()) == sch["B"]
+            sch = oracle.schedule_topk(lp.survival[t].cpu(), sps, cap)
         np.testing.assert_array_equal(lp.lengths[t].cpu().numpy(), sch["lengths"])
         assert int(lp.batch[t].item()) == sch["B"]
         assert float(lp.theta[t].item()) == sch["theta"]
@@ -74,10 +80,11 @@ def check_iteration(lp, wl, t, sample=None, report=None):
         report["verify_margin_cases"] = report.get("verify_margin_cases", 0) + int((diff & amb).sum())
 
 
-@pytest.mark.parametrize("schedule", [True, False])
+@pytest.mark.parametrize("schedule", [True, False, "async"])
 def test_loop_matches_oracle_iteration_by_iteration(spec, schedule):
-    wl = W.full_loop("cpu", R=6, gamma=4, V=1040, rank=64, iterations=3, seed=31)
-    lp = _loop(spec, wl, schedule)
+    iters = 6 if schedule == "async" else 3
+    wl = W.full_loop("cpu", R=6, gamma=4, V=1040, rank=64, iterations=iters, seed=31)
+    lp = _loop(spec, wl, bool(schedule), async_schedule=schedule == "async")
     lp.run()
     torch.cuda.synchronize()
     assert lp.ws.status() == 0
@@ -103,6 +110,22 @@ def test_loop_graph_replay_equals_eager(spec):
     graph.replay()                       # replays start again from anchors[0]
     torch.cuda.synchronize()
     assert torch.equal(first, graph.out_tokens)
+    assert eager.ws.status() == 0 and graph.ws.status() == 0
+
+
+def test_async_loop_graph_replay_equals_eager(spec):
+    """The asynchronous scheduler's capacity history lives on the device, so a captured graph of
+    the whole loop reproduces the eager run, including the top-K lengths."""
+    wl = W.full_loop("cpu", R=40, gamma=5, V=2048, rank=64, iterations=6, seed=35)
+    eager = _loop(spec, wl, async_schedule=True)
+    eager.run()
+    graph = _loop(spec, wl, async_schedule=True)
+    graph.capture()
+    graph.replay()
+    torch.cuda.synchronize()
+    for name in ("anchors", "lengths", "batch", "accept_len", "out_tokens", "theta"):
+        assert torch.equal(getattr(eager, name), getattr(graph, name)), name
+    assert torch.equal(eager.batch_opt[2:], graph.batch_opt[2:])
     assert eager.ws.status() == 0 and graph.ws.status() == 0
 
 

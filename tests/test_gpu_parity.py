@@ -184,6 +184,34 @@ def test_scheduler_bit_exact(spec, ws, R, gamma, kind):
     assert float(theta.item()) == ref["theta"]          # bit-identical
 
 
+@pytest.mark.parametrize("R,gamma,kind", [(1, 1, 0), (37, 7, 0), (512, 16, 1), (1024, 16, 2),
+                                          (16384, 1, 0)])
+def test_scheduler_topk_bit_exact(spec, ws, R, gamma, kind):
+    """Dynamic top-K: every capacity from below R to beyond Bmax, bit-exact against the oracle,
+    and the fused Theta optimum equals the plain scheduler's."""
+    a = W.random_survival(R, gamma, seed=7 * R + gamma)
+    if kind == 2:
+        a[:, :] = a[:, :1]
+    Bmax = R * (gamma + 1) - (R // 3)
+    sps = W.sps_table(Bmax) if kind == 1 else torch.from_numpy(
+        np.random.default_rng(R + 1).uniform(0.5, 1.0, Bmax + 1))
+    opt = oracle.schedule_prefix(a, sps.numpy())
+    caps = sorted({-5, 0, R - 1, R, R + 1, (R + Bmax) // 2, opt["B"], Bmax, Bmax + 3})
+    ad, sd = a.cuda(), sps.cuda()
+    for cap in caps:
+        c = torch.tensor([cap], dtype=torch.int32, device="cuda")
+        b_opt = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+        lengths, B, theta = spec.spec_schedule_prefix(ad, sd, workspace=ws, capacity=c,
+                                                      B_opt_out=b_opt)
+        ref = oracle.schedule_topk(a, sps.numpy(), max(cap, 0))
+        np.testing.assert_array_equal(lengths.cpu().numpy(), ref["lengths"])
+        assert int(B.item()) == ref["B"]
+        assert float(theta.item()) == ref["theta"]
+        assert int(b_opt.item()) == opt["B"]
+        st = spec.spec_device_status(ws)
+        assert st == (spec.SPEC_DEV_BAD_LENGTH if cap < 0 else 0)
+
+
 # ----------------------------------------------------------------------------- lossless grid
 
 def test_rejection_pipeline_per_uniform_agreement_v8(spec, ws):

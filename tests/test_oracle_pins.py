@@ -650,3 +650,36 @@ def test_topk_takes_the_k_largest_survivals_prefix_closed(orc, seed):
     same = orc.schedule_topk(a, sps, opt["B"])
     np.testing.assert_array_equal(same["lengths"], opt["lengths"])
     assert same["theta"] == opt["theta"]
+
+
+# ----------------------------------------------------------------------------- flattened batch
+
+def test_flat_layout_worked_example(orc):
+    """Packed rows of a variable-length verify batch (DSpark section 7), written out by hand for
+    lengths (2, 0, 3) with gamma = 3: request 0 owns rows 0-2, request 1 row 3, request 2 rows
+    4-7, and the last four of the 12 rows are past the batch."""
+    out = orc.flat_layout(np.array([2, 0, 3]), 3)
+    np.testing.assert_array_equal(out["offsets"], [0, 3, 4, 8])
+    np.testing.assert_array_equal(out["row_req"], [0, 0, 0, 1, 2, 2, 2, 2, -1, -1, -1, -1])
+    np.testing.assert_array_equal(out["row_pos"], [0, 1, 2, 0, 0, 1, 2, 3, -1, -1, -1, -1])
+
+
+def test_flat_layout_batch_is_the_schedulers_B(orc):
+    """The packed batch of the scheduler's lengths has exactly B = sum_r (1 + l_r) rows
+    (DSpark section 6), and packing then reading row offsets[r] + i returns position (r, i)."""
+    rng = np.random.default_rng(8)
+    R, gamma = 23, 6
+    a = np.sort(rng.uniform(0.0, 1.0, (R, gamma)), axis=1)[:, ::-1].astype(np.float32)
+    sps = np.linspace(1.0, 0.4, R * (gamma + 1) + 1)
+    sch = orc.schedule_prefix(a, sps)
+    lay = orc.flat_layout(sch["lengths"], gamma)
+    assert lay["offsets"][-1] == sch["B"]
+    padded = rng.integers(0, 1 << 30, (R, gamma + 1))
+    packed = np.full(R * (gamma + 1), -7)
+    for r in range(R):
+        for i in range(sch["lengths"][r] + 1):
+            packed[lay["offsets"][r] + i] = padded[r, i]
+    live = lay["row_req"] >= 0
+    assert live.sum() == sch["B"]
+    np.testing.assert_array_equal(packed[live], padded[lay["row_req"][live], lay["row_pos"][live]])
+    assert (packed[~live] == -7).all()
