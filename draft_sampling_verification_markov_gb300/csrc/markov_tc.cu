@@ -329,6 +329,12 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   return d;
 }
 
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -449,7 +455,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* a_full = acc_empty + KA;  // [2]: A of the pair's first / second row block
   uint64_t* a_empty = a_full + 2;
   uint64_t* drain = a_empty + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* scr_free = drain + 1;  // the first A gather is done with its scratch (B stage 1)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(scr_free + 1);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
   // gathered modes: T and U row indices of the pair's two row blocks, [block][row]
   int* row_t = reinterpret_cast<int*>(tail + 256);
@@ -484,6 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&a_full[1], kEpiWarps);
     mbar_init(a_empty, 1);
     mbar_init(drain, 1);
+    mbar_init(scr_free, kEpiWarps);
     *abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -519,6 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int ka = 0; ka < ka_n; ++ka) tma_prefetch_2d(&map_w2, ka * 64, pf * BN, pol_keep);
       if (u + kPrefetch < u_end && ++pf == n_nt) pf = 0;
       ok = mbar_wait(&b_empty[bs], bph ^ 1, abort, status);
+      if (ok && u == u_begin + 1) ok = mbar_wait(scr_free, 0, abort, status);
       if (ok && lane == 0 && !(P.stall && u == u_begin)) {
         mbar_arrive_expect_tx(&b_full[bs], ka_n * C::kBAtomBytes);
         for (int ka = 0; ka < ka_n; ++ka)
@@ -679,50 +688,111 @@ __global__ void __launch_bounds__(kThreads, 1)
           aeph ^= 1;
           if (!ok) break;
         }
+        const bool first_pair = cur_mp < 0;
         cur_mp = mp;
-        // gather A into tensor memory, one row block after the other: thread (q, h) owns row i
-        // and half h of its K; one load of the previous token, then all of its W1 chunks in
-        // flight, then tcgen05.st (a bad token is flagged afterwards)
+        // gather A into tensor memory: thread (q, h) owns row i of each block of the pair and
+        // half h of its K. The previous tokens first (a bad one is flagged and its row read as
+        // zeros), then every W1 chunk in flight at once, then tcgen05.st.
+        const int per = j.rank / 16;  // 16-byte chunks of a half row (<= 16)
+        int src_row[2] = {-1, -1};
         for (int sb = 0; sb < nb; ++sb) {
           const TileRow tr = tile_row(j, P.t, 2 * mp + sb, i);
-          int prev = 0;
-          if (tr.valid) {
-            if (j.map == MAP_FINAL) {
-              const int n = j.final_n[tr.r];
-              prev = n == 0 ? j.anchors[tr.r] : j.tokens[(size_t)tr.r * j.gamma + n - 1];
-            } else {
-              prev = tr.k == 1 ? j.anchors[tr.r] : j.tokens[(size_t)tr.r * j.gamma + tr.k - 2];
+          if (!tr.valid) continue;
+          int prev;
+          if (j.map == MAP_FINAL) {
+            const int n = j.final_n[tr.r];
+            prev = n == 0 ? j.anchors[tr.r] : j.tokens[(size_t)tr.r * j.gamma + n - 1];
+          } else {
+            prev = tr.k == 1 ? j.anchors[tr.r] : j.tokens[(size_t)tr.r * j.gamma + tr.k - 2];
+          }
+          if (prev < 0 || prev >= j.V) atomicOr(status, SPEC_DEV_BAD_TOKEN);
+          else src_row[sb] = prev;
+        }
+        const uint4* w1 = reinterpret_cast<const uint4*>(j.W1);
+        const int row_chunks = 2 * per;  // 16-byte chunks of a W1 row
+        if (first_pair) {
+          // The CTA's first pair reads the rows whole (eight lanes per 128-byte piece, so an
+          // instruction touches 4 lines rather than 32) and turns them into one row per lane
+          // through a 4 KB per-warp scratch in the second W2 stage, which is not loaded before
+          // the scratch is released. Piece p of a half row is chunks 8p..8p+7; chunk c of
+          // warp row rl sits at slot c ^ (rl & 7), so stores and loads are conflict-free.
+          static_assert(kEpiWarps * 4096 <= C::kBStageBytes && KB >= 2, "gather scratch");
+          const uint32_t scr = smem_u32(sB + C::kBStageBytes) + ew * 4096;
+          uint4 v[2][2][8];
+#pragma unroll
+          for (int sb = 0; sb < 2; ++sb)
+#pragma unroll
+            for (int p = 0; p < 2; ++p)
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                const int rl = 4 * k + (lane >> 3), c = 8 * p + (lane & 7);
+                const int row = __shfl_sync(0xffffffffu, src_row[sb], rl);
+                v[sb][p][k] = make_uint4(0, 0, 0, 0);
+                if (row >= 0 && c < per) v[sb][p][k] = __ldg(w1 + (size_t)row * row_chunks + h * per + c);
+              }
+#pragma unroll
+          for (int sb = 0; sb < 2; ++sb) {
+            if (sb >= nb) break;
+            const uint32_t a_addr = tmem + ((uint32_t)(q * 32) << 16) + C::kAccCols +
+                                    sb * C::kACols + h * (j.rank / 4);
+#pragma unroll
+            for (int p = 0; p < 2; ++p) {
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                const int rl = 4 * k + (lane >> 3);
+                sts128(scr + rl * 128 + (((lane & 7) ^ (rl & 7)) << 4), v[sb][p][k]);
+              }
+              __syncwarp();
+              uint32_t w[32];
+#pragma unroll
+              for (int c = 0; c < 8; ++c) {
+                const uint4 x = lds128(scr + lane * 128 + ((c ^ (lane & 7)) << 4));
+                w[4 * c] = x.x;
+                w[4 * c + 1] = x.y;
+                w[4 * c + 2] = x.z;
+                w[4 * c + 3] = x.w;
+              }
+              __syncwarp();
+              // chunk c of the half holds K elements 8c..8c+7 = columns 4c..4c+3 of the half
+              if (8 * p < per) tmem_st16(a_addr + 32 * p, w);
+              if (8 * p + 4 < per) tmem_st16(a_addr + 32 * p + 16, w + 16);
             }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&a_full[sb]);
           }
-          const bool bad = tr.valid && (prev < 0 || prev >= j.V);
-          const int per = j.rank / 16;  // 16-byte chunks of this thread's half row (<= 16)
-          const uint4* src = reinterpret_cast<const uint4*>(
-                                 reinterpret_cast<const unsigned short*>(j.W1) +
-                                 (size_t)(bad ? 0 : prev) * j.rank) + h * per;
-          uint32_t w[64];
-#pragma unroll
-          for (int it = 0; it < 16; ++it) {
-            const uint4 v = (tr.valid && it < per) ? __ldg(src + it) : make_uint4(0, 0, 0, 0);
-            w[4 * it] = v.x;
-            w[4 * it + 1] = v.y;
-            w[4 * it + 2] = v.z;
-            w[4 * it + 3] = v.w;
-          }
-          // chunk c of the half holds K elements 8c..8c+7 = columns 4c..4c+3 of the half
-          const uint32_t a_addr = tmem + ((uint32_t)(q * 32) << 16) + C::kAccCols +
-                                  sb * C::kACols + h * (j.rank / 4);
-#pragma unroll
-          for (int b = 0; b < 4; ++b)
-            if (4 * b < per) tmem_st16(a_addr + 16 * b, w + 16 * b);
-          tmem_wait_st();
-          if (bad) atomicOr(status, SPEC_DEV_BAD_TOKEN);
-          tc_fence_before();
+          // the scratch's generic-proxy accesses are ordered before the W2 copy into it
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           __syncwarp();
-          if (lane == 0) mbar_arrive(&a_full[sb]);
-          if constexpr (kPair) {
-            if (sb == 0) row_norms_tc<MODE>(j, tr, dn0, tn0, rs0);
-            else row_norms_tc<MODE>(j, tr, dn1, tn1, rs1);
+          if (lane == 0) mbar_arrive(scr_free);
+        } else {
+          for (int sb = 0; sb < nb; ++sb) {
+            uint32_t w[64];
+#pragma unroll
+            for (int it = 0; it < 16; ++it) {
+              const uint4 x = (src_row[sb] >= 0 && it < per)
+                                  ? __ldg(w1 + (size_t)src_row[sb] * row_chunks + h * per + it)
+                                  : make_uint4(0, 0, 0, 0);
+              w[4 * it] = x.x;
+              w[4 * it + 1] = x.y;
+              w[4 * it + 2] = x.z;
+              w[4 * it + 3] = x.w;
+            }
+            const uint32_t a_addr = tmem + ((uint32_t)(q * 32) << 16) + C::kAccCols +
+                                    sb * C::kACols + h * (j.rank / 4);
+#pragma unroll
+            for (int b = 0; b < 4; ++b)
+              if (4 * b < per) tmem_st16(a_addr + 16 * b, w + 16 * b);
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&a_full[sb]);
           }
+        }
+        if constexpr (kPair) {
+          row_norms_tc<MODE>(j, tile_row(j, P.t, 2 * mp, i), dn0, tn0, rs0);
+          if (nb > 1) row_norms_tc<MODE>(j, tile_row(j, P.t, 2 * mp + 1, i), dn1, tn1, rs1);
         }
       }
       const int col0 = h * kHalf;  // first tile column of this warp
