@@ -3,27 +3,30 @@
 // DSpark", section 4 "Markov Head": B(x_{k-1}, .) = W1[x_{k-1}] W2 added to the base logits,
 // section 3 softmax; section 5 TV label; the residual of rejection sampling).
 //
-// One tile = 128 rows (requests, TMEM lanes) x N vocabulary columns (N = 128 for softmax
-// partials, 64 for the TV / residual passes), K = rank (<= 256, a multiple of 64). A work unit
+// One tile = 128 rows (requests, TMEM lanes) x N vocabulary columns (N = 128 for the softmax
+// partials and the residual, 64 for the TV pass), K = rank (<= 256, a multiple of 64). A work unit
 // is one W2 column tile against a pair of row blocks: the B tile is loaded once and feeds both
 // blocks' MMA groups, which halves the W2 bytes each SM pulls into shared memory.
 //   A  [128 x rank] bf16 per row block: the W1 rows of each row's previous token, gathered by
-//      the epilogue warps and stored into tensor memory with tcgen05.st (lane = row, two bf16
-//      of K per 32-bit column); both blocks of the current pair stay resident.
+//      the epilogue warps (the first pair of a CTA through a shared-memory transpose, so that
+//      the rows are read whole) and stored into tensor memory with tcgen05.st (lane = row, two
+//      bf16 of K per 32-bit column); both blocks of the current pair stay resident.
 //   B  [N x rank] bf16: W2 rows (W2 stored [V, rank], K-major) by TMA, one whole tile per
 //      pipeline stage, kept in L2 with an evict-last policy and prefetched two units ahead.
 //   D  [128 x N] fp32 in tensor memory (2 stages at N = 128, 4 at N = 64), read back with
 //      tcgen05.ld.
 //   U / T tiles: the base-logit (and target) rows of each (unit, row block), by TMA with an
 //      evict-first policy (read once), 64-column boxes in the 128-byte-swizzled layout; rows
-//      that are not equally spaced (the final rows of rejection verification) come four at a
-//      time with tile::gather4 into the same layout.
+//      that are not equally spaced (the final rows of rejection verification) are copied by
+//      the producer warp with 16-byte cp.async into the same layout, each row's piece read
+//      whole by neighbouring lanes.
 // The W1 rows of the A gather are prefetched into L2 by the kernel that drew the tokens, so
 // the logit stream starts at once.
-// Warp roles (352 threads, one CTA per SM, persistent over a contiguous range of units):
+// Warp roles (384 threads, one CTA per SM, persistent over a contiguous range of units):
 //   warp 0  W2 (B operand) TMA producer;  warp 1  TMEM allocator + single-thread MMA issuer;
-//   warp 2  U / T tile producer;  warps 3..10  epilogue: warp w reads TMEM lanes 32*(w%4)..
-//   and column half (w-3)/4 of the tile.
+//   warp 2  U / T tile producer (T rows only when rows are gathered);  warps 3..10  epilogue:
+//   warp w reads TMEM lanes 32*(w%4).. and column half (w-3)/4 of the tile;  warp 11  the
+//   gathered U rows (idle otherwise).
 // Epilogues (per row, per N/2-column half tile, one partial each):
 //   MODE_STATS  z = (U + bias) * scale -> (max z, sum exp(z - max), first argmax);
 //   MODE_TV     sum min(p_d, p_t);    MODE_RESID  sum max(0, p_t - p_d) (p_t on bonus rows).
@@ -42,23 +45,27 @@ namespace tc {
 constexpr int kBM = 128;                            // rows per tile (one MMA, 128 TMEM lanes)
 constexpr int kEpiWarps = 8;
 constexpr int kFirstEpi = 3;                       // warps 0..2: B producer, MMA, U/T producer
-constexpr int kThreads = (kFirstEpi + kEpiWarps) * 32;
+constexpr int kRowWarp = kFirstEpi + kEpiWarps;     // second producer of gathered rows
+constexpr int kThreads = (kRowWarp + 1) * 32;
 constexpr long long kSpinCycles = 4000000000LL;  // ~2 s at the maximum SM clock
 constexpr uint32_t kBoxBytes = kBM * 128;         // one TMA box: 128 rows x 64 columns (bf16)
 
 // Per pass mode. Shared memory (A lives in tensor memory):
-//   MODE_STATS: N = 128: B 2 x 64 KB + U 3 x 32 KB          = 224 KB; TMEM 2 x 128 + 2 x 128 cols
-//   MODE_TV / MODE_RESID: N = 64: B 2 x 32 KB + (U + T) 4 x 2 x 16 KB = 192 KB; TMEM 4 x 64 + 2 x 128
+//   MODE_STATS: N = 128: B 2 x 64 KB + U 3 x 32 KB             = 224 KB; TMEM 2 x 128 + 2 x 128 cols
+//   MODE_TV:    N = 64:  B 2 x 32 KB + (U + T) 4 x 2 x 16 KB   = 192 KB; TMEM 4 x 64 + 2 x 128
+//   MODE_RESID: N = 128: B 1 x 64 KB + (U + T) 2 x 2 x 32 KB   = 192 KB; TMEM 2 x 128 + 2 x 128
+// The residual pass gathers its rows: a row piece of 256 bytes (N = 128) costs about as much
+// HBM time as one of 128 bytes, so it takes the wide tile at the price of a single W2 stage.
 template <int MODE>
 struct Cfg {
-  static constexpr int kBN = MODE == MODE_STATS ? 128 : 64;  // vocabulary columns per tile
+  static constexpr int kBN = MODE == MODE_TV ? 64 : 128;     // vocabulary columns per tile
   static constexpr int kBoxes = kBN / 64;                     // 64-column boxes per logit tile
   static constexpr uint32_t kBAtomBytes = kBN * 128;          // kBN W2 rows x 64 K
   static constexpr uint32_t kBStageBytes = 4 * kBAtomBytes;   // K <= 256
-  static constexpr int kBStages = 2;
+  static constexpr int kBStages = MODE == MODE_RESID ? 1 : 2;
   static constexpr uint32_t kTileBytes = kBoxes * kBoxBytes;
-  static constexpr int kUStages = MODE == MODE_STATS ? 3 : 4;
-  static constexpr int kAccStages = MODE == MODE_STATS ? 2 : 4;  // accumulator stages in TMEM
+  static constexpr int kUStages = MODE == MODE_STATS ? 3 : (MODE == MODE_RESID ? 2 : 4);
+  static constexpr int kAccStages = kBN == 128 ? 2 : 4;       // accumulator stages in TMEM
   static constexpr int kAccCols = kAccStages * kBN;
   static constexpr int kACols = 128;                          // one A block (rank <= 256)
   static constexpr int kTmemCols = 512;                       // accumulators + two A blocks
@@ -460,6 +467,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
   // gathered modes: T and U row indices of the pair's two row blocks, [block][row]
   int* row_t = reinterpret_cast<int*>(tail + 256);
+  // scratch of the CTA's first A gather (4 KB per epilogue warp): the second W2 stage, or with
+  // a single W2 stage the second T stage; whoever fills it first waits for scr_free
+  constexpr bool kScrInB = KB >= 2;
+  static_assert(kScrInB ? kEpiWarps * 4096 <= C::kBStageBytes
+                        : (kPair && KU >= 2 && kEpiWarps * 4096 <= C::kTileBytes),
+                "gather scratch");
+  unsigned char* const scr_base = kScrInB ? sB + C::kBStageBytes : sT + C::kTileBytes;
   int* row_u = row_t + 2 * kBM;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -480,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&b_empty[s], 1);
     }
     for (int s = 0; s < KU; ++s) {
-      mbar_init(&u_full[s], GATHER ? 32 : 1);  // gathered rows: one arrival per producer lane
+      mbar_init(&u_full[s], GATHER ? 64 : 1);  // gathered rows: one arrival per producer lane
       mbar_init(&u_empty[s], kEpiWarps);
     }
     for (int s = 0; s < KA; ++s) {
@@ -527,7 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int ka = 0; ka < ka_n; ++ka) tma_prefetch_2d(&map_w2, ka * 64, pf * BN, pol_keep);
       if (u + kPrefetch < u_end && ++pf == n_nt) pf = 0;
       ok = mbar_wait(&b_empty[bs], bph ^ 1, abort, status);
-      if (ok && u == u_begin + 1) ok = mbar_wait(scr_free, 0, abort, status);
+      if (ok && kScrInB && u == u_begin + 1) ok = mbar_wait(scr_free, 0, abort, status);
       if (ok && lane == 0 && !(P.stall && u == u_begin)) {
         mbar_arrive_expect_tx(&b_full[bs], ka_n * C::kBAtomBytes);
         for (int ka = 0; ka < ka_n; ++ka)
@@ -539,31 +553,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     // drain: every issued copy lands before the CTA moves on
     if (lane == 0)
       for (int s = 0; s < KB; ++s) mbar_drain(&b_full[s], (s < bs) ? bph : (bph ^ 1));
-  } else if (warp == 2) {
+  } else if (warp == 2 || (GATHER && warp == kRowWarp)) {
     // ---------------------------------------------------------------- U / T producer
     const uint64_t pol_stream = policy_evict_first();
     int us = 0;
     uint32_t uph = 0;
     bool ok = true;
     int mp = mp_first, nt = nt_first, rows_mp = -1;
+    const bool tside = warp == 2;
     // gathered row indices of the pair's two row blocks, loaded once per pair into a table
     // (rows past R and the U rows of bonus rows point at row 0 and are ignored)
     for (long long u = u_begin; u < u_end && ok; ++u) {
       const int n0 = nt * BN;
       const int nb = 2 * mp + 1 < n_mt ? 2 : 1;
       if constexpr (GATHER) {
+        // warp 2 gathers the T rows and the second producer warp the U rows; each builds its
+        // own table, with every load of a lane in flight at once
         if (mp != rows_mp) {
           rows_mp = mp;
-          for (int q = lane; q < 2 * kBM; q += 32) {
-            const int r = 2 * mp * kBM + q;  // q / kBM is the block of the pair
-            int tr = 0, ur = 0;
-            if (r < j.R && q / kBM < nb) {
-              const int n = j.final_n[r];
-              tr = (int)target_row(j, r, n);
-              if (j.final_kind[r]) ur = r * j.gamma + n;
-            }
-            row_t[q] = tr;
-            row_u[q] = ur;
+          constexpr int kPer = 2 * kBM / 32;
+          int nn[kPer], kind[kPer];
+#pragma unroll
+          for (int t = 0; t < kPer; ++t) {
+            const int q = lane + 32 * t, r = 2 * mp * kBM + q;  // q / kBM: block of the pair
+            const bool in = r < j.R && q / kBM < nb;
+            nn[t] = in ? j.final_n[r] : -1;
+            kind[t] = in && !tside ? j.final_kind[r] : 0;
+          }
+#pragma unroll
+          for (int t = 0; t < kPer; ++t) {
+            const int q = lane + 32 * t, r = 2 * mp * kBM + q;
+            if (tside) row_t[q] = nn[t] >= 0 ? (int)target_row(j, r, nn[t]) : 0;
+            else row_u[q] = kind[t] ? r * j.gamma + nn[t] : 0;
           }
           __syncwarp();
         }
@@ -571,6 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int sb = 0; sb < nb && ok; ++sb) {
         const int mt = 2 * mp + sb;
         ok = mbar_wait(&u_empty[us], uph ^ 1, abort, status);
+        if (ok && !kScrInB && us == 1 && uph == 0) ok = mbar_wait(scr_free, 0, abort, status);
         if (!ok) break;
         unsigned char* du = sU + us * C::kTileBytes;
         unsigned char* dt = sT + us * C::kTileBytes;
@@ -588,23 +610,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         } else {
-          // final rows of rejection verification: per instruction, 8 lanes copy one row's 128
-          // bytes (16 each) of T and of U, so a warp moves 4 whole rows; pieces land in the
-          // 128-byte swizzled layout, and columns past V are zero-filled without a read
-          static_assert(C::kBoxes == 1, "gathered tiles are one box wide");
+          // final rows of rejection verification: per instruction, 8 lanes per 64-column box
+          // copy one row's piece (16 bytes each) of this warp's tensor (T or U), so a warp
+          // moves 4 / kBoxes whole row pieces; pieces land in the 128-byte swizzled box layout,
+          // and columns past V are zero-filled without a read
+          constexpr int kLanesPerRow = 8 * C::kBoxes, kRowsPerInstr = 32 / kLanesPerRow;
           const unsigned short* Tb = static_cast<const unsigned short*>(j.T);
           const unsigned short* Ub = static_cast<const unsigned short*>(j.U);
           const uint32_t st_base = smem_u32(dt), su_base = smem_u32(du);
-          const int c = lane & 7;
+          const int c = lane % kLanesPerRow;          // 16-byte chunk of the row piece
+          const int bx = c >> 3, cc = c & 7;          // box and chunk within the box
           const uint32_t nb16 = n0 + 8 * c < j.V ? 16u : 0u;
 #pragma unroll 4
-          for (int k = 0; k < kBM / 4; ++k) {
-            const int i = 4 * k + (lane >> 3);  // row within the block
-            const long long tro = (long long)row_t[sb * kBM + i] * j.V + n0 + 8 * c;
-            const long long uro = (long long)row_u[sb * kBM + i] * j.V + n0 + 8 * c;
-            const uint32_t so = i * 128 + ((c ^ (i & 7)) << 4);
-            cp_async16(st_base + so, Tb + (nb16 ? tro : 0), nb16);
-            cp_async16(su_base + so, Ub + (nb16 ? uro : 0), nb16);
+          for (int k = 0; k < kBM / kRowsPerInstr; ++k) {
+            const int i = kRowsPerInstr * k + lane / kLanesPerRow;  // row within the block
+            const int* tab = tside ? row_t : row_u;
+            const long long ro = (long long)tab[sb * kBM + i] * j.V + n0 + 8 * c;
+            const uint32_t so = bx * kBoxBytes + i * 128 + ((cc ^ (i & 7)) << 4);
+            cp_async16((tside ? st_base : su_base) + so, (tside ? Tb : Ub) + (nb16 ? ro : 0),
+                       nb16);
           }
           cp_async_arrive(&u_full[us]);
         }
@@ -713,11 +737,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (first_pair) {
           // The CTA's first pair reads the rows whole (eight lanes per 128-byte piece, so an
           // instruction touches 4 lines rather than 32) and turns them into one row per lane
-          // through a 4 KB per-warp scratch in the second W2 stage, which is not loaded before
-          // the scratch is released. Piece p of a half row is chunks 8p..8p+7; chunk c of
-          // warp row rl sits at slot c ^ (rl & 7), so stores and loads are conflict-free.
-          static_assert(kEpiWarps * 4096 <= C::kBStageBytes && KB >= 2, "gather scratch");
-          const uint32_t scr = smem_u32(sB + C::kBStageBytes) + ew * 4096;
+          // through the 4 KB per-warp scratch, which is not refilled before it is released.
+          // Piece p of a half row is chunks 8p..8p+7; chunk c of warp row rl sits at slot
+          // c ^ (rl & 7), so stores and loads are conflict-free.
+          const uint32_t scr = smem_u32(scr_base) + ew * 4096;
           uint4 v[2][2][8];
 #pragma unroll
           for (int sb = 0; sb < 2; ++sb)
@@ -926,7 +949,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int e = 0; e < 8; ++e) {
                 const float pt = prob_of(tv[e] * j.scale, tn);
                 float pd = prob_of((uv[e] + __uint_as_float(braw[c * 8 + e])) * j.scale, dn);
-                if (!((mlo >> (c * 8 + e)) & 1u)) pd = 0.0f;  // disallowed draft token
+                const int be = c * 8 + e;  // column of the warp's half tile
+                if (!(((be < 32 ? mlo : mhi) >> (be & 31)) & 1u)) pd = 0.0f;  // disallowed
                 float x;
                 if constexpr (MODE == MODE_TV) x = fminf(pt, pd);
                 else x = fmaxf(pt - (resid ? pd : 0.0f), 0.0f);  // bonus rows: p_t
@@ -1008,7 +1032,10 @@ cudaError_t launch_t(const TcParams& p, const CUtensorMap& w2, const CUtensorMap
 
 }  // namespace tc
 
-int markov_tc_seg(int mode) { return mode == MODE_STATS ? 64 : 32; }
+int markov_tc_seg(int mode) {
+  return mode == MODE_STATS ? tc::Cfg<MODE_STATS>::kSeg
+                            : (mode == MODE_TV ? tc::Cfg<MODE_TV>::kSeg : tc::Cfg<MODE_RESID>::kSeg);
+}
 
 bool markov_tc_supported(int udt, int wdt, int rank, int V, const void* U, const void* T,
                          const void* W1, const void* W2) {
@@ -1031,7 +1058,8 @@ cudaError_t launch_markov_tc(const RowJob& j, float* pm, float* ps, int* pi, boo
   using namespace tc;
   TraceScope ts(SPEC_KCLASS_MARKOV, s);
   const bool pair = j.mode != MODE_STATS;
-  const int BN = pair ? Cfg<MODE_TV>::kBN : Cfg<MODE_STATS>::kBN;
+  const int BN = j.mode == MODE_STATS ? Cfg<MODE_STATS>::kBN
+                 : (j.mode == MODE_TV ? Cfg<MODE_TV>::kBN : Cfg<MODE_RESID>::kBN);
   TcParams p;
   p.j = j;
   p.pm = pm;
