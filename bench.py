@@ -43,6 +43,7 @@ def parse_args():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-other-configs", action="store_true")
     return p.parse_args()
 
 
@@ -245,6 +246,140 @@ def run_reference(args):
 
 # ----------------------------------------------------------------------------- our arm
 
+# ----------------------------------------------------------------------------- other configs
+
+def graph_ms(run, stream, reps=5, warm=2):
+    """Milliseconds per replay of `run` captured as one CUDA graph on `stream`."""
+    import torch
+    with torch.cuda.stream(stream):
+        run()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        run()
+    with torch.cuda.stream(stream):
+        for _ in range(warm):
+            g.replay()
+    stream.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(reps):
+            g.replay()
+    b.record(stream)
+    b.synchronize()
+    return a.elapsed_time(b) / reps
+
+
+def other_configs(spec, workloads, dev, peak):
+    """The other rows of the path on their own workloads, each step one CUDA graph with inputs
+    resident: the fp32 greedy toy, MTP-1 greedy verify, confidence + scheduling, and one
+    iteration of the 20-iteration loop. Bytes are the algorithmic bytes the step must touch."""
+    import torch
+    from draft_sampling_verification_markov_gb300.loop import SpecLoop
+    out = {}
+    stream = torch.cuda.Stream(device=dev)
+
+    def entry(name, ms, rows, nbytes, extra=None):
+        e = {"ms_per_step": ms, "rows_per_s": rows / (ms / 1e3), "rows_per_step": rows,
+             "algorithmic_bytes": nbytes, "hbm_gbs": nbytes / (ms / 1e3) / 1e9,
+             "hbm_frac": nbytes / (ms / 1e3) / 1e9 / peak}
+        e.update(extra or {})
+        out[name] = e
+
+    # fp32 greedy toy: Markov argmax (CUDA-core canonical chain) + greedy verify; latency-bound
+    wl = workloads.greedy_toy("cuda")
+    ws = spec.Workspace(device=dev)
+    R, g, V = wl.R, wl.gamma, wl.V
+    toks = torch.empty(R, g, dtype=torch.int32, device=dev)
+    res = [torch.empty(R, dtype=torch.int32, device=dev),
+           torch.empty(R, g + 1, dtype=torch.int32, device=dev),
+           torch.empty(R, dtype=torch.int32, device=dev)]
+    for op in range(6):
+        ws.for_op(op, R, g, V, wl.rank, stream)
+
+    def toy():
+        spec.spec_markov_propose(wl.U, wl.W1, wl.W2, wl.anchors, None, 0.0, draft_tokens=toks,
+                                 want_stats=False, workspace=ws, stream=stream)
+        spec.spec_verify_greedy(wl.target, toks, accept_len=res[0], out_tokens=res[1],
+                                next_anchor=res[2], workspace=ws, stream=stream)
+    ms = graph_ms(toy, stream)
+    nbytes = (wl.U.numel() + wl.target.numel() + wl.W2.numel()) * 4
+    entry("greedy_toy_fp32_R4_g4_V32000", ms, R * (2 * g + 1), nbytes,
+          {"bound": "latency", "us_per_step": ms * 1e3})
+    del wl
+
+    # MTP-1 greedy: rank-0 argmax proposal + greedy verify
+    wl = workloads.mtp_greedy("cuda")
+    R, g, V = wl.R, wl.gamma, wl.V
+    toks = torch.empty(R, g, dtype=torch.int32, device=dev)
+    res = [torch.empty(R, dtype=torch.int32, device=dev),
+           torch.empty(R, g + 1, dtype=torch.int32, device=dev),
+           torch.empty(R, dtype=torch.int32, device=dev)]
+    for op in range(6):
+        ws.for_op(op, R, g, V, 0, stream)
+
+    def mtp():
+        spec.spec_markov_propose(wl.U, None, None, None, None, 0.0, draft_tokens=toks,
+                                 want_stats=False, workspace=ws, stream=stream)
+        spec.spec_verify_greedy(wl.target, toks, accept_len=res[0], out_tokens=res[1],
+                                next_anchor=res[2], workspace=ws, stream=stream)
+    ms = graph_ms(mtp, stream)
+    entry("mtp_greedy_R64_g3_V129280", ms, R * (2 * g + 1),
+          (wl.U.numel() + wl.target.numel()) * 2,
+          {"mean_accept_len": float(res[0].float().mean())})
+    del wl
+
+    # confidence + scheduling: proposal, target normalisers, TV labels + survival, scheduler
+    wl = workloads.confidence_scheduling("cuda")
+    R, g, V = wl.R, wl.gamma, wl.V
+    toks = torch.empty(R, g, dtype=torch.int32, device=dev)
+    logp = torch.empty(R, g, dtype=torch.float32, device=dev)
+    dst = torch.empty(R, g, 2, dtype=torch.float32, device=dev)
+    tst = torch.empty(R * (g + 1), 2, dtype=torch.float32, device=dev)
+    conf = torch.empty(R, g, dtype=torch.float32, device=dev)
+    surv = torch.empty(R, g, dtype=torch.float32, device=dev)
+    lens = torch.empty(R, dtype=torch.int32, device=dev)
+    B = torch.empty(1, dtype=torch.int32, device=dev)
+    th = torch.empty(1, dtype=torch.float64, device=dev)
+    sps = wl.sps.to(dev)
+    for op in range(6):
+        ws.for_op(op, R, g, V, wl.rank, stream)
+
+    def conf_sched():
+        spec.spec_markov_propose(wl.U, wl.W1, wl.W2, wl.anchors, wl.u_draft, wl.temperature,
+                                 draft_tokens=toks, draft_logp=logp, draft_stats=dst,
+                                 workspace=ws, stream=stream)
+        spec.spec_target_stats(wl.target, wl.temperature, stats=tst, workspace=ws,
+                               stream=stream)
+        spec.spec_tv_confidence(wl.U, wl.target, wl.W1, wl.W2, wl.anchors, toks,
+                                wl.temperature, draft_stats=dst, target_stats=tst, conf=conf,
+                                survival=surv, workspace=ws, stream=stream)
+        spec.spec_schedule_prefix(surv, sps, lengths=lens, B_out=B, theta_out=th,
+                                  workspace=ws, stream=stream)
+    ms = graph_ms(conf_sched, stream, reps=3)
+    entry("confidence_scheduling_R512_g16_V129280", ms, R * (2 * g + 1),
+          (wl.U.numel() + wl.target.numel() + wl.W2.numel()) * 2,
+          {"scheduled_B": int(B.item()), "note": "U and target counted once; the TV pass "
+           "reads them a second time"})
+    del wl, toks, logp, dst, tst, conf, surv
+
+    # the 20-iteration loop: two chained iterations per graph, time per iteration
+    wl = workloads.full_loop("cuda", iterations=2)
+    lp = SpecLoop(wl.U, wl.target, wl.W1, wl.W2, wl.anchors, wl.u_draft, wl.u_accept,
+                  wl.u_resid, wl.temperature, wl.sps.to(dev), iterations=2)
+    ms = graph_ms(lambda: lp.run(), stream, reps=3) / 2
+    R, g = wl.R, wl.gamma
+    entry("full_loop_R1024_g16_V129280_per_iteration", ms, R * (2 * g + 1),
+          (wl.U.numel() + wl.target.numel() + wl.W2.numel()) * 2,
+          {"mean_emitted_per_request": float(lp.emitted_tokens().float().mean())})
+    assert ws.status() == 0 and lp.ws.status() == 0, "device status word set"
+    del wl, lp
+    torch.cuda.empty_cache()
+    return out
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
@@ -394,6 +529,18 @@ def main():
                 "step_hbm_frac_of_8tbs_nominal":
                     algorithmic_bytes_per_step() * args.steps / (ms / 1e3) / 1e9 / 8000.0,
                 "class_ms_per_step": {names[k]: totals[k][0] / args.steps for k in totals}}
+    # the W2 projection of the Markov class on the tensor pipe: 2 * R * rank * V flops per
+    # launch (gamma proposal positions + the residual pass), against the bf16 dense peak
+    mk = totals[0]
+    if mk[1] > 0:
+        flops = 2.0 * R * W["rank"] * V * mk[1]
+        # timed inside a long step: the sustained figure
+        bf16 = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops", 1700.0)))
+        tf = flops / (mk[0] / 1e3) / 1e12
+        roofline["w2_projection"] = {"bound": "tensor", "achieved": tf, "peak": bf16,
+                                     "unit": "TFLOP/s", "frac": tf / bf16,
+                                     "note": "flops over the Markov class's launch time; the "
+                                             "class is not tensor-bound"}
 
     # end to end through the C ABI from pinned host buffers (weights stay resident): every step
     # copies its inputs host -> device and reads its outputs back. Two device input buffers let
@@ -471,6 +618,9 @@ def main():
                          f"{reps} times, of the same seeded bytes, {dt:.1f} s"}
 
     clocks = sampler.summary(w0, w1)
+    others = None
+    if rank == 0 and world == 1 and not args.no_other_configs:
+        others = other_configs(spec, workloads, dev, peak)
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
@@ -485,7 +635,8 @@ def main():
                 "gpu_launches": int(launches), "clocks": clocks,
                 "tokens_per_s": float(n_acc.sum().item() + R) * args.steps * world / (ms / 1e3),
                 "mean_accept_len": float(n_acc.float().mean().item()),
-                "mean_emitted_per_request": float(n_acc.float().mean().item()) + 1.0}
+                "mean_emitted_per_request": float(n_acc.float().mean().item()) + 1.0,
+                "other_configs": others}
         print(json.dumps(line), flush=True)
     if pg:
         pg.destroy_process_group()
