@@ -90,7 +90,7 @@ size_t partial_entries(int op, int R, int gamma, int V, int rank) {
   const size_t tgt = tr * stream_nseg(V);
   size_t e = 0;
   switch (op) {
-    case SPEC_OP_PROPOSE: e = (size_t)R * seg_draft; break;
+    case SPEC_OP_PROPOSE: e = (size_t)R * (rank > 0 ? 1 : gamma) * seg_draft; break;
     case SPEC_OP_VERIFY_GREEDY: e = tr; break;
     case SPEC_OP_TARGET_STATS: e = tgt; break;
     case SPEC_OP_VERIFY_REJECTION: e = tgt > (size_t)R * seg_draft ? tgt : (size_t)R * seg_draft; break;
@@ -328,6 +328,19 @@ static int markov_propose_impl(const void* U, int u_dtype, const void* W1, const
   o.greedy = greedy;
   const int wdt = rank > 0 ? w_dtype : u_dtype;
   const bool vec = vec_ok(U, nullptr, u_dtype, V);
+  if (rank == 0) {
+    // no Markov head: the positions do not depend on one another, so one streaming pass and
+    // one select cover all R * gamma rows (row m = r * gamma + k - 1, uniform u_draft[m])
+    j.rows = R * gamma;
+    j.map = MAP_ALL_POS;
+    o.uni_stride = 1;
+    o.uni_offset = 0;
+    const int nseg = stream_nseg(V);
+    launch_stream_partials(j, u_dtype, kStreamSeg, nseg, vec, true, greedy, w.pm, w.ps, w.pi,
+                           grid_for((long long)j.rows * nseg, 1), s);
+    launch_select(j, u_dtype, wdt, kStreamSeg, nseg, w.pm, w.ps, greedy ? w.pi : nullptr, o, s);
+    return finish();
+  }
   for (int k = 1; k <= gamma; ++k) {
     j.k = k;
     o.uni_offset = k - 1;

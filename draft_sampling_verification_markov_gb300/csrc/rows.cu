@@ -23,17 +23,60 @@ namespace spec {
 
 // ------------------------------------------------------------------------------ logits
 
-// Draft logit z_d(v) of a row (DSpark sections 3-4): (U + W1[prev] . W2[v]) * scale, the bias
-// in the canonical fp32 chain acc = fma(W1[prev][i], W2[v][i], acc), i ascending.
-template <int UDT, int WDT>
-__device__ __forceinline__ float draft_logit(const RowJob& j, const RowInfo& ri, int v) {
-  if (!draft_allowed(j, ri.r, v)) return -INFINITY;
+// 8 consecutive weights from a 16-byte aligned address, as fp32.
+template <int WDT>
+__device__ __forceinline__ void ld_w8(const void* p, size_t i, float* x) {
+  if constexpr (WDT == SPEC_BF16) {
+    const uint4 q = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const unsigned short*>(p) + i));
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      x[2 * t] = __uint_as_float(w[t] << 16);
+      x[2 * t + 1] = __uint_as_float(w[t] & 0xffff0000u);
+    }
+  } else {
+    const float4* f = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(p) + i);
+    const float4 a = __ldg(f), b = __ldg(f + 1);
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+  }
+}
+
+// Markov bias W1[prev] . W2[v] in the canonical fp32 chain acc = fma(W1[prev][i], W2[v][i], acc),
+// i ascending. With 16-byte aligned rows the weights come 8 at a time, 64 in flight, and the
+// chain is unchanged, so the result is bit-identical to the element-by-element loop.
+template <int WDT>
+__device__ __forceinline__ float markov_bias(const RowJob& j, int prev, int v) {
   float acc = 0.0f;
-  if (j.rank > 0) {
-    const size_t a = (size_t)ri.prev * j.rank, b = (size_t)v * j.rank;
+  const size_t a = (size_t)prev * j.rank, b = (size_t)v * j.rank;
+  const bool vec = (j.rank & 7) == 0 &&
+                   ((reinterpret_cast<uintptr_t>(j.W1) | reinterpret_cast<uintptr_t>(j.W2)) & 15) == 0;
+  if (vec) {
+    for (int i0 = 0; i0 < j.rank; i0 += 64) {
+      float xa[64], xb[64];
+#pragma unroll
+      for (int t = 0; t < 8; ++t)
+        if (i0 + 8 * t < j.rank) {
+          ld_w8<WDT>(j.W1, a + i0 + 8 * t, xa + 8 * t);
+          ld_w8<WDT>(j.W2, b + i0 + 8 * t, xb + 8 * t);
+        }
+#pragma unroll
+      for (int t = 0; t < 64; ++t)
+        if (i0 + t < j.rank) acc = __fmaf_rn(xa[t], xb[t], acc);
+    }
+  } else {
     for (int i = 0; i < j.rank; ++i)
       acc = __fmaf_rn(ld_elem<WDT>(j.W1, a + i), ld_elem<WDT>(j.W2, b + i), acc);
   }
+  return acc;
+}
+
+// Draft logit z_d(v) of a row (DSpark sections 3-4): (U + W1[prev] . W2[v]) * scale, the bias
+// in the canonical fp32 chain.
+template <int UDT, int WDT>
+__device__ __forceinline__ float draft_logit(const RowJob& j, const RowInfo& ri, int v) {
+  if (!draft_allowed(j, ri.r, v)) return -INFINITY;
+  const float acc = j.rank > 0 ? markov_bias<WDT>(j, ri.prev, v) : 0.0f;
   const float s = __fadd_rn(ld_elem<UDT>(j.U, (size_t)ri.urow * j.V + v), acc);
   return __fmul_rn(s, j.scale);
 }
@@ -329,6 +372,104 @@ __global__ void __launch_bounds__(kRowThreads, 2) row_stats_kernel(RowJob j, boo
 }
 
 // ------------------------------------------------------------------------------ generic Markov producer
+
+// Softmax partials of Markov rows on CUDA cores with the W2 column tile staged once per block:
+// a block takes a 64-column segment, copies its W2 rows into shared memory (coalesced, converted
+// to fp32, rows padded by 16 bytes so that a row per thread reads without bank conflicts), then
+// covers the rows four at a time: thread (row slot t / 64, column t % 64) runs the canonical fp32
+// chain against the shared tile. The same arithmetic as draft_logit, so the partials are
+// identical; only the memory traffic changes (each W2 row is read once per segment, not once per
+// row). Needs rank <= 256, rank % 8 == 0 and 16-byte aligned weights.
+constexpr int kTileCols = 64;
+template <int UDT, int WDT, bool ARGMAX>
+__global__ void __launch_bounds__(256) markov_ffma_tile(RowJob j, int nseg, float* pm, float* ps,
+                                                        int* pi) {
+  extern __shared__ __align__(16) float w2s[];  // [kTileCols][rank + 4]
+  __shared__ __align__(16) float w1s[4][256];    // W1 rows of the four rows in flight
+  __shared__ StatsAcc half[4][2];
+  const int pitch = j.rank + 4;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int slot = threadIdx.x >> 6, col = threadIdx.x & 63;
+  const int k8 = j.rank / 8;  // 8-weight chunks per row
+  for (int sg = blockIdx.x; sg < nseg; sg += gridDim.x) {
+    const int v0 = sg * kTileCols;
+    __syncthreads();  // the previous segment's tile is no longer read
+    {
+      // every chunk of this thread in flight before the first store
+      constexpr int kIt = kTileCols * 32 / 256;  // chunks per thread at rank 256
+      float x[kIt][8];
+#pragma unroll
+      for (int it = 0; it < kIt; ++it) {
+        const int c = threadIdx.x + it * 256, rr = c / k8, q = c - rr * k8, v = v0 + rr;
+#pragma unroll
+        for (int t = 0; t < 8; ++t) x[it][t] = 0.0f;
+        if (c < kTileCols * k8 && v < j.V) ld_w8<WDT>(j.W2, (size_t)v * j.rank + 8 * q, x[it]);
+      }
+#pragma unroll
+      for (int it = 0; it < kIt; ++it) {
+        const int c = threadIdx.x + it * 256, rr = c / k8, q = c - rr * k8;
+        if (c < kTileCols * k8) {
+          float4* d = reinterpret_cast<float4*>(w2s + rr * pitch + 8 * q);
+          d[0] = make_float4(x[it][0], x[it][1], x[it][2], x[it][3]);
+          d[1] = make_float4(x[it][4], x[it][5], x[it][6], x[it][7]);
+        }
+      }
+    }
+    __syncthreads();
+    for (int r0 = 0; r0 < j.rows; r0 += 4) {
+      const int row = r0 + slot, v = v0 + col;
+      RowInfo ri;
+      ri.prev = 0;
+      if (row < j.rows) {
+        ri = row_info(j, row);
+        // the row's W1[prev] into shared memory: 64 threads, 8 weights each
+        if (8 * col < j.rank) {
+          float xa[8];
+          ld_w8<WDT>(j.W1, (size_t)ri.prev * j.rank + 8 * col, xa);
+          float4* d = reinterpret_cast<float4*>(&w1s[slot][8 * col]);
+          d[0] = make_float4(xa[0], xa[1], xa[2], xa[3]);
+          d[1] = make_float4(xa[4], xa[5], xa[6], xa[7]);
+        }
+      }
+      __syncthreads();
+      // columns past V take no part; a masked or non-finite column is a -inf entry
+      StatsAcc e = stats_empty();
+      if (row < j.rows && v < j.V) {
+        e = {-INFINITY, 0.0f, v};
+        if (draft_allowed(j, ri.r, v)) {
+          float acc = 0.0f;
+          const float* at = w1s[slot];
+          const float* bt = w2s + col * pitch;
+          for (int i0 = 0; i0 < j.rank; i0 += 8) {
+            const float4 a0 = *reinterpret_cast<const float4*>(at + i0);
+            const float4 a1 = *reinterpret_cast<const float4*>(at + i0 + 4);
+            const float xa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const float4 b0 = *reinterpret_cast<const float4*>(bt + i0);
+            const float4 b1 = *reinterpret_cast<const float4*>(bt + i0 + 4);
+            const float xb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+            for (int t = 0; t < 8; ++t) acc = __fmaf_rn(xa[t], xb[t], acc);
+          }
+          const float z = __fmul_rn(__fadd_rn(ld_elem<UDT>(j.U, (size_t)ri.urow * j.V + v), acc),
+                                    j.scale);
+          if (z > -INFINITY) e = {z, 1.0f, v};
+        }
+      }
+      StatsAcc w = warp_merge(e);
+      if (lane == 0) half[slot][warp & 1] = w;
+      __syncthreads();
+      if (col == 0 && row < j.rows) {
+        const StatsAcc m = stats_merge(half[slot][0], half[slot][1]);
+        const size_t out = (size_t)row * nseg + sg;
+        pm[out] = m.m;
+        ps[out] = m.s;
+        if (ARGMAX) pi[out] = m.idx;
+      }
+      __syncthreads();
+    }
+  }
+}
+
 
 // One warp per (row, 64-column chunk); lane l handles columns c*64 + l and c*64 + 32 + l.
 template <int UDT, int WDT, int MODE, bool ARGMAX>
@@ -798,7 +939,8 @@ __global__ void __launch_bounds__(256) select_kernel(RowJob j, int seg, int nseg
   // 4. outputs
   if (tid == 0) {
     if (!resid) {
-      const size_t q = (size_t)row * j.gamma + (j.k - 1);
+      // the row's (request, position): one position per pass, or all of them (no Markov head)
+      const size_t q = j.map == MAP_ALL_POS ? (size_t)row : (size_t)row * j.gamma + (j.k - 1);
       o.tokens[q] = x;
       if (o.w1) l2_prefetch_bytes(static_cast<const char*>(o.w1) + (size_t)x * o.w1_row_bytes,
                                   o.w1_row_bytes);
@@ -976,6 +1118,22 @@ void launch_stream_t(const RowJob& j, int seg, int nseg, bool vec, float* pm, fl
 template <int UDT, int WDT>
 void launch_ffma_t(const RowJob& j, int nseg, bool argmax, float* pm, float* ps, int* pi, int grid,
                    cudaStream_t s) {
+  const bool tile = j.mode == MODE_STATS && j.rank > 0 && j.rank <= 256 && j.rank % 8 == 0 &&
+                    ((reinterpret_cast<uintptr_t>(j.W1) | reinterpret_cast<uintptr_t>(j.W2)) & 15) == 0;
+  if (tile) {
+    const size_t smem = (size_t)kTileCols * (j.rank + 4) * sizeof(float);
+    const int g = nseg < num_sms() * 3 ? nseg : num_sms() * 3;
+    if (argmax) {
+      cudaFuncSetAttribute(markov_ffma_tile<UDT, WDT, true>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      markov_ffma_tile<UDT, WDT, true><<<g, 256, smem, s>>>(j, nseg, pm, ps, pi);
+    } else {
+      cudaFuncSetAttribute(markov_ffma_tile<UDT, WDT, false>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      markov_ffma_tile<UDT, WDT, false><<<g, 256, smem, s>>>(j, nseg, pm, ps, pi);
+    }
+    return;
+  }
   switch (j.mode) {
     case MODE_STATS:
       if (argmax)
