@@ -43,7 +43,7 @@ __device__ __forceinline__ void ld_w8(const void* p, size_t i, float* x) {
 }
 
 // Markov bias W1[prev] . W2[v] in the canonical fp32 chain acc = fma(W1[prev][i], W2[v][i], acc),
-// i ascending. With 16-byte aligned rows the weights come 8 at a time, 64 in flight, and the
+// i ascending. With 16-byte aligned rows the weights come 8 at a time, 32 in flight, and the
 // chain is unchanged, so the result is bit-identical to the element-by-element loop.
 template <int WDT>
 __device__ __forceinline__ float markov_bias(const RowJob& j, int prev, int v) {
@@ -52,16 +52,17 @@ __device__ __forceinline__ float markov_bias(const RowJob& j, int prev, int v) {
   const bool vec = (j.rank & 7) == 0 &&
                    ((reinterpret_cast<uintptr_t>(j.W1) | reinterpret_cast<uintptr_t>(j.W2)) & 15) == 0;
   if (vec) {
-    for (int i0 = 0; i0 < j.rank; i0 += 64) {
-      float xa[64], xb[64];
+    constexpr int kChunk = 32;  // weights in flight per operand (registers are scarce in select)
+    for (int i0 = 0; i0 < j.rank; i0 += kChunk) {
+      float xa[kChunk], xb[kChunk];
 #pragma unroll
-      for (int t = 0; t < 8; ++t)
+      for (int t = 0; t < kChunk / 8; ++t)
         if (i0 + 8 * t < j.rank) {
           ld_w8<WDT>(j.W1, a + i0 + 8 * t, xa + 8 * t);
           ld_w8<WDT>(j.W2, b + i0 + 8 * t, xb + 8 * t);
         }
 #pragma unroll
-      for (int t = 0; t < 64; ++t)
+      for (int t = 0; t < kChunk; ++t)
         if (i0 + t < j.rank) acc = __fmaf_rn(xa[t], xb[t], acc);
     }
   } else {
@@ -566,6 +567,8 @@ __device__ void segment_logits(const RowJob& j, const RowInfo& ri, int v0, int n
     const int col = tid / tpc, part = tid % tpc;
     const int v = v0 + col;
     float acc = 0.0f;
+    // the base logit is independent of the dot product: its load goes out first
+    const float uval = col < n && part == 0 ? ld_elem<UDT>(j.U, (size_t)ri.urow * j.V + v) : 0.0f;
     if (col < n) {
       const uint4* w1 = reinterpret_cast<const uint4*>(
           reinterpret_cast<const unsigned short*>(j.W1) + (size_t)ri.prev * j.rank);
@@ -596,7 +599,7 @@ __device__ void segment_logits(const RowJob& j, const RowInfo& ri, int v0, int n
     }
     for (int off = tpc / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (col < n && part == 0) {
-      const float s = __fadd_rn(ld_elem<UDT>(j.U, (size_t)ri.urow * j.V + v), acc);
+      const float s = __fadd_rn(uval, acc);
       zs[col] = draft_allowed(j, ri.r, v) ? __fmul_rn(s, j.scale) : -INFINITY;
     }
   } else {
@@ -633,7 +636,7 @@ __device__ __forceinline__ void l2_prefetch_bytes(const void* p, unsigned bytes)
 // Only the crossing segment is recomputed element by element; everything else uses the
 // partials. Markov segments (<= 64 columns) are rebuilt once into shared memory.
 template <int UDT, int WDT>
-__global__ void __launch_bounds__(256) select_kernel(RowJob j, int seg, int nseg, const float* pm,
+__global__ void __launch_bounds__(256, 2) select_kernel(RowJob j, int seg, int nseg, const float* pm,
                                                      const float* ps, const int* pi,
                                                      SelectOut o) {
   __shared__ int sh_c, sh_x, sh_last;
