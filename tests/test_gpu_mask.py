@@ -126,3 +126,42 @@ def test_all_ones_mask_equals_no_mask(spec):
                                  allowed=ones)
     for x, y in zip(a, b):
         assert torch.equal(x, y)
+
+
+def test_masked_loop_iterations_match_oracle(spec):
+    """The device-resident loop with a grammar mask: every iteration's proposals, confidences,
+    scheduler lengths and verification against the oracle given the GPU's anchors, and every
+    drafted token allowed."""
+    from draft_sampling_verification_markov_gb300.loop import SpecLoop
+    R, gamma, V = 6, 4, 1040
+    wl = W.full_loop("cpu", R=R, gamma=gamma, V=V, rank=64, iterations=3, seed=41)
+    allowed, words = _mask(R, V, 0.3, 9)
+    g = {k: v.cuda() for k, v in wl.tensors().items()}
+    lp = SpecLoop(g["U"], g["target"], g["W1"], g["W2"], g["anchors"], g["u_draft"],
+                  g["u_accept"], g["u_resid"], wl.temperature, g["sps"], allowed=words.cuda())
+    lp.run()
+    torch.cuda.synchronize()
+    assert lp.ws.status() == 0
+    mask = words.numpy()
+    for t in range(wl.iterations):
+        a_t = lp.anchors[t].cpu()
+        toks = lp.draft_tokens[t].cpu()
+        tk = toks.numpy()
+        assert allowed[np.arange(R)[:, None], tk].all()
+        ref = oracle.markov_propose(wl.U, wl.W1, wl.W2, a_t, wl.u_draft[t], wl.temperature,
+                                    mask=mask)
+        compare_proposals(toks, None, None, ref)
+        tv = oracle.tv_confidence(wl.U, wl.target, wl.W1, wl.W2, a_t, toks, wl.temperature,
+                                  mask=mask)
+        assert_conf_close(lp.conf[t], tv["conf"])
+        sch = oracle.schedule_prefix(lp.survival[t].cpu(), wl.sps.numpy())
+        np.testing.assert_array_equal(lp.lengths[t].cpu().numpy(), sch["lengths"])
+        rv = oracle.verify_rejection(wl.target, wl.U, wl.W1, wl.W2, a_t, toks, wl.u_accept[t],
+                                     wl.u_resid[t], wl.temperature, lp.lengths[t].cpu(),
+                                     mask=mask)
+        n = lp.accept_len[t].cpu().numpy()
+        nxt = lp.anchors[t + 1].cpu().numpy()
+        amb = (np.nan_to_num(rv["accept_margin"], nan=1.0) < 1e-6).any(axis=1) | (
+            rv["resid_margin"] < 1e-6)
+        diff = (n != rv["accept_len"]) | (nxt != rv["next_anchor"])
+        assert not (diff & ~amb).any(), f"iteration {t}: {np.nonzero(diff & ~amb)}"
