@@ -481,7 +481,9 @@ static int verify_rejection_impl(const void* target, const void* U, int l_dtype,
   int rc = check_ws(ws, ws_bytes, SPEC_OP_VERIFY_REJECTION, R, gamma, V, rank, &L);
   if (rc != SPEC_OK) return rc;
   if (R == 0) return SPEC_OK;
-  if (!target || !U || !u_resid || !accept_len || !out_tokens) return SPEC_ERR_INVALID_ARG;
+  // without draft positions the draft side (U and the draft arrays) is never read
+  if (!target || (gamma > 0 && !U) || !u_resid || !accept_len || !out_tokens)
+    return SPEC_ERR_INVALID_ARG;
   if (gamma > 0 && (!draft_tokens || !draft_logp || !draft_stats || !u_accept))
     return SPEC_ERR_INVALID_ARG;
   if (rank > 0 && (!W1 || !W2 || !anchors)) return SPEC_ERR_INVALID_ARG;
@@ -527,7 +529,9 @@ static int verify_rejection_impl(const void* target, const void* U, int l_dtype,
   j.toff = toff;
   const int wdt = rank > 0 ? w_dtype : l_dtype;
   int seg, nseg;
-  if (rank == 0) {
+  if (rank == 0 || gamma == 0) {
+    // no Markov head, or no draft positions (every final row is a bonus row drawn from p_t
+    // alone, so the draft side is never read): the streaming pass
     seg = kStreamSeg;
     nseg = stream_nseg(V);
     launch_stream_partials(j, l_dtype, seg, nseg, vec_ok(target, U, l_dtype, V), true, false,

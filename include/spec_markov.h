@@ -170,7 +170,8 @@ int spec_target_stats(const void* target, int t_dtype, float temperature, int ro
  *   at the first rejection k = n+1 the output token is the inverse-CDF draw with u_resid[r]
  *   from norm(max(0, p_t,n - p_d,n+1)); if all l survive it is drawn from p_t,l.
  * Arguments:
- *   target       [R, gamma+1, V] and U [R, gamma, V], both dtype l_dtype.
+ *   target       [R, gamma+1, V] and U [R, gamma, V], both dtype l_dtype. With gamma = 0 every
+ *                final row is a bonus row drawn from p_t alone and U may be NULL.
  *   W1, W2, rank, anchors: as spec_markov_propose (they rebuild p_d for the residual).
  *   draft_tokens [R, gamma] int32 from spec_markov_propose.
  *   draft_logp   [R, gamma] and draft_stats [R, gamma, 2] from the same propose call, at the
