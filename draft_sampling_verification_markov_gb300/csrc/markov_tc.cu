@@ -3,18 +3,17 @@
 // DSpark", section 4 "Markov Head": B(x_{k-1}, .) = W1[x_{k-1}] W2 added to the base logits,
 // section 3 softmax; section 5 TV label; the residual of rejection sampling).
 //
-// One tile = 128 rows (requests, TMEM lanes) x N vocabulary columns (N = 128 for the softmax
-// partials and the residual, 64 for the TV pass), K = rank (<= 256, a multiple of 64). A work unit
-// is one W2 column tile against a pair of row blocks: the B tile is loaded once and feeds both
-// blocks' MMA groups, which halves the W2 bytes each SM pulls into shared memory.
+// One tile = 128 rows (requests, TMEM lanes) x N = 128 vocabulary columns, K = rank (<= 256, a
+// multiple of 64). A work unit is one W2 column tile against a pair of row blocks: the B tile
+// is loaded once and feeds both blocks' MMA groups, which halves the W2 bytes each SM pulls
+// into shared memory.
 //   A  [128 x rank] bf16 per row block: the W1 rows of each row's previous token, gathered by
 //      the epilogue warps (the first pair of a CTA through a shared-memory transpose, so that
 //      the rows are read whole) and stored into tensor memory with tcgen05.st (lane = row, two
 //      bf16 of K per 32-bit column); both blocks of the current pair stay resident.
 //   B  [N x rank] bf16: W2 rows (W2 stored [V, rank], K-major) by TMA, one whole tile per
 //      pipeline stage, kept in L2 with an evict-last policy and prefetched two units ahead.
-//   D  [128 x N] fp32 in tensor memory (2 stages at N = 128, 4 at N = 64), read back with
-//      tcgen05.ld.
+//   D  [128 x N] fp32 in tensor memory (2 stages), read back with tcgen05.ld.
 //   U / T tiles: the base-logit (and target) rows of each (unit, row block), by TMA with an
 //      evict-first policy (read once), 64-column boxes in the 128-byte-swizzled layout; rows
 //      that are not equally spaced (the final rows of rejection verification) are copied by
@@ -51,20 +50,20 @@ constexpr long long kSpinCycles = 4000000000LL;  // ~2 s at the maximum SM clock
 constexpr uint32_t kBoxBytes = kBM * 128;         // one TMA box: 128 rows x 64 columns (bf16)
 
 // Per pass mode. Shared memory (A lives in tensor memory):
-//   MODE_STATS: N = 128: B 2 x 64 KB + U 3 x 32 KB             = 224 KB; TMEM 2 x 128 + 2 x 128 cols
-//   MODE_TV:    N = 64:  B 2 x 32 KB + (U + T) 4 x 2 x 16 KB   = 192 KB; TMEM 4 x 64 + 2 x 128
-//   MODE_RESID: N = 128: B 1 x 64 KB + (U + T) 2 x 2 x 32 KB   = 192 KB; TMEM 2 x 128 + 2 x 128
-// The residual pass gathers its rows: a row piece of 256 bytes (N = 128) costs about as much
-// HBM time as one of 128 bytes, so it takes the wide tile at the price of a single W2 stage.
+//   MODE_STATS:          B 2 x 64 KB + U 3 x 32 KB             = 224 KB; TMEM 2 x 128 + 2 x 128 cols
+//   MODE_TV, MODE_RESID: B 1 x 64 KB + (U + T) 2 x 2 x 32 KB   = 192 KB; TMEM 2 x 128 + 2 x 128
+// N = 128 columns everywhere. The pair passes read two logit tensors; a row piece of 256 bytes
+// costs little more HBM time than one of 128 bytes, so they take the wide tile at the price of
+// a single W2 stage (the TV pass went from 1.51 to 1.29 ms at R = 512, gamma = 16).
 template <int MODE>
 struct Cfg {
-  static constexpr int kBN = MODE == MODE_TV ? 64 : 128;     // vocabulary columns per tile
+  static constexpr int kBN = 128;                             // vocabulary columns per tile
   static constexpr int kBoxes = kBN / 64;                     // 64-column boxes per logit tile
   static constexpr uint32_t kBAtomBytes = kBN * 128;          // kBN W2 rows x 64 K
   static constexpr uint32_t kBStageBytes = 4 * kBAtomBytes;   // K <= 256
-  static constexpr int kBStages = MODE == MODE_RESID ? 1 : 2;
+  static constexpr int kBStages = MODE == MODE_STATS ? 2 : 1;
   static constexpr uint32_t kTileBytes = kBoxes * kBoxBytes;
-  static constexpr int kUStages = MODE == MODE_STATS ? 3 : (MODE == MODE_RESID ? 2 : 4);
+  static constexpr int kUStages = MODE == MODE_STATS ? 3 : 2;
   static constexpr int kAccStages = kBN == 128 ? 2 : 4;       // accumulator stages in TMEM
   static constexpr int kAccCols = kAccStages * kBN;
   static constexpr int kACols = 128;                          // one A block (rank <= 256)
