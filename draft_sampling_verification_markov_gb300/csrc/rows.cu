@@ -630,7 +630,7 @@ __device__ __forceinline__ void l2_prefetch_bytes(const void* p, unsigned bytes)
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
-// One block (256 threads) per row.
+// One block per row: 256 threads, or 128 when the rows exceed one wave of 256-thread blocks.
 //   kind 0 (MODE_STATS partials): greedy argmax, or inverse-CDF draw from the softmax;
 //   kind 1 (MODE_RESID partials): inverse-CDF draw from the residual / bonus distribution.
 // Only the crossing segment is recomputed element by element; everything else uses the
@@ -1209,10 +1209,13 @@ void launch_select(const RowJob& j, int udt, int wdt, int seg, int nseg, const f
                    const float* ps, const int* pi, const SelectOut& o, cudaStream_t s) {
   if (j.rows == 0) return;
   TraceScope ts(SPEC_KCLASS_SELECT, s);
-  if (udt == SPEC_BF16 && wdt == SPEC_BF16) select_kernel<SPEC_BF16, SPEC_BF16><<<j.rows, 256, 0, s>>>(j, seg, nseg, pm, ps, pi, o);
-  else if (udt == SPEC_BF16) select_kernel<SPEC_BF16, SPEC_F32><<<j.rows, 256, 0, s>>>(j, seg, nseg, pm, ps, pi, o);
-  else if (wdt == SPEC_BF16) select_kernel<SPEC_F32, SPEC_BF16><<<j.rows, 256, 0, s>>>(j, seg, nseg, pm, ps, pi, o);
-  else select_kernel<SPEC_F32, SPEC_F32><<<j.rows, 256, 0, s>>>(j, seg, nseg, pm, ps, pi, o);
+  // two 256-thread blocks fit an SM; beyond one wave of those, 128-thread blocks (four per SM)
+  // halve the number of waves at some cost per row
+  const int nt = j.rows > 2 * num_sms() ? 128 : 256;
+  if (udt == SPEC_BF16 && wdt == SPEC_BF16) select_kernel<SPEC_BF16, SPEC_BF16><<<j.rows, nt, 0, s>>>(j, seg, nseg, pm, ps, pi, o);
+  else if (udt == SPEC_BF16) select_kernel<SPEC_BF16, SPEC_F32><<<j.rows, nt, 0, s>>>(j, seg, nseg, pm, ps, pi, o);
+  else if (wdt == SPEC_BF16) select_kernel<SPEC_F32, SPEC_BF16><<<j.rows, nt, 0, s>>>(j, seg, nseg, pm, ps, pi, o);
+  else select_kernel<SPEC_F32, SPEC_F32><<<j.rows, nt, 0, s>>>(j, seg, nseg, pm, ps, pi, o);
 }
 
 void launch_finalize_stats(int rows, int nseg, const float* pm, const float* ps, float* stats,
