@@ -352,7 +352,7 @@ int spec_verify_rejection_flat(const void* target, const void* U, int l_dtype, c
 
 /*
  * Greedy verification that allocates nothing and takes no workspace.
- * The paper has no counterpart: this entry point exists for callers that cannot allocate
+ * No page defines this entry point: it exists for callers that cannot allocate
  * device memory at the call site (a plug-in inside an engine that reserves all device memory at
  * start-up, a latency-critical loop that must not meet cudaMalloc's implicit synchronisation,
  * a host whose memory is owned by another framework's allocator). It computes exactly what

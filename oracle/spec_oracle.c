@@ -27,7 +27,7 @@
  *     tau = sum(1 + sum_{j<=l_r} a_{r,j}), Theta = tau * SPS(B), queue all (r, j) by a_{r,j}
  *     descending: DSpark section 6.
  *
- * Readings where the pages are silent (each one is also listed in the design doc):
+ * Readings where the pages are silent:
  *   R1  Markov bias arithmetic. With fp32 weights the bias is the canonical fp32 chain
  *       acc = fmaf(W1[x][i], W2[v][i], acc) for i = 0..r-1 ascending, and the logit is the
  *       fp32 sum U + acc. With bf16 weights every product is exact and the sum is taken in
