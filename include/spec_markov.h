@@ -52,7 +52,7 @@ extern "C" {
 #define SPEC_ERR_UNSUPPORTED_DTYPE (-2)  /* dtype code outside {SPEC_F32, SPEC_BF16} */
 #define SPEC_ERR_WORKSPACE_TOO_SMALL (-3)
 #define SPEC_ERR_CUDA (-4)               /* a CUDA runtime call or launch failed */
-#define SPEC_ERR_UNSUPPORTED (-6)        /* a combination this build does not implement */
+#define SPEC_ERR_UNSUPPORTED (-6)        /* a combination the library does not implement */
 #define SPEC_ERR_TOO_LARGE (-7)          /* sizes beyond a fixed limit (SPEC_NOALLOC_MAX_ROWS) */
 
 /* dtype codes */
