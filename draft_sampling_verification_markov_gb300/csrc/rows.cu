@@ -294,6 +294,37 @@ __device__ __forceinline__ void row_word(const float (&x)[8], int v, float c, fl
   }
 }
 
+// The normaliser part of row_word over a whole batch of words: one maximum and at most one
+// rescale per batch instead of per word (fewer instructions per element; the same sum up to
+// rounding).
+template <int NB>
+__device__ __forceinline__ void row_words_stats(const float (&x)[NB][8], float c, float& mx,
+                                                unsigned long long& s2) {
+  float g = mx;
+#pragma unroll
+  for (int b = 0; b < NB; ++b)
+    g = fmaxf(g, fmaxf(fmax3(x[b][0], x[b][1], x[b][2]),
+                       fmax3(fmax3(x[b][3], x[b][4], x[b][5]), x[b][6], x[b][7])));
+  if (g > mx) {
+    if (mx > -INFINITY) {
+      const float f = fast_exp2((mx - g) * c);
+      s2 = mulx2(s2, pk2(f, f));
+    }
+    mx = g;
+  }
+  if (mx > -INFINITY) {  // words with no finite value so far add nothing (and no NaN)
+    const unsigned long long nm = pk2(-mx, -mx), c2 = pk2(c, c);
+#pragma unroll
+    for (int b = 0; b < NB; ++b)
+#pragma unroll
+      for (int i = 0; i < 8; i += 2) {
+        float a, bb;
+        upk2(mulx2(addx2(pk2(x[b][i], x[b][i + 1]), nm), c2), a, bb);
+        s2 = addx2(s2, pk2(fast_exp2(a), fast_exp2(bb)));
+      }
+  }
+}
+
 template <int DT>
 __device__ __forceinline__ void unpack_word(const uint4& q, float (&x)[8]) {
   if constexpr (DT == SPEC_BF16) {
@@ -334,11 +365,18 @@ __global__ void __launch_bounds__(kRowThreads, 2) row_stats_kernel(RowJob j, boo
         const int w = w0 + stride + b * kRowThreads;
         nxt[b] = w < nw ? ld_stream16(p + w) : make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
       }
+      if constexpr (STATS && !ARGMAX) {
+        float x[kBatch][8];
 #pragma unroll
-      for (int b = 0; b < kBatch; ++b) {
-        float x[8];
-        unpack_word<DT>(cur[b], x);  // padding words decode to -inf
-        row_word<DT, STATS, ARGMAX>(x, (w0 + b * kRowThreads) * 8, c, mx, s2, idx);
+        for (int b = 0; b < kBatch; ++b) unpack_word<DT>(cur[b], x[b]);  // padding: -inf
+        row_words_stats<kBatch>(x, c, mx, s2);
+      } else {
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+          float x[8];
+          unpack_word<DT>(cur[b], x);  // padding words decode to -inf
+          row_word<DT, STATS, ARGMAX>(x, (w0 + b * kRowThreads) * 8, c, mx, s2, idx);
+        }
       }
 #pragma unroll
       for (int b = 0; b < kBatch; ++b) cur[b] = nxt[b];
