@@ -183,9 +183,12 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
 }
 
 // 16 bytes global -> shared, asynchronous; src_bytes 0 writes zeros without reading.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-               "r"(src_bytes)
+// The gathered logit rows are read once: they go to L2 with an evict-first policy so that they
+// do not push out W2, which the next proposal reads again.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes,
+                                           uint64_t policy) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(dst),
+               "l"(src), "r"(src_bytes), "l"(policy)
                : "memory");
 }
 
@@ -627,7 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const long long ro = (long long)tab[sb * kBM + i] * j.V + n0 + 8 * c;
             const uint32_t so = bx * kBoxBytes + i * 128 + ((cc ^ (i & 7)) << 4);
             cp_async16((tside ? st_base : su_base) + so, (tside ? Tb : Ub) + (nb16 ? ro : 0),
-                       nb16);
+                       nb16, pol_stream);
           }
           cp_async_arrive(&u_full[us]);
         }
