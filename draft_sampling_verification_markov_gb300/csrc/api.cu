@@ -65,6 +65,12 @@ void trace_end(int kclass, cudaStream_t s) {
   }
 }
 
+bool trace_active() {
+  for (const TraceState& t : g_trace)
+    if (t.capacity > 0) return true;
+  return false;
+}
+
 namespace {
 
 constexpr size_t kAlign = 256;
@@ -338,11 +344,14 @@ static int markov_propose_impl(const void* U, int u_dtype, const void* W1, const
     const int nseg = stream_nseg(V);
     launch_stream_partials(j, u_dtype, kStreamSeg, nseg, vec, true, greedy, w.pm, w.ps, w.pi,
                            grid_for((long long)j.rows * nseg, 1), s);
+    j.pdl = 1;
     launch_select(j, u_dtype, wdt, kStreamSeg, nseg, w.pm, w.ps, greedy ? w.pi : nullptr, o, s);
     return finish();
   }
+  // every launch after the first is chained to the one before it
   for (int k = 1; k <= gamma; ++k) {
     j.k = k;
+    j.pdl = k > 1;
     o.uni_offset = k - 1;
     int seg, nseg;
     if (rank == 0) {
@@ -363,6 +372,7 @@ static int markov_propose_impl(const void* U, int u_dtype, const void* W1, const
     const int w1_row = rank * (int)esize(wdt);
     o.w1 = rank > 0 && k < gamma && aligned16(W1) && w1_row % 16 == 0 ? W1 : nullptr;
     o.w1_row_bytes = w1_row;
+    j.pdl = 1;
     launch_select(j, u_dtype, wdt, seg, nseg, w.pm, w.ps, greedy ? w.pi : nullptr, o, s);
   }
   return finish();
@@ -499,8 +509,10 @@ static int verify_rejection_impl(const void* target, const void* U, int l_dtype,
   const int w1_row = rank * (int)esize(w_dtype);
   const RowPrefetch pf = {rank > 0 && aligned16(W1) && w1_row % 16 == 0 ? W1 : nullptr, w1_row,
                           anchors};
+  // chained to the target normaliser pass when this call ran it
   launch_accept(l_dtype, R, gamma, V, scale, target, tstats, draft_tokens, draft_logp, u_accept,
-                lengths, toff, w.final_n, w.final_kind, accept_len, out_tokens, w.status, pf, s);
+                lengths, toff, w.final_n, w.final_kind, accept_len, out_tokens, w.status, pf,
+                tstats == w.tstats, s);
 
   RowJob j;
   memset(&j, 0, sizeof j);
@@ -527,6 +539,7 @@ static int verify_rejection_impl(const void* target, const void* U, int l_dtype,
   j.mask = mask;
   j.mask_words = (V + 31) / 32;
   j.toff = toff;
+  j.pdl = 1;  // after the acceptance scan
   const int wdt = rank > 0 ? w_dtype : l_dtype;
   int seg, nseg;
   if (rank == 0 || gamma == 0) {

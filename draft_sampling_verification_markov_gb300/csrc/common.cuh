@@ -18,6 +18,18 @@ namespace spec {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
+// ------------------------------------------------------------------------------ launch chaining
+
+// Programmatic dependent launch. A kernel launched with programmatic stream serialisation is
+// scheduled as the blocks of the kernel before it on the stream exit, without waiting for that
+// kernel's completion and memory flush. grid_dep_wait() returns once that kernel has completed
+// and its writes are visible; a thread must pass it before it reads anything the earlier kernels
+// of the call write, or writes anything they read. For a kernel launched without the attribute
+// it returns at once. No kernel here signals its dependents early
+// (griddepcontrol.launch_dependents): a Markov pass scheduled while the select kernel still ran
+// made every such pair about 6 us slower, even with nothing done before its wait.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------------------------------------------ element loads
 
 __device__ __forceinline__ float bf16_to_f32(uint16_t b) {
@@ -272,6 +284,9 @@ struct RowJob {
   // flattened verify batch: target rows of request r are toff[r] .. toff[r+1]-1 of a packed
   // [*, V] array (toff[R] rows in all), or null for the padded [R, gamma+1, V] layout
   const int32_t* toff;
+  // nonzero: the pass may be launched while the previous kernel of the same call still runs
+  // (its kernels then wait with grid_dep_wait before touching that kernel's data)
+  int pdl;
 };
 
 // Row of target position i (0..gamma) of request r in a target array of R*(gamma+1) rows,

@@ -62,7 +62,8 @@ void launch_accept(int dtype, int R, int gamma, int V, float scale, const void* 
                    const float* tstats, const int32_t* tokens, const float* dlogp,
                    const float* u_accept, const int32_t* lengths, const int32_t* toff,
                    int32_t* final_n, int32_t* final_kind, int32_t* accept_len,
-                   int32_t* out_tokens, uint32_t* status, RowPrefetch pf, cudaStream_t s);
+                   int32_t* out_tokens, uint32_t* status, RowPrefetch pf, bool chained,
+                   cudaStream_t s);
 void launch_tv_finalize(int R, int gamma, int nseg, const float* ps, float* conf, float* survival,
                         cudaStream_t s);
 cudaError_t launch_schedule(const float* survival, const double* sps, int Bmax, int R, int gamma,
@@ -91,6 +92,32 @@ int num_sms();
 // end events of its kernel class on the launch stream.
 void trace_begin(int kclass, cudaStream_t s);
 void trace_end(int kclass, cudaStream_t s);
+
+// Whether any kernel class has caller-owned trace events attached. Chained launches are then
+// issued plainly, so that every recorded interval spans exactly one kernel.
+bool trace_active();
+
+// Launch of kernel k on stream s. With `chained` it is a programmatic dependent launch: k is
+// scheduled as the blocks of the previous kernel on the stream exit, without waiting for that
+// kernel's completion, and must call grid_dep_wait before it touches what that kernel or an
+// earlier one of the same call writes or reads. Only the kernels of a call after its first
+// launch are chained, so what a chained kernel reads before its wait (inputs of the call that
+// no kernel of the call writes) was finished before the call's first kernel began.
+template <typename... P, typename... A>
+cudaError_t launch_kernel(void (*k)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                          bool chained, A&&... args) {
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = &attr;
+  cfg.numAttrs = chained && !trace_active() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k, static_cast<A&&>(args)...);
+}
 
 struct TraceScope {
   int kclass;

@@ -522,6 +522,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // When this launch is chained to the kernel that drew the previous tokens, the W2 and logit
+  // tiles (inputs that no kernel writes) start loading before that kernel's completion; the
+  // warps that read its tokens or write the partials it reads pass grid_dep_wait first.
 
   if (warp == 0) {
     // ---------------------------------------------------------------- W2 (B) producer
@@ -563,6 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     int mp = mp_first, nt = nt_first, rows_mp = -1;
     const bool tside = warp == 2;
+    if constexpr (GATHER) grid_dep_wait();  // the final rows come from the acceptance scan
     // gathered row indices of the pair's two row blocks, loaded once per pair into a table
     // (rows past R and the U rows of bonus rows point at row 0 and are ignored)
     for (long long u = u_begin; u < u_end && ok; ++u) {
@@ -694,6 +698,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp >= kFirstEpi && warp < kFirstEpi + kEpiWarps) {
     // ---------------------------------------------------------------- epilogue
+    grid_dep_wait();
     const int ew = warp - kFirstEpi;
     const int q = warp & 3;          // TMEM lane quarter
     const int h = ew >> 2;           // column half
@@ -1028,8 +1033,7 @@ cudaError_t launch_t(const TcParams& p, const CUtensorMap& w2, const CUtensorMap
   auto k = markov_tc_kernel<MODE, ARGMAX, GATHER>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  k<<<grid, kThreads, smem, s>>>(w2, u, t, p);
-  return cudaGetLastError();
+  return launch_kernel(k, dim3(grid), dim3(kThreads), smem, s, p.j.pdl != 0, w2, u, t, p);
 }
 
 }  // namespace tc

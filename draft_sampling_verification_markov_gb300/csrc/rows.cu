@@ -684,8 +684,9 @@ __global__ void __launch_bounds__(256, 2) select_kernel(RowJob j, int seg, int n
   __shared__ float es[64];
   __shared__ int sh_zv0;
   const int row = blockIdx.x;
-  if (row >= j.rows) return;
+  grid_dep_wait();  // the partials come from the kernel before
   if (o.l2_prefetch && threadIdx.x == 0) l2_prefetch_share(o.l2_prefetch, o.l2_prefetch_bytes);
+  if (row >= j.rows) return;
   const RowInfo ri = row_info(j, row);
   const int tid = threadIdx.x;
   const bool resid = o.kind == 1;
@@ -1076,6 +1077,7 @@ __global__ void accept_kernel(int R, int gamma, int V, float scale, const void* 
                               const int32_t* toff, int32_t* final_n, int32_t* final_kind,
                               int32_t* accept_len, int32_t* out_tokens, uint32_t* status,
                               RowPrefetch pf) {
+  grid_dep_wait();  // the target normalisers may come from the kernel before
   const int lane = threadIdx.x & 31;
   const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (r >= R) return;
@@ -1250,10 +1252,11 @@ void launch_select(const RowJob& j, int udt, int wdt, int seg, int nseg, const f
   // two 256-thread blocks fit an SM; beyond one wave of those, 128-thread blocks (four per SM)
   // halve the number of waves at some cost per row
   const int nt = j.rows > 2 * num_sms() ? 128 : 256;
-  if (udt == SPEC_BF16 && wdt == SPEC_BF16) select_kernel<SPEC_BF16, SPEC_BF16><<<j.rows, nt, 0, s>>>(j, seg, nseg, pm, ps, pi, o);
-  else if (udt == SPEC_BF16) select_kernel<SPEC_BF16, SPEC_F32><<<j.rows, nt, 0, s>>>(j, seg, nseg, pm, ps, pi, o);
-  else if (wdt == SPEC_BF16) select_kernel<SPEC_F32, SPEC_BF16><<<j.rows, nt, 0, s>>>(j, seg, nseg, pm, ps, pi, o);
-  else select_kernel<SPEC_F32, SPEC_F32><<<j.rows, nt, 0, s>>>(j, seg, nseg, pm, ps, pi, o);
+  auto k = udt == SPEC_BF16 ? (wdt == SPEC_BF16 ? select_kernel<SPEC_BF16, SPEC_BF16>
+                                                : select_kernel<SPEC_BF16, SPEC_F32>)
+                            : (wdt == SPEC_BF16 ? select_kernel<SPEC_F32, SPEC_BF16>
+                                                : select_kernel<SPEC_F32, SPEC_F32>);
+  launch_kernel(k, dim3(j.rows), dim3(nt), 0, s, j.pdl != 0, j, seg, nseg, pm, ps, pi, o);
 }
 
 void launch_finalize_stats(int rows, int nseg, const float* pm, const float* ps, float* stats,
@@ -1278,17 +1281,14 @@ void launch_accept(int dtype, int R, int gamma, int V, float scale, const void* 
                    const float* tstats, const int32_t* tokens, const float* dlogp,
                    const float* u_accept, const int32_t* lengths, const int32_t* toff,
                    int32_t* final_n, int32_t* final_kind, int32_t* accept_len,
-                   int32_t* out_tokens, uint32_t* status, RowPrefetch pf, cudaStream_t s) {
+                   int32_t* out_tokens, uint32_t* status, RowPrefetch pf, bool chained,
+                   cudaStream_t s) {
   TraceScope ts(SPEC_KCLASS_OTHER, s);
   const int grid = (R + 7) / 8;  // one warp per request, 8 warps per block
-  if (dtype == SPEC_BF16)
-    accept_kernel<SPEC_BF16><<<grid, 256, 0, s>>>(R, gamma, V, scale, T, tstats, tokens, dlogp,
-                                                  u_accept, lengths, toff, final_n, final_kind,
-                                                  accept_len, out_tokens, status, pf);
-  else
-    accept_kernel<SPEC_F32><<<grid, 256, 0, s>>>(R, gamma, V, scale, T, tstats, tokens, dlogp,
-                                                 u_accept, lengths, toff, final_n, final_kind,
-                                                 accept_len, out_tokens, status, pf);
+  launch_kernel(dtype == SPEC_BF16 ? accept_kernel<SPEC_BF16> : accept_kernel<SPEC_F32>,
+                dim3(grid), dim3(256), 0, s, chained, R, gamma, V, scale, T, tstats, tokens,
+                dlogp, u_accept, lengths, toff, final_n, final_kind, accept_len, out_tokens,
+                status, pf);
 }
 
 void launch_tv_finalize(int R, int gamma, int nseg, const float* ps, float* conf, float* survival,
