@@ -363,12 +363,7 @@ static int markov_propose_impl(const void* U, int u_dtype, const void* W1, const
       rc = markov_pass(j, u_dtype, wdt, w, greedy, s, &seg, &nseg);
       if (rc != SPEC_OK) return rc;
     }
-    // the next position's Markov pass re-reads all of W2: have L2 fetch it during this select
-    const size_t w2_bytes = (size_t)V * rank * esize(wdt);
-    const bool pf = rank > 0 && k < gamma && aligned16(W2) && w2_bytes % 16 == 0;
-    o.l2_prefetch = pf ? W2 : nullptr;
-    o.l2_prefetch_bytes = pf ? w2_bytes : 0;
-    // ... and the W1 row of each drawn token, which the next position gathers
+    // the W1 row of each drawn token, which the next position gathers, is pulled into L2
     const int w1_row = rank * (int)esize(wdt);
     o.w1 = rank > 0 && k < gamma && aligned16(W1) && w1_row % 16 == 0 ? W1 : nullptr;
     o.w1_row_bytes = w1_row;
@@ -561,12 +556,8 @@ static int verify_rejection_impl(const void* target, const void* U, int l_dtype,
   o.uni = u_resid;
   o.uni_stride = 1;
   o.uni_offset = 0;
-  // a decoding loop proposes next from the emitted tokens: have L2 fetch W2 and their W1 rows
-  const size_t w2_bytes = (size_t)V * rank * esize(wdt);
-  const bool next_pf = rank > 0 && aligned16(W2) && w2_bytes % 16 == 0;
-  o.l2_prefetch = next_pf ? W2 : nullptr;
-  o.l2_prefetch_bytes = next_pf ? w2_bytes : 0;
-  o.w1 = next_pf && aligned16(W1) && (rank * esize(wdt)) % 16 == 0 ? W1 : nullptr;
+  // a decoding loop proposes next from the emitted tokens: have L2 fetch their W1 rows
+  o.w1 = rank > 0 && aligned16(W1) && (rank * esize(wdt)) % 16 == 0 ? W1 : nullptr;
   o.w1_row_bytes = rank * (int)esize(wdt);
   launch_select(j, l_dtype, wdt, seg, nseg, w.pm, w.ps, nullptr, o, s);
   return finish();

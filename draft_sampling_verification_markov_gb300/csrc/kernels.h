@@ -23,10 +23,6 @@ struct SelectOut {
   const float* uni;      // uniforms, indexed row * uni_stride + uni_offset
   int uni_stride, uni_offset;
   int greedy;
-  // optional: bytes the next kernel reads (the Markov projection), pulled into L2 while this
-  // latency-bound kernel runs; 16-byte aligned, a multiple of 16 bytes
-  const void* l2_prefetch;
-  unsigned long long l2_prefetch_bytes;
   // optional: the Markov embedding; the row of each drawn token (w1_row_bytes, a multiple of
   // 16) is pulled into L2 for the next position's A-operand gather
   const void* w1;

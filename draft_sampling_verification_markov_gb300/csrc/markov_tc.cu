@@ -12,7 +12,10 @@
 //      the rows are read whole) and stored into tensor memory with tcgen05.st (lane = row, two
 //      bf16 of K per 32-bit column); both blocks of the current pair stay resident.
 //   B  [N x rank] bf16: W2 rows (W2 stored [V, rank], K-major) by TMA, one whole tile per
-//      pipeline stage, kept in L2 with an evict-last policy and prefetched two units ahead.
+//      pipeline stage, kept in L2 with an evict-last policy. W2 is re-read by every position
+//      and stays in L2 while the logit streams are evict-first, so no copy is prefetched: an
+//      L2 prefetch two units ahead, and one of all of W2 by the select kernel, only queued in
+//      front of the copies the pipeline waits for.
 //   D  [128 x N] fp32 in tensor memory (2 stages), read back with tcgen05.ld.
 //   U / T tiles: the base-logit (and target) rows of each (unit, row block), by TMA with an
 //      evict-first policy (read once), 64-column boxes in the 128-byte-swizzled layout; rows
@@ -63,7 +66,8 @@ struct Cfg {
   static constexpr uint32_t kBStageBytes = 4 * kBAtomBytes;   // K <= 256
   static constexpr int kBStages = MODE == MODE_STATS ? 2 : 1;
   static constexpr uint32_t kTileBytes = kBoxes * kBoxBytes;
-  static constexpr int kUStages = MODE == MODE_STATS ? 3 : 2;
+  // two stages: a third kept more copies queued ahead of the W2 tile the MMA waits for
+  static constexpr int kUStages = 2;
   static constexpr int kAccStages = kBN == 128 ? 2 : 4;       // accumulator stages in TMEM
   static constexpr int kAccCols = kAccStages * kBN;
   static constexpr int kACols = 128;                          // one A block (rank <= 256)
@@ -149,15 +153,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
-// Prefetch a tile of a 2-D tensor into L2 (no shared-memory destination).
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int c0, int c1,
-                                                uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.prefetch.tensor.2d.L2.global.tile.L2::cache_hint [%0, {%1, %2}], %3;" ::"l"(
-          reinterpret_cast<uint64_t>(map)),
-      "r"(c0), "r"(c1), "l"(policy)
-      : "memory");
-}
 
 // Four rows (r0..r3) x 64 columns of a 2-D tensor whose box is one row high, into 512
 // consecutive bytes of shared memory (swizzled by address like a 4-row box).
@@ -532,19 +527,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     int bs = 0;
     uint32_t bph = 0;
     bool ok = true;
-    constexpr int kPrefetch = 2;  // units ahead of the shared-memory ring, into L2
-    int nt = nt_first, pf = nt_first;
-    if (lane == 0)
-      for (long long u = u_begin; u < u_begin + kPrefetch && u < u_end; ++u) {
-        for (int ka = 0; ka < ka_n; ++ka) tma_prefetch_2d(&map_w2, ka * 64, pf * BN, pol_keep);
-        if (++pf == n_nt) pf = 0;
-      }
+    int nt = nt_first;
     for (long long u = u_begin; u < u_end && ok; ++u) {
       const int n0 = nt * BN;
       if (++nt == n_nt) nt = 0;
-      if (lane == 0 && u + kPrefetch < u_end)
-        for (int ka = 0; ka < ka_n; ++ka) tma_prefetch_2d(&map_w2, ka * 64, pf * BN, pol_keep);
-      if (u + kPrefetch < u_end && ++pf == n_nt) pf = 0;
       ok = mbar_wait(&b_empty[bs], bph ^ 1, abort, status);
       if (ok && kScrInB && u == u_begin + 1) ok = mbar_wait(scr_free, 0, abort, status);
       if (ok && lane == 0 && !(P.stall && u == u_begin)) {

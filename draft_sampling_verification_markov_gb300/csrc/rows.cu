@@ -646,23 +646,6 @@ __device__ void segment_logits(const RowJob& j, const RowInfo& ri, int v0, int n
   __syncthreads();
 }
 
-// Block b asks L2 for its share of [base, base + bytes) (a bulk prefetch, no data returned).
-__device__ __forceinline__ void l2_prefetch_share(const void* base, unsigned long long bytes) {
-  const unsigned long long share = ((bytes + gridDim.x - 1) / gridDim.x + 15) & ~15ull;
-  const unsigned long long b0 = share * blockIdx.x;
-  const unsigned long long b1 = b0 + share < bytes ? b0 + share : bytes;
-  uint64_t pol;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
-  // one instruction per block: issuing is the slow part, not the size
-  for (unsigned long long off = b0; off < b1; off += (1ull << 30)) {
-    const unsigned n = (unsigned)(b1 - off < (1ull << 30) ? b1 - off : (1ull << 30));
-    asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(
-                     reinterpret_cast<const char*>(base) + off),
-                 "r"(n), "l"(pol)
-                 : "memory");
-  }
-}
-
 // Bulk prefetch of [p, p + bytes) into L2 (16-byte aligned, a multiple of 16 bytes).
 __device__ __forceinline__ void l2_prefetch_bytes(const void* p, unsigned bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
@@ -685,7 +668,6 @@ __global__ void __launch_bounds__(256, 2) select_kernel(RowJob j, int seg, int n
   __shared__ int sh_zv0;
   const int row = blockIdx.x;
   grid_dep_wait();  // the partials come from the kernel before
-  if (o.l2_prefetch && threadIdx.x == 0) l2_prefetch_share(o.l2_prefetch, o.l2_prefetch_bytes);
   if (row >= j.rows) return;
   const RowInfo ri = row_info(j, row);
   const int tid = threadIdx.x;
