@@ -406,6 +406,7 @@ struct TcParams {
   int* pi;
   int nseg;   // partial segments per row (row-major partial arrays)
   int stall;  // test of the bounded waits: the first W2 tile is never loaded
+  int w1_32;  // W1 is 32-byte aligned: the first A gather may use 32-byte loads
 };
 
 // Per-row normalisers of the pair modes for one row (loaded once per row block).
@@ -734,18 +735,49 @@ __global__ void __launch_bounds__(kThreads, 1)
           // Piece p of a half row is chunks 8p..8p+7; chunk c of warp row rl sits at slot
           // c ^ (rl & 7), so stores and loads are conflict-free.
           const uint32_t scr = smem_u32(scr_base) + ew * 4096;
+          // Softmax-partial and residual passes: four lanes per piece, 32 bytes each (eight rows
+          // per instruction), which halves the loads in flight; slot k of v holds the piece's
+          // chunk pair of row 8(k/2) + lane/4, half k%2. TV pass: eight lanes per piece, 16 bytes
+          // each (the wide loads made that pass slower); slot k holds row 4k + lane/8.
+          constexpr bool kWide = MODE != MODE_TV;
           uint4 v[2][2][8];
 #pragma unroll
           for (int sb = 0; sb < 2; ++sb)
 #pragma unroll
-            for (int p = 0; p < 2; ++p)
+            for (int p = 0; p < 2; ++p) {
+              if constexpr (kWide) {
 #pragma unroll
-              for (int k = 0; k < 8; ++k) {
-                const int rl = 4 * k + (lane >> 3), c = 8 * p + (lane & 7);
-                const int row = __shfl_sync(0xffffffffu, src_row[sb], rl);
-                v[sb][p][k] = make_uint4(0, 0, 0, 0);
-                if (row >= 0 && c < per) v[sb][p][k] = __ldg(w1 + (size_t)row * row_chunks + h * per + c);
+                for (int k = 0; k < 4; ++k) {
+                  const int rl = 8 * k + (lane >> 2), c = 8 * p + 2 * (lane & 3);
+                  const int row = __shfl_sync(0xffffffffu, src_row[sb], rl);
+                  uint4 a = make_uint4(0, 0, 0, 0), b = a;
+                  // per is a multiple of 4 and c even, so chunk c + 1 is in the row too
+                  if (row >= 0 && c < per) {
+                    const uint4* src = w1 + (size_t)row * row_chunks + h * per + c;
+                    if (P.w1_32) {
+                      asm volatile("ld.global.nc.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                                   : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x),
+                                     "=r"(b.y), "=r"(b.z), "=r"(b.w)
+                                   : "l"(src));
+                    } else {
+                      a = __ldg(src);
+                      b = __ldg(src + 1);
+                    }
+                  }
+                  v[sb][p][2 * k] = a;
+                  v[sb][p][2 * k + 1] = b;
+                }
+              } else {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                  const int rl = 4 * k + (lane >> 3), c = 8 * p + (lane & 7);
+                  const int row = __shfl_sync(0xffffffffu, src_row[sb], rl);
+                  v[sb][p][k] = make_uint4(0, 0, 0, 0);
+                  if (row >= 0 && c < per)
+                    v[sb][p][k] = __ldg(w1 + (size_t)row * row_chunks + h * per + c);
+                }
               }
+            }
 #pragma unroll
           for (int sb = 0; sb < 2; ++sb) {
             if (sb >= nb) break;
@@ -753,10 +785,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     sb * C::kACols + h * (j.rank / 4);
 #pragma unroll
             for (int p = 0; p < 2; ++p) {
+              if constexpr (kWide) {
 #pragma unroll
-              for (int k = 0; k < 8; ++k) {
-                const int rl = 4 * k + (lane >> 3);
-                sts128(scr + rl * 128 + (((lane & 7) ^ (rl & 7)) << 4), v[sb][p][k]);
+                for (int k = 0; k < 4; ++k) {
+                  const int rl = 8 * k + (lane >> 2), cc = 2 * (lane & 3);
+                  sts128(scr + rl * 128 + ((cc ^ (rl & 7)) << 4), v[sb][p][2 * k]);
+                  sts128(scr + rl * 128 + (((cc + 1) ^ (rl & 7)) << 4), v[sb][p][2 * k + 1]);
+                }
+              } else {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                  const int rl = 4 * k + (lane >> 3);
+                  sts128(scr + rl * 128 + (((lane & 7) ^ (rl & 7)) << 4), v[sb][p][k]);
+                }
               }
               __syncwarp();
               uint32_t w[32];
@@ -1063,6 +1104,7 @@ cudaError_t launch_markov_tc(const RowJob& j, float* pm, float* ps, int* pi, boo
   p.t.n_nt = (j.V + BN - 1) / BN;
   p.nseg = (j.V + BN / 2 - 1) / (BN / 2);
   p.stall = __atomic_exchange_n(&g_stall_next, 0, __ATOMIC_RELAXED);
+  p.w1_32 = (reinterpret_cast<uintptr_t>(j.W1) & 31) == 0;
   // work units: one column tile against a pair of row blocks
   const long long total = (long long)((p.t.n_mt + 1) / 2) * p.t.n_nt;
   if (total == 0) return cudaSuccess;

@@ -102,3 +102,25 @@ def test_one_token_vocabulary(spec, ws):
     assert (conf == 1).all() and (surv == 1).all()
     n, out, nxt = spec.spec_verify_greedy(T, toks, workspace=ws)
     assert (n == gamma).all() and (nxt == 0).all()
+
+
+def test_w1_alignment_16_bytes(spec, ws):
+    """The tensor-core pass reads W1 rows with 32-byte loads when W1 is 32-byte aligned and
+    with 16-byte loads otherwise: a W1 at a 16-byte offset gives bit-identical proposals and
+    residual draws."""
+    R, gamma, V, rank = 200, 4, 4104, 256
+    wl = W.markov_rejection("cuda", R=R, gamma=gamma, V=V, rank=rank, seed=77, temperature=1.0)
+    buf = torch.empty(V * rank + 8, dtype=wl.W1.dtype, device="cuda")
+    W1_off = buf[8:].view(V, rank)
+    W1_off.copy_(wl.W1)
+    assert W1_off.data_ptr() % 32 == 16
+    outs = []
+    for W1 in (wl.W1, W1_off):
+        toks, logp, st = spec.spec_markov_propose(wl.U, W1, wl.W2, wl.anchors, wl.u_draft, 1.0,
+                                                  workspace=ws)
+        n, out, nxt = spec.spec_verify_rejection(wl.target, wl.U, W1, wl.W2, wl.anchors, toks,
+                                                 logp, st, wl.u_accept, wl.u_resid, 1.0,
+                                                 workspace=ws)
+        outs.append([x.cpu() for x in (toks, logp, st, n, out, nxt)])
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
