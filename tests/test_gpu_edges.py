@@ -104,11 +104,13 @@ def test_one_token_vocabulary(spec, ws):
     assert (n == gamma).all() and (nxt == 0).all()
 
 
-def test_w1_alignment_16_bytes(spec, ws):
+@pytest.mark.parametrize("R,V", [(200, 4104), (600, 129280)])
+def test_w1_alignment_16_bytes(spec, ws, R, V):
     """The tensor-core pass reads W1 rows with 32-byte loads when W1 is 32-byte aligned and
     with 16-byte loads otherwise: a W1 at a 16-byte offset gives bit-identical proposals and
-    residual draws."""
-    R, gamma, V, rank = 200, 4, 4104, 256
+    residual draws. At R = 600 the CTAs' unit ranges cross row-block pairs, so the gather of a
+    CTA's later pair (16-byte loads either way) runs too."""
+    gamma, rank = 4, 256
     wl = W.markov_rejection("cuda", R=R, gamma=gamma, V=V, rank=rank, seed=77, temperature=1.0)
     buf = torch.empty(V * rank + 8, dtype=wl.W1.dtype, device="cuda")
     W1_off = buf[8:].view(V, rank)
