@@ -53,7 +53,7 @@ constexpr long long kSpinCycles = 4000000000LL;  // ~2 s at the maximum SM clock
 constexpr uint32_t kBoxBytes = kBM * 128;         // one TMA box: 128 rows x 64 columns (bf16)
 
 // Per pass mode. Shared memory (A lives in tensor memory):
-//   MODE_STATS:          B 2 x 64 KB + U 3 x 32 KB             = 224 KB; TMEM 2 x 128 + 2 x 128 cols
+//   MODE_STATS:          B 2 x 64 KB + U 2 x 32 KB             = 192 KB; TMEM 2 x 128 + 2 x 128 cols
 //   MODE_TV, MODE_RESID: B 1 x 64 KB + (U + T) 2 x 2 x 32 KB   = 192 KB; TMEM 2 x 128 + 2 x 128
 // N = 128 columns everywhere. The pair passes read two logit tensors; a row piece of 256 bytes
 // costs little more HBM time than one of 128 bytes, so they take the wide tile at the price of
