@@ -74,7 +74,9 @@ bool trace_active() {
 namespace {
 
 constexpr size_t kAlign = 256;
-constexpr size_t kHeader = 256;
+constexpr size_t kHeader = 256;                        // status word + spare
+constexpr size_t kFixed = kSyncOffset + kSyncBytes;    // header + persistent-proposal counters
+static_assert(kSyncOffset >= kHeader, "counters after the header");
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 int cdiv(long long a, long long b) { return (int)((a + b - 1) / b); }
@@ -96,7 +98,14 @@ size_t partial_entries(int op, int R, int gamma, int V, int rank) {
   const size_t tgt = tr * stream_nseg(V);
   size_t e = 0;
   switch (op) {
-    case SPEC_OP_PROPOSE: e = (size_t)R * (rank > 0 ? 1 : gamma) * seg_draft; break;
+    case SPEC_OP_PROPOSE:
+      e = (size_t)R * (rank > 0 ? 1 : gamma) * seg_draft;
+      // the persistent proposal: 64-column partials, then 2 coarse ones per tile range
+      if (rank > 0) {
+        const size_t pe = (size_t)R * (cdiv(V, 64) + 2 * kMaxPropGrid);
+        e = e > pe ? e : pe;
+      }
+      break;
     case SPEC_OP_VERIFY_GREEDY: e = tr; break;
     case SPEC_OP_TARGET_STATS: e = tgt; break;
     case SPEC_OP_VERIFY_REJECTION: e = tgt > (size_t)R * seg_draft ? tgt : (size_t)R * seg_draft; break;
@@ -118,7 +127,7 @@ Layout layout(int op, int R, int gamma, int V, int rank) {
     e = partial_entries(op, R, gamma, V, rank);
   }
   L.entries = e;
-  size_t off = kHeader;
+  size_t off = kFixed;
   L.pm = off; off = align_up(off + e * sizeof(float));
   L.ps = off; off = align_up(off + e * sizeof(float));
   L.pi = off; off = align_up(off + e * sizeof(int));
@@ -270,7 +279,8 @@ size_t spec_workspace_bytes(int op, int R, int gamma, int V, int rank) {
 int spec_workspace_init(void* ws, size_t ws_bytes, void* stream) {
   if (!ws || ws_bytes < kHeader || (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0)
     return SPEC_ERR_INVALID_ARG;
-  if (cudaMemsetAsync(ws, 0, kHeader, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+  const size_t n = ws_bytes < kFixed ? ws_bytes : kFixed;
+  if (cudaMemsetAsync(ws, 0, n, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return SPEC_ERR_CUDA;
   return SPEC_OK;
 }
@@ -286,23 +296,36 @@ int spec_device_status(void* ws, size_t ws_bytes, void* stream, uint32_t* status
   return SPEC_OK;
 }
 
+// The target normalisers of the fused proposal entry point when the proposal did not run as
+// one persistent launch: a streaming pass of their own after it.
+static int target_after(const void* target, float* target_stats, int dtype, float temperature,
+                        int R, int gamma, int V, const Ws& w, cudaStream_t s) {
+  if (target)
+    target_stats_pass(target, dtype, 1.0f / temperature, R, gamma, V, nullptr, target_stats, w, s);
+  return finish();
+}
+
 static int markov_propose_impl(const void* U, int u_dtype, const void* W1, const void* W2,
                                int w_dtype, int rank, const int32_t* anchors, const float* u_draft,
                                float temperature, int R, int gamma, int V, int32_t* draft_tokens,
                                float* draft_logp, float* draft_stats, void* ws, size_t ws_bytes,
-                               void* stream, const uint32_t* mask) {
+                               void* stream, const uint32_t* mask, const void* target = nullptr,
+                               float* target_stats = nullptr) {
   if (!sizes_ok(R, gamma, V) || rank < 0 || rank > 1024) return SPEC_ERR_INVALID_ARG;
   if (!dtype_ok(u_dtype) || (rank > 0 && !dtype_ok(w_dtype))) return SPEC_ERR_UNSUPPORTED_DTYPE;
   if (!(temperature >= 0.0f) || !isfinite(temperature)) return SPEC_ERR_INVALID_ARG;
   Layout L;
   int rc = check_ws(ws, ws_bytes, SPEC_OP_PROPOSE, R, gamma, V, rank, &L);
   if (rc != SPEC_OK) return rc;
-  if (R == 0 || gamma == 0) return SPEC_OK;
+  if (target && (!target_stats || !(temperature > 0.0f))) return SPEC_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const Ws w = carve(ws, L);
+  if (R == 0) return SPEC_OK;
+  if (gamma == 0)  // nothing to propose; the window is the bonus row alone
+    return target_after(target, target_stats, u_dtype, temperature, R, gamma, V, w, s);
   if (!U || !draft_tokens) return SPEC_ERR_INVALID_ARG;
   if (rank > 0 && (!W1 || !W2 || !anchors)) return SPEC_ERR_INVALID_ARG;
   const bool greedy = u_draft == nullptr || temperature == 0.0f;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const Ws w = carve(ws, L);
 
   RowJob j;
   memset(&j, 0, sizeof j);
@@ -346,6 +369,17 @@ static int markov_propose_impl(const void* U, int u_dtype, const void* W1, const
                            grid_for((long long)j.rows * nseg, 1), s);
     j.pdl = 1;
     launch_select(j, u_dtype, wdt, kStreamSeg, nseg, w.pm, w.ps, greedy ? w.pi : nullptr, o, s);
+    return target_after(target, target_stats, u_dtype, temperature, R, gamma, V, w, s);
+  }
+  // bf16 weights on the tensor cores: every position, selects included, in one persistent
+  // launch that pipelines the positions of different request groups
+  if (markov_propose_tc_supported(u_dtype, wdt, rank, R, gamma, V, U, W1, W2)) {
+    o.w1 = aligned16(W1) && (rank * (int)esize(wdt)) % 16 == 0 ? W1 : nullptr;
+    o.w1_row_bytes = rank * (int)esize(wdt);
+    uint32_t* sync = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + kSyncOffset);
+    if (launch_markov_propose_tc(j, o, w.pm, w.ps, greedy ? w.pi : nullptr, greedy, sync, s,
+                                 target, target_stats, 1.0f / temperature) != cudaSuccess)
+      return SPEC_ERR_CUDA;
     return finish();
   }
   // every launch after the first is chained to the one before it
@@ -370,7 +404,7 @@ static int markov_propose_impl(const void* U, int u_dtype, const void* W1, const
     j.pdl = 1;
     launch_select(j, u_dtype, wdt, seg, nseg, w.pm, w.ps, greedy ? w.pi : nullptr, o, s);
   }
-  return finish();
+  return target_after(target, target_stats, u_dtype, temperature, R, gamma, V, w, s);
 }
 
 static int verify_greedy_impl(const void* target, int t_dtype, const int32_t* draft_tokens,
@@ -695,6 +729,18 @@ int spec_markov_propose_masked(const void* U, int u_dtype, const void* W1, const
   return markov_propose_impl(U, u_dtype, W1, W2, w_dtype, rank, anchors, u_draft, temperature, R,
                              gamma, V, draft_tokens, draft_logp, draft_stats, ws, ws_bytes,
                              stream, allowed);
+}
+
+int spec_markov_propose_target_stats(const void* U, int l_dtype, const void* W1, const void* W2,
+                                     int w_dtype, int rank, const int32_t* anchors,
+                                     const float* u_draft, float temperature, int R, int gamma,
+                                     int V, int32_t* draft_tokens, float* draft_logp,
+                                     float* draft_stats, const void* target, float* target_stats,
+                                     void* ws, size_t ws_bytes, void* stream) {
+  if (!target) return SPEC_ERR_INVALID_ARG;
+  return markov_propose_impl(U, l_dtype, W1, W2, w_dtype, rank, anchors, u_draft, temperature, R,
+                             gamma, V, draft_tokens, draft_logp, draft_stats, ws, ws_bytes,
+                             stream, nullptr, target, target_stats);
 }
 
 int spec_verify_rejection(const void* target, const void* U, int l_dtype, const void* W1,

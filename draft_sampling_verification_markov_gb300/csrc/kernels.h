@@ -1,6 +1,7 @@
 // kernels.h -- host-side launchers of the libspecmarkov kernels (internal to the library).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -77,6 +78,29 @@ bool markov_tc_supported(int udt, int wdt, int rank, int V, const void* U, const
                          const void* W1, const void* W2);
 cudaError_t launch_markov_tc(const RowJob& j, float* pm, float* ps, int* pi, bool argmax,
                              cudaStream_t s);
+// The whole Markov proposal (all positions, selects included) in one persistent tcgen05 launch
+// (markov_propose.cu); `sync` is the workspace's counter area, zero on entry and on return.
+bool markov_propose_tc_supported(int udt, int wdt, int rank, int R, int gamma, int V,
+                                 const void* U, const void* W1, const void* W2);
+// With `target` (bf16 [R * (gamma + 1), V]) the same launch also writes the target rows'
+// softmax normalisers (m, log Z) of target * tscale into tstats.
+cudaError_t launch_markov_propose_tc(const RowJob& j, const SelectOut& o, float* pm, float* ps,
+                                     int* pi, bool argmax, uint32_t* sync, cudaStream_t s,
+                                     const void* target = nullptr, float* tstats = nullptr,
+                                     float tscale = 1.0f);
+// Workspace bytes [kSyncOffset, kSyncOffset + kSyncBytes): inter-CTA counters of the persistent
+// proposal, at a fixed place whatever the problem size, zeroed by spec_workspace_init.
+constexpr size_t kSyncOffset = 256;
+constexpr size_t kSyncBytes = 8192;
+// CTAs of the persistent proposal at most (the coarse partials of its select, two per CTA and
+// row, are sized for this many).
+constexpr int kMaxPropGrid = 256;
+// A 2-D or 3-D bf16 tensor map with a 128-byte swizzle (false if it cannot be encoded).
+bool make_tensor_map_bf16(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
+                          const cuuint64_t* strides_bytes, const cuuint32_t* box);
+// Consume the test request that makes the next tensor-core launch never load its first W2
+// tile (spec_test_stall_next_markov).
+int take_stall_request();
 // Vocabulary columns per partial written by the tcgen05 producer in pass mode `mode`.
 int markov_tc_seg(int mode);
 // Smallest partial segment any Markov producer writes (sizes the workspace).

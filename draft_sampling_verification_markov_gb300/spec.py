@@ -66,6 +66,8 @@ def lib():
         L.spec_verify_greedy_noalloc.argtypes = [vp, i, vp, vp, i, i, i, vp, vp, vp, vp, vp]
         L.spec_markov_propose_masked.argtypes = [vp, i, vp, vp, i, i, vp, vp, f, i, i, i, vp, vp,
                                                  vp, vp, vp, sz, vp]
+        L.spec_markov_propose_target_stats.argtypes = [vp, i, vp, vp, i, i, vp, vp, f, i, i, i,
+                                                       vp, vp, vp, vp, vp, vp, sz, vp]
         L.spec_verify_rejection_masked.argtypes = [vp, vp, i, vp, vp, i, i, vp, vp, vp, vp, vp,
                                                    vp, vp, f, vp, i, i, i, vp, vp, vp, vp, vp,
                                                    sz, vp]
@@ -87,6 +89,7 @@ def lib():
                      "spec_tv_confidence", "spec_schedule_prefix", "spec_schedule_topk",
                      "spec_verify_greedy_noalloc", "spec_markov_propose_masked",
                      "spec_verify_rejection_masked", "spec_tv_confidence_masked",
+                     "spec_markov_propose_target_stats",
                      "spec_flat_layout", "spec_target_stats_flat", "spec_verify_greedy_flat",
                      "spec_verify_rejection_flat"):
             getattr(L, name).restype = i
@@ -222,6 +225,35 @@ def spec_markov_propose(U, W1, W2, anchors, u_draft, temperature, *, rank=None,
                                               _stream(stream))
     _check("spec_markov_propose", rc)
     return draft_tokens, draft_logp, draft_stats
+
+
+def spec_markov_propose_target_stats(U, W1, W2, anchors, u_draft, temperature, target, *,
+                                     rank=None, draft_tokens=None, draft_logp=None,
+                                     draft_stats=None, target_stats=None, workspace=None,
+                                     stream=None):
+    """Draft proposal plus the target normalisers of the same window in one call. Returns
+    (draft_tokens [R,g] int32, draft_logp [R,g] fp32, draft_stats [R,g,2],
+    target_stats [R*(g+1), 2] fp32)."""
+    R, gamma, V = U.shape
+    rank = _rank_of(W1, rank)
+    dev = U.device
+    if draft_tokens is None:
+        draft_tokens = torch.empty(R, gamma, dtype=torch.int32, device=dev)
+    if draft_logp is None:
+        draft_logp = torch.empty(R, gamma, dtype=torch.float32, device=dev)
+    if draft_stats is None:
+        draft_stats = torch.empty(R, gamma, 2, dtype=torch.float32, device=dev)
+    if target_stats is None:
+        target_stats = torch.empty(R * (gamma + 1), 2, dtype=torch.float32, device=dev)
+    ws = workspace or default_workspace(dev)
+    wp, wn = ws.for_op(SPEC_OP_PROPOSE, R, gamma, V, rank, stream)
+    wdt = _dt(W1) if W1 is not None else SPEC_BF16
+    rc = lib().spec_markov_propose_target_stats(
+        _ptr(U), _dt(U), _ptr(W1), _ptr(W2), wdt, rank, _ptr(anchors), _ptr(u_draft),
+        float(temperature), R, gamma, V, _ptr(draft_tokens), _ptr(draft_logp), _ptr(draft_stats),
+        _ptr(target), _ptr(target_stats), wp, wn, _stream(stream))
+    _check("spec_markov_propose_target_stats", rc)
+    return draft_tokens, draft_logp, draft_stats, target_stats
 
 
 def spec_verify_greedy(target, draft_tokens, lengths=None, *, accept_len=None, out_tokens=None,

@@ -132,6 +132,29 @@ int spec_markov_propose(const void* U, int u_dtype, const void* W1, const void* 
                         void* stream);
 
 /*
+ * Draft proposal and the target normalisers of the same window in one call.
+ * Defines: as spec_markov_propose followed by spec_target_stats(target, l_dtype, temperature,
+ *   R * (gamma + 1), V, target_stats): the proposal of "[DeepSeek-6] DSpark", sections 3-4, and
+ *   the p_t normalisers that its rejection verification (section 9) needs.
+ * The target normalisers do not depend on the proposal. With bf16 weights on the tensor cores
+ * the proposal runs as one persistent launch whose positions leave HBM partly idle; a share of
+ * its CTAs streams the target rows meanwhile, so the two cost about as much time as the
+ * proposal alone. Other shapes run the two operations one after the other.
+ * Arguments: as spec_markov_propose (U of dtype l_dtype), plus
+ *   target       [R, gamma+1, V] target logits, dtype l_dtype (required).
+ *   target_stats [R*(gamma+1), 2] fp32 output (m, log Z) of softmax(target[row,:] / T), for
+ *                spec_verify_rejection's target_stats.
+ *   temperature  > 0 (the normalisers are those of the tempered target).
+ * Errors as spec_markov_propose; SPEC_ERR_INVALID_ARG for a NULL target or target_stats.
+ */
+int spec_markov_propose_target_stats(const void* U, int l_dtype, const void* W1, const void* W2,
+                                     int w_dtype, int rank, const int32_t* anchors,
+                                     const float* u_draft, float temperature, int R, int gamma,
+                                     int V, int32_t* draft_tokens, float* draft_logp,
+                                     float* draft_stats, const void* target, float* target_stats,
+                                     void* ws, size_t ws_bytes, void* stream);
+
+/*
  * Greedy verification with a bonus token.
  * Defines: "DeepSeek-V4 MTP/NextN 怎样逐步生成候选", sections 三-四 (verify window
  *   [bonus, d1..d_gamma]; all accepted -> gamma drafts + one new bonus; first mismatch -> one

@@ -56,7 +56,9 @@ def test_trace_events_time_markov_launches(spec, captured):
         torch.cuda.synchronize()
     finally:
         spec.lib().spec_trace_events(0, None, None, 0)
-    assert count == 3                                # one Markov launch per position
+    # bf16 weights on the tensor cores: the whole proposal (three positions, two request
+    # groups) is one persistent launch
+    assert count == 1
     times = [b[i].elapsed_time(e[i]) for i in range(count)]
     assert all(t > 0 for t in times)
     assert ws.status() == 0
