@@ -33,6 +33,10 @@ sys.path.insert(0, ROOT)
 METRIC = "draft+verify logit rows/s at V=129280, R=256 (HBM GB/s, % of peak)"
 UNIT = "rows/s"
 WORKLOAD = dict(R=256, gamma=7, V=129280, rank=256, temperature=1.0, seed=1003)
+# timed regions of K steps each; `value` is their median
+REPEATS = 5
+# the step's proposal and target normalisers in one call (spec_markov_propose_target_stats)
+FUSED = False
 
 
 def parse_args():
@@ -91,6 +95,17 @@ def algorithmic_bytes_per_step():
     """What one step must touch: U and the target read once, W2 read once, W1 row gathers."""
     R, g, V, r = (WORKLOAD[k] for k in ("R", "gamma", "V", "rank"))
     return 2 * (R * g * V + R * (g + 1) * V + V * r + R * g * r)
+
+
+def class_bytes_per_launch():
+    """Algorithmic bytes of one launch of each kernel class in the step (bf16 everywhere):
+    the persistent proposal reads U, W2 and the gathered W1 rows (and, in the fused entry point,
+    the target); the residual pass reads each request's final U and target rows, W2 and W1 rows;
+    the target normalisers read the target; selects and scans read only partials."""
+    R, g, V, r = (WORKLOAD[k] for k in ("R", "gamma", "V", "rank"))
+    propose = 2 * (R * g * V + V * r + R * g * r) + (2 * R * (g + 1) * V if FUSED else 0)
+    return {4: propose, 0: 2 * (2 * R * V + V * r + R * r), 1: 2 * R * (g + 1) * V,
+            2: 8 * R * ((V + 63) // 64), 3: 0}
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -183,20 +198,50 @@ def recorded_traffic(kernel_class):
 # ----------------------------------------------------------------------------- CPU baseline
 
 def cpu_baseline_run(wl_host, n_req):
-    """Time the oracle (propose + rejection verify) on the first n_req requests."""
+    """Time the oracle (propose + rejection verify) on the first n_req requests. Returns
+    (rows/s, seconds, proposal, verification) with the oracle's outputs."""
     import oracle
     sl = lambda t: None if t is None else t[:n_req]
     t0 = time.perf_counter()
     ref = oracle.markov_propose(sl(wl_host["U"]), wl_host["W1"], wl_host["W2"],
                                 sl(wl_host["anchors"]), sl(wl_host["u_draft"]),
                                 WORKLOAD["temperature"])
-    oracle.verify_rejection(sl(wl_host["target"]), sl(wl_host["U"]), wl_host["W1"],
-                            wl_host["W2"], sl(wl_host["anchors"]), ref["tokens"],
-                            sl(wl_host["u_accept"]), sl(wl_host["u_resid"]),
-                            WORKLOAD["temperature"])
+    rv = oracle.verify_rejection(sl(wl_host["target"]), sl(wl_host["U"]), wl_host["W1"],
+                                 wl_host["W2"], sl(wl_host["anchors"]), ref["tokens"],
+                                 sl(wl_host["u_accept"]), sl(wl_host["u_resid"]),
+                                 WORKLOAD["temperature"])
     dt = time.perf_counter() - t0
     rows = n_req * (2 * WORKLOAD["gamma"] + 1)
-    return rows / dt, dt
+    return rows / dt, dt, ref, rv
+
+
+def parity_summary(ref, rv, toks, n_acc, out, margin=1e-6):
+    """The GPU step's outputs against the oracle's on the same requests (the tests' rule): a
+    request's proposals must be identical unless, where they first differ, the oracle's CDF
+    margin is below `margin`; the verification of a request with identical proposals must be
+    identical unless an acceptance ratio or the final draw lies within `margin` of its uniform.
+    Mismatches outside these margins are counted, not hidden."""
+    import numpy as np
+    rt = ref["tokens"]
+    same = (toks == rt).all(axis=1)
+    margin_cases = 0
+    outside = 0
+    for r in np.nonzero(~same)[0]:
+        k = int(np.argmax(toks[r] != rt[r]))
+        if ref["margin"][r, k] < margin:
+            margin_cases += 1
+        else:
+            outside += 1
+    amb = (np.nan_to_num(rv["accept_margin"], nan=1.0) < margin).any(axis=1)
+    amb |= rv["resid_margin"] < margin
+    diff = (n_acc != rv["accept_len"]) | (out != rv["out_tokens"]).any(axis=1)
+    return {"requests_compared": int(len(rt)), "proposals_exact": int(same.sum()),
+            "margin_cases": margin_cases, "verify_exact": int((same & ~diff).sum()),
+            "verify_margin_cases": int((same & diff & amb).sum()),
+            "mismatches_outside_margin": outside + int((same & diff & ~amb).sum()),
+            "margin": margin,
+            "rule": "tokens, accept lengths and emitted tokens identical to the fp64 oracle except "
+                    "at a CDF or acceptance margin below 1e-6"}
 
 
 def host_sample(n_req, device):
@@ -223,7 +268,7 @@ def run_reference(args):
     n_req = max(1, min(WORKLOAD["R"], threads))
     wl = host_sample(n_req, "cpu")
     for _ in range(args.warmup):
-        cpu_baseline_run(wl, n_req)
+        cpu_baseline_run(wl, n_req)[:2]
     times = []
     for _ in range(args.steps):
         times.append(cpu_baseline_run(wl, n_req)[1])
@@ -251,6 +296,7 @@ def run_reference(args):
 def graph_ms(run, stream, reps=5, warm=2):
     """Milliseconds per replay of `run` captured as one CUDA graph on `stream`."""
     import torch
+    stream.wait_stream(torch.cuda.current_stream())  # inputs drawn on the current stream
     with torch.cuda.stream(stream):
         run()
     torch.cuda.synchronize()
@@ -406,6 +452,7 @@ def main():
     R, g, V = W["R"], W["gamma"], W["V"]
     T = W["temperature"]
     stream = torch.cuda.Stream(device=dev)
+    stream.wait_stream(torch.cuda.current_stream(dev))  # the inputs are drawn on that stream
     ws = spec.Workspace(device=dev)
     for op in range(6):
         ws.for_op(op, R, g, V, W["rank"], stream)
@@ -418,9 +465,16 @@ def main():
     nxt = torch.empty(R, dtype=torch.int32, device=dev)
 
     def step(U, target, anchors, u_draft, u_acc, u_res):
-        spec.spec_markov_propose(U, wl.W1, wl.W2, anchors, u_draft, T, draft_tokens=toks,
-                                 draft_logp=logp, draft_stats=dstats, workspace=ws, stream=stream)
-        spec.spec_target_stats(target, T, stats=tstats, workspace=ws, stream=stream)
+        if FUSED:
+            spec.spec_markov_propose_target_stats(U, wl.W1, wl.W2, anchors, u_draft, T, target,
+                                                  draft_tokens=toks, draft_logp=logp,
+                                                  draft_stats=dstats, target_stats=tstats,
+                                                  workspace=ws, stream=stream)
+        else:
+            spec.spec_markov_propose(U, wl.W1, wl.W2, anchors, u_draft, T, draft_tokens=toks,
+                                     draft_logp=logp, draft_stats=dstats, workspace=ws,
+                                     stream=stream)
+            spec.spec_target_stats(target, T, stats=tstats, workspace=ws, stream=stream)
         spec.spec_verify_rejection(target, U, wl.W1, wl.W2, anchors, toks, logp, dstats, u_acc,
                                    u_res, T, target_stats=tstats, accept_len=n_acc,
                                    out_tokens=out, next_anchor=nxt, workspace=ws, stream=stream)
@@ -443,38 +497,50 @@ def main():
             graph.replay()
     torch.cuda.synchronize()
 
-    # timed region: K replays of the step, no per-launch instrumentation
+    # timed regions: REPEATS times K replays of the step, no per-launch instrumentation; each
+    # region is bracketed by a barrier and a synchronisation and timed with CUDA events on the
+    # launch stream; `value` is the median region, its spread reported beside it
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    if pg:
-        pg.barrier()
-    torch.cuda.synchronize()
+    region_ms = []
     w0 = time.time()
-    t_start.record(stream)
-    with torch.cuda.stream(stream):
-        for _ in range(args.steps):
-            graph.replay()
-    t_end.record(stream)
-    torch.cuda.synchronize()
+    for _ in range(REPEATS):
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        if pg:
+            pg.barrier()
+        torch.cuda.synchronize()
+        t_start.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(args.steps):
+                graph.replay()
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        if pg:
+            pg.barrier()
+        region_ms.append(max_over_ranks(t_start.elapsed_time(t_end), pg, dev))
     w1 = time.time()
-    if pg:
-        pg.barrier()
     time.sleep(0.15)
     sampler.stop()
     launches = launches_per_step * args.steps
-    ms = max_over_ranks(t_start.elapsed_time(t_end), pg, dev)
+    ms = sorted(region_ms)[len(region_ms) // 2]
     assert ws.status() == 0, "device status word set during the timed region"
+    # the step's outputs (every replay computes the same ones), for the parity check below
+    gpu_out = {"tokens": toks.cpu().numpy(), "accept_len": n_acc.cpu().numpy(),
+               "out_tokens": out.cpu().numpy()}
     rows_per_step = R * (2 * g + 1)
     value = whole_job_rate(rows_per_step, args.steps, world, ms)
+    spread = {"regions": REPEATS, "steps_per_region": args.steps,
+              "value_min": whole_job_rate(rows_per_step, args.steps, world, max(region_ms)),
+              "value_max": whole_job_rate(rows_per_step, args.steps, world, min(region_ms)),
+              "ms_per_step_regions": [x / args.steps for x in region_ms]}
 
     # per-class launch durations, live: the same step captured with caller-owned CUDA events
     # around every library launch (on the launch stream), replayed and read back replay by
     # replay. The events cost about 15 % of a step, so they stay out of the region above.
     import ctypes
-    caps = {0: g + 1, 1: 1, 2: g + 1, 3: 2}   # launches per step and class
+    caps = {kc: g + 2 for kc in range(5)}   # at most this many launches per step and class
     ev, keep = {}, []
     for kc, cap in caps.items():
         b = [torch.cuda.Event(enable_timing=True) for _ in range(cap)]
@@ -491,16 +557,16 @@ def main():
     graph_ev = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph_ev, stream=stream):
         step(*inputs)
-    counts = {kc: spec.lib().spec_trace_count(kc) for kc in range(4)}
-    for kc in range(4):
+    counts = {kc: spec.lib().spec_trace_count(kc) for kc in range(5)}
+    for kc in range(5):
         spec.lib().spec_trace_events(kc, None, None, 0)
     n_prof = max(1, min(args.steps, 50))
-    totals = {kc: [0.0, 0] for kc in range(4)}
+    totals = {kc: [0.0, 0] for kc in range(5)}
     for _ in range(n_prof):
         with torch.cuda.stream(stream):
             graph_ev.replay()
         stream.synchronize()
-        for kc in range(4):
+        for kc in range(5):
             b, e = ev[kc]
             for i in range(counts[kc]):
                 totals[kc][0] += b[i].elapsed_time(e[i])
@@ -509,11 +575,11 @@ def main():
     totals = {kc: (v[0] * args.steps / n_prof, v[1] * args.steps / n_prof)
               for kc, v in totals.items()}
     dom = max(totals, key=lambda k: totals[k][0])
-    names = {0: "markov_producer", 1: "stream_rows", 2: "select", 3: "other"}
-    per_unit = algorithmic_bytes_per_step() / rows_per_step
-    units_per_launch = {0: R, 1: R * (g + 1), 2: R, 3: R}
+    names = {0: "markov_producer", 1: "stream_rows", 2: "select", 3: "other",
+             4: "persistent_proposal"}
+    bytes_per_launch = class_bytes_per_launch()
     dur_s = totals[dom][0] / max(totals[dom][1], 1) / 1e3
-    achieved = per_unit * units_per_launch[dom] / dur_s / 1e9
+    achieved = bytes_per_launch[dom] / dur_s / 1e9
     peaks = {}
     try:
         peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
@@ -528,10 +594,13 @@ def main():
                 "step_hbm_frac": algorithmic_bytes_per_step() * args.steps / (ms / 1e3) / 1e9 / peak,
                 "step_hbm_frac_of_8tbs_nominal":
                     algorithmic_bytes_per_step() * args.steps / (ms / 1e3) / 1e9 / 8000.0,
-                "class_ms_per_step": {names[k]: totals[k][0] / args.steps for k in totals}}
-    # the W2 projection of the Markov class on the tensor pipe: 2 * R * rank * V flops per
-    # launch (gamma proposal positions + the residual pass), against the bf16 dense peak
-    mk = totals[0]
+                "class_ms_per_step": {names[k]: totals[k][0] / args.steps for k in totals},
+                "algorithmic_bytes_per_launch": bytes_per_launch[dom],
+                "class_launches_per_step": {names[k]: totals[k][1] / args.steps
+                                            for k in totals}}
+    # the W2 projection on the tensor pipe: 2 * R * rank * V flops per position (gamma in the
+    # persistent proposal, one in the residual pass), against the bf16 dense peak
+    mk = (totals[0][0] + totals[4][0], totals[0][1] + totals[4][1] * g)
     if mk[1] > 0:
         flops = 2.0 * R * W["rank"] * V * mk[1]
         # timed inside a long step: the sustained figure
@@ -539,8 +608,9 @@ def main():
         tf = flops / (mk[0] / 1e3) / 1e12
         roofline["w2_projection"] = {"bound": "tensor", "achieved": tf, "peak": bf16,
                                      "unit": "TFLOP/s", "frac": tf / bf16,
-                                     "note": "flops over the Markov class's launch time; the "
-                                             "class is not tensor-bound"}
+                                     "note": "flops over the tensor-core launches' time (the "
+                                             "persistent proposal and the residual pass); "
+                                             "they are not tensor-bound"}
 
     # end to end through the C ABI from pinned host buffers (weights stay resident): every step
     # copies its inputs host -> device and reads its outputs back. Two device input buffers let
@@ -599,6 +669,7 @@ def main():
                        "this host link), overlapped with the previous step's compute"}
 
     cpu = None
+    parity = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
         oracle.build()
@@ -609,8 +680,11 @@ def main():
                 for k, v in wl.tensors().items()}
         dt, reps = 0.0, 0
         while reps < 4 and (reps == 0 or dt < 10.0):
-            dt += cpu_baseline_run(wl_h, n_req)[1]
+            _, t_run, ref_p, ref_v = cpu_baseline_run(wl_h, n_req)
+            dt += t_run
             reps += 1
+        parity = parity_summary(ref_p, ref_v, gpu_out["tokens"], gpu_out["accept_len"],
+                                gpu_out["out_tokens"])
         v_cpu = reps * n_req * (2 * g + 1) / dt
         cpu = {"value": v_cpu, "unit": UNIT, "cores": min(threads, n_req), "kind": "oracle",
                "host_cores_available": len(os.sched_getaffinity(0)),
@@ -631,6 +705,7 @@ def main():
                                                  "replays without per-launch events; launch "
                                                  "durations from a replayed capture with "
                                                  "events around each library launch"}),
+                "timing_spread": spread, "parity": parity,
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": int(launches), "clocks": clocks,
                 "tokens_per_s": float(n_acc.sum().item() + R) * args.steps * world / (ms / 1e3),

@@ -1026,7 +1026,7 @@ cudaError_t launch_markov_propose_tc(const RowJob& j, const SelectOut& o, float*
                                      int* pi, bool argmax, uint32_t* sync, cudaStream_t s,
                                      const void* target, float* tstats, float tscale) {
   using namespace prop;
-  TraceScope ts(SPEC_KCLASS_MARKOV, s);
+  TraceScope ts(SPEC_KCLASS_PROPOSE, s);
   Params p;
   memset(&p, 0, sizeof p);
   p.j = j;

@@ -21,6 +21,8 @@ SPEC_F32, SPEC_BF16 = 0, 1
 (SPEC_DEV_BAD_TOKEN, SPEC_DEV_NONFINITE, SPEC_DEV_EMPTY_RESIDUAL, SPEC_DEV_BAD_LENGTH,
  SPEC_DEV_TIMEOUT) = 1, 2, 4, 8, 16
 SPEC_SCHEDULE_MAX_CANDIDATES = 16384
+(SPEC_KCLASS_MARKOV, SPEC_KCLASS_STREAM, SPEC_KCLASS_SELECT, SPEC_KCLASS_OTHER,
+ SPEC_KCLASS_PROPOSE) = range(5)
 SPEC_NOALLOC_MAX_ROWS = 65536
 SPEC_ERR_TOO_LARGE = -7
 

@@ -412,13 +412,15 @@ int spec_test_stall_next_markov(void);
  * Kernel classes: SPEC_KCLASS_MARKOV (the Markov producer: tensor-core GEMM fused with the
  * softmax / residual / TV epilogue, or its CUDA-core form), SPEC_KCLASS_STREAM (rank-0 streaming
  * row reductions), SPEC_KCLASS_SELECT (per-row select / sample), SPEC_KCLASS_OTHER (scans,
- * finalisers, the scheduler).
+ * finalisers, the scheduler), SPEC_KCLASS_PROPOSE (the persistent tensor-core proposal: every
+ * position with its selects, and the target normalisers of the fused entry point).
  */
 #define SPEC_KCLASS_MARKOV 0
 #define SPEC_KCLASS_STREAM 1
 #define SPEC_KCLASS_SELECT 2
 #define SPEC_KCLASS_OTHER 3
-#define SPEC_KCLASS_COUNT 4
+#define SPEC_KCLASS_PROPOSE 4
+#define SPEC_KCLASS_COUNT 5
 
 /* Number of kernels this process has launched through the library (all classes). */
 unsigned long long spec_launch_count(void);

@@ -32,3 +32,23 @@ def orc():
     import oracle
     oracle.build()
     return oracle
+
+
+def pytest_terminal_summary(terminalreporter):
+    """One line with the session's parity totals against the oracle (gpu_util.PARITY), and the
+    same as JSON in $SPEC_PARITY_JSON when that is set."""
+    try:
+        from gpu_util import PARITY
+    except ImportError:
+        return
+    if not (PARITY["proposal_requests"] or PARITY["verify_requests"]):
+        return
+    terminalreporter.write_line(
+        "parity vs oracle: proposals {proposal_exact}/{proposal_requests} requests identical, "
+        "{proposal_margin_cases} CDF-margin cases; verify {verify_exact}/{verify_requests} "
+        "identical, {verify_margin_cases} margin cases".format(**PARITY))
+    path = os.environ.get("SPEC_PARITY_JSON")
+    if path:
+        import json
+        with open(path, "w") as f:
+            json.dump(PARITY, f)

@@ -11,6 +11,14 @@ LOG_TOL = 1e-5
 CONF_RTOL, CONF_ATOL = 1e-5, 1e-7
 
 
+# Session totals of every comparison with the oracle (printed in the test summary, see
+# conftest.py): requests compared, requests identical to the oracle, and the mismatches the
+# margin rule allowed (sampled draft tokens whose oracle CDF margin is below MARGIN; acceptance
+# decisions within MARGIN of the ratio or final draws below MARGIN, on the verify side).
+PARITY = {"proposal_requests": 0, "proposal_exact": 0, "proposal_margin_cases": 0,
+          "verify_requests": 0, "verify_exact": 0, "verify_margin_cases": 0}
+
+
 def to_dev(wl, dev):
     return {k: v.to(dev) for k, v in wl.tensors().items()}
 
@@ -47,7 +55,35 @@ def compare_proposals(gpu_tokens, gpu_logp, gpu_stats, ref, greedy=False, report
         assert dn.size == 0 or dn.max() <= LOG_TOL, f"log-normaliser differs by {dn.max():.3e}"
     if report is not None:
         report["margin_mismatches"] = report.get("margin_mismatches", 0) + n_margin
+    PARITY["proposal_requests"] += int(same.size)
+    PARITY["proposal_exact"] += int(same.sum())
+    PARITY["proposal_margin_cases"] += n_margin
     return same
+
+
+def compare_verify(accept_len, out_tokens, next_anchor, rv, same=None, report=None):
+    """Compare rejection-verification outputs with the oracle's, request by request. A request
+    whose proposals differ from the oracle's (`same` False) is not compared; the others must
+    agree exactly unless the oracle's acceptance ratio or final draw lies within MARGIN of the
+    uniform (counted). Returns the number of requests compared."""
+    gn, go = np.asarray(accept_len), np.asarray(out_tokens)
+    gx = None if next_anchor is None else np.asarray(next_anchor)
+    R = gn.shape[0]
+    same = np.ones(R, bool) if same is None else np.asarray(same)
+    amb = (np.nan_to_num(rv["accept_margin"], nan=1.0) < MARGIN).any(axis=1)
+    amb |= rv["resid_margin"] < MARGIN
+    diff = (gn != rv["accept_len"]) | (go != rv["out_tokens"]).any(axis=1)
+    if gx is not None:
+        diff |= gx != rv["next_anchor"]
+    bad = same & diff & ~amb
+    assert not bad.any(), f"verify differs for requests {np.nonzero(bad)[0][:10]}"
+    n_margin = int((same & diff & amb).sum())
+    if report is not None:
+        report["verify_margin_cases"] = report.get("verify_margin_cases", 0) + n_margin
+    PARITY["verify_requests"] += int(same.sum())
+    PARITY["verify_exact"] += int((same & ~diff).sum())
+    PARITY["verify_margin_cases"] += n_margin
+    return int(same.sum())
 
 
 def assert_conf_close(gpu, ref, what="confidence"):

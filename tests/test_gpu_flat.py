@@ -11,7 +11,7 @@ import torch
 
 import oracle
 from draft_sampling_verification_markov_gb300 import workloads as W
-from gpu_util import compare_proposals, to_dev
+from gpu_util import compare_proposals, compare_verify, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -137,11 +137,7 @@ def test_rejection_flat_matches_padded_and_oracle(spec, ws, R, gamma, V, rank, w
     rv = oracle.verify_rejection(wl.target, wl.U, wl.W1, wl.W2, wl.anchors, toks.cpu(),
                                  wl.u_accept, wl.u_resid, 0.8, lengths, rank=rank)
     gn, go, gx = n.cpu().numpy(), out.cpu().numpy(), nxt.cpu().numpy()
-    amb = (np.nan_to_num(rv["accept_margin"], nan=1.0) < 1e-6).any(axis=1)
-    amb |= rv["resid_margin"] < 1e-6
-    diff = (gn != rv["accept_len"]) | (go != rv["out_tokens"]).any(axis=1) | (
-        gx != rv["next_anchor"])
-    assert not (diff & ~amb).any(), f"verify differs for requests {np.nonzero(diff & ~amb)}"
+    compare_verify(gn, go, gx, rv)
     assert (gn <= lengths.numpy()).all()
     assert same.any()
 

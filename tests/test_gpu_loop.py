@@ -12,7 +12,7 @@ import torch
 
 import oracle
 from draft_sampling_verification_markov_gb300 import workloads as W
-from gpu_util import assert_conf_close, compare_proposals
+from gpu_util import assert_conf_close, compare_proposals, compare_verify
 
 pytestmark = pytest.mark.gpu
 
@@ -69,15 +69,10 @@ def check_iteration(lp, wl, t, sample=None, report=None):
     n = lp.accept_len[t][sample].cpu().numpy()
     o = lp.out_tokens[t][sample].cpu().numpy()
     nxt = lp.anchors[t + 1][sample].cpu().numpy()
-    amb = (np.nan_to_num(rv["accept_margin"], nan=1.0) < 1e-6).any(axis=1) | (
-        rv["resid_margin"] < 1e-6)
-    diff = (n != rv["accept_len"]) | (o != rv["out_tokens"]).any(axis=1) | (
-        nxt != rv["next_anchor"])
-    assert not (diff & ~amb).any(), f"iteration {t}: verify differs for {np.nonzero(diff & ~amb)}"
+    # the oracle ran on the GPU's own draft tokens, so every request is compared
+    compare_verify(n, o, nxt, rv, report=report)
     # the emitted token is the next anchor
     np.testing.assert_array_equal(nxt, o[np.arange(len(sample)), n])
-    if report is not None:
-        report["verify_margin_cases"] = report.get("verify_margin_cases", 0) + int((diff & amb).sum())
 
 
 @pytest.mark.parametrize("schedule", [True, False, "async"])
@@ -88,9 +83,8 @@ def test_loop_matches_oracle_iteration_by_iteration(spec, schedule):
     lp.run()
     torch.cuda.synchronize()
     assert lp.ws.status() == 0
-    report = {}
     for t in range(wl.iterations):
-        check_iteration(lp, wl, t, report=report)
+        check_iteration(lp, wl, t)
     if not schedule:
         assert (lp.accept_len <= wl.gamma).all()
 

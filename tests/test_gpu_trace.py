@@ -32,30 +32,31 @@ def _attach(spec, kclass, n, stream):
 
 
 @pytest.mark.parametrize("captured", [False, True])
-def test_trace_events_time_markov_launches(spec, captured):
+def test_trace_events_time_the_proposal_launch(spec, captured):
     wl = W.markov_rejection("cuda", R=130, gamma=3, V=4096, rank=128, seed=9)
     ws = spec.Workspace(device="cuda")
     stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())  # the inputs are drawn on the current stream
     run = lambda: spec.spec_markov_propose(wl.U, wl.W1, wl.W2, wl.anchors, wl.u_draft, 1.0,
                                            workspace=ws, stream=stream)
     run()                                           # sizes the workspace before any capture
     torch.cuda.synchronize()
-    b, e, keep = _attach(spec, spec.SPEC_KCLASS_MARKOV if hasattr(spec, "SPEC_KCLASS_MARKOV")
-                         else 0, 8, stream)
+    kc = spec.SPEC_KCLASS_PROPOSE
+    b, e, keep = _attach(spec, kc, 8, stream)
     try:
         if captured:
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
                 run()
-            count = spec.lib().spec_trace_count(0)
+            count = spec.lib().spec_trace_count(kc)
             with torch.cuda.stream(stream):
                 g.replay()
         else:
             run()
-            count = spec.lib().spec_trace_count(0)
+            count = spec.lib().spec_trace_count(kc)
         torch.cuda.synchronize()
     finally:
-        spec.lib().spec_trace_events(0, None, None, 0)
+        spec.lib().spec_trace_events(kc, None, None, 0)
     # bf16 weights on the tensor cores: the whole proposal (three positions, two request
     # groups) is one persistent launch
     assert count == 1
