@@ -183,13 +183,13 @@ __device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
 // Draft logits of columns [v0, v0 + n) (n <= 64) by the 128 threads of a select team, with the
 // previous token's W1 row staged in shared memory (w1s, rank / 8 chunks of 16 bytes): two
 // threads per column, thread `part` summing chunks part, part + 2, ... of the rank-256 dot
-// product in the canonical order, every W2 load of a thread in flight at once.
+// product in four independent chains, every W2 load of a thread in flight at once.
 __device__ __forceinline__ void rebuild_segment(const RowJob& j, const RowInfo& ri,
                                                 const uint4* w1s, int v0, int n, float* zs,
                                                 int tid, NamedBarrier wg) {
   const int col = tid >> 1, part = tid & 1, v = v0 + col;
   const int nc = j.rank / 8;  // 16-byte chunks of a weight row (<= 32)
-  float acc = 0.0f;
+  float acc4[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // independent chains, summed at the end
   const float uval = col < n && part == 0 ? ld_elem<SPEC_BF16>(j.U, (size_t)ri.urow * j.V + v)
                                           : 0.0f;
   if (col < n) {
@@ -208,6 +208,7 @@ __device__ __forceinline__ void rebuild_segment(const RowJob& j, const RowInfo& 
         const uint4 a = w1s[c];
         const uint32_t aa[4] = {a.x, a.y, a.z, a.w};
         const uint32_t bb[4] = {b[q].x, b[q].y, b[q].z, b[q].w};
+        float& acc = acc4[q & 3];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           acc = fmaf(__uint_as_float(aa[e] << 16), __uint_as_float(bb[e] << 16), acc);
@@ -217,6 +218,7 @@ __device__ __forceinline__ void rebuild_segment(const RowJob& j, const RowInfo& 
       }
     }
   }
+  float acc = (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
   acc += __shfl_xor_sync(0xffffffffu, acc, 1);
   if (col < n && part == 0) {
     const float s = __fadd_rn(uval, acc);
@@ -265,15 +267,24 @@ __device__ bool spin_count(const uint32_t* ctr, uint32_t target, uint32_t* gabor
 // cores) for the in-segment draw. The greedy token is the coarse partials' first maximum.
 template <bool ARGMAX>
 __device__ void select_two_level(const Params& P, const RowInfo& ri, int r, int s, int tid,
-                                 NamedBarrier wg, SelectShared& S, uint4* w1s) {
+                                 NamedBarrier wg, SelectShared& S, uint4* w1s, uint32_t* drawn) {
   const RowJob& j = P.j;
-  // the previous token's W1 row, for the segment rebuild, staged while the partials load
+  // loads that do not depend on the partials go out first: the previous token's W1 row (for the
+  // segment rebuild) and the row's uniform
   if (tid < j.rank / 8)
     w1s[tid] = __ldg(reinterpret_cast<const uint4*>(j.W1) + (size_t)ri.prev * (j.rank / 8) + tid);
   const int grid = P.ns;  // tile ranges
   const int warp = tid >> 5, lane = tid & 31;
   const bool greedy = P.o.greedy != 0;
+  const float u_row = greedy ? 0.0f : __ldg(P.o.uni + ri.urow);
   const size_t cb = (size_t)r * grid * 2;
+  if (tid == 0) {
+    S.c = -1;
+    S.rem = 1e30f;
+    S.x = -1;
+    S.last = -1;
+    S.zv0 = -1;
+  }
 
   // level 1: ranges c = tid and tid + 128 (grid <= 256), both halves of each
   float em[2][2], es[2][2];
@@ -335,21 +346,21 @@ __device__ void select_two_level(const Params& P, const RowInfo& ri, int r, int 
     if (lane == 31) S.wt[4 * a + warp] = incl[a];
   }
   wg();
-  DF Z = df_zero();
+  // the eight warp totals in range order, scanned across lanes 0..7 of every warp (each warp
+  // computes the same prefix sums): Z, and the mass before each warp's ranges
+  DF pre = lane < 8 ? S.wt[lane] : df_zero();
 #pragma unroll
-  for (int w = 0; w < 8; ++w) Z = df_add(Z, S.wt[w]);
+  for (int off = 1; off < 8; off <<= 1) {
+    const DF y = df_shfl_up(pre, off);
+    if (lane >= off && lane < 8) pre = df_add(y, pre);
+  }
+  const DF Z = df_shfl(pre, 7);
   if (tid == 0) {
     S.M = M;
     const bool zok = Z.hi > 0.0f && isfinite(Z.hi);
     S.lz = zok ? df_log(Z) : logf(Z.hi);
-    S.c = -1;
-    S.rem = 1e30f;
-    S.x = -1;
-    S.last = -1;
-    S.zv0 = -1;
     if (!zok || !(M > -INFINITY)) atomicOr(j.status, SPEC_DEV_NONFINITE);
   }
-  wg();
 
   // the segment to rebuild: the greedy token's (for its log-probability) or the crossing one
   int x = -1;
@@ -359,17 +370,19 @@ __device__ void select_two_level(const Params& P, const RowInfo& ri, int r, int 
       if (tid == 0) atomicOr(j.status, SPEC_DEV_NONFINITE);
       x = 0;
     }
-    if (tid == 0 && P.o.logp) S.zv0 = (x / kSeg) * kSeg;
-  } else {
-    const DF t = df_mul(Z, P.o.uni[ri.urow]);
-    // the crossing range: the warp (in range order) whose mass holds t, then its lane
-    DF before = df_zero();
-    int wstar = -1;
-    for (int w = 0; w < 8 && wstar < 0; ++w) {
-      const DF next = df_add(before, S.wt[w]);
-      if (df_gt(next, t)) wstar = w;
-      else before = next;
+    if (tid == 0) {
+      // the greedy token is known before its log-probability: publish it now
+      P.o.tokens[ri.urow] = x;
+      red_release_add(drawn, 1u);
+      if (P.o.logp) S.zv0 = (x / kSeg) * kSeg;
     }
+  } else {
+    const DF t = df_mul(Z, u_row);
+    // the crossing range: the warp (in range order) whose mass holds t, then its lane
+    const unsigned wh = __ballot_sync(0xffffffffu, lane < 8 && df_gt(pre, t));
+    const int wstar = wh ? __ffs(wh) - 1 : -1;
+    const DF pb = df_shfl(pre, wstar > 0 ? wstar - 1 : 0);
+    const DF before = wstar > 0 ? pb : df_zero();
     if (wstar >= 0 && warp == (wstar & 3)) {
       const int a = wstar >> 2;
       const DF ia = a ? incl[1] : incl[0], ba = a ? before_lane[1] : before_lane[0];
@@ -472,10 +485,12 @@ __device__ void select_two_level(const Params& P, const RowInfo& ri, int r, int 
     if (x < 0) x = 0;  // no mass at all: the status word already records it
   }
 
-  // outputs
-  if (tid == 0) {
-    const size_t q = (size_t)ri.urow;
+  // outputs: the token first, counted at once (the gathers wait for it), then the rest
+  const size_t q = (size_t)ri.urow;
+  if (tid == 0 && !greedy) {
     P.o.tokens[q] = x;
+    red_release_add(drawn, 1u);  // the token is visible before the count
+  } else if (tid == 32) {
     if (P.o.w1) l2_prefetch_bytes(static_cast<const char*>(P.o.w1) + (size_t)x * P.o.w1_row_bytes,
                                   P.o.w1_row_bytes);
     if (P.o.logp) {
@@ -562,29 +577,53 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mbar_wait(&st.full[x], (uint32_t)((q / kTStages) & 1), abort, status)))
           break;
         const int ri = (int)(q / parts), part = (int)(q % parts);
-        const int n = min(kTChunk, j.V - part * kTChunk);  // a multiple of 8
+        const int nw = min(kTChunk, j.V - part * kTChunk) / 8;  // 16-byte words
         const uint32_t base = smem_u32(st.stage[x]);
-        // maximum of the raw values (the scale is positive), then the sum of exponentials
+        // one pass: batches of four words per lane, the running maximum of the raw values (the
+        // scale is positive) with at most one rescale per batch, exp2((x - max) * scale * log2e)
+        // in packed pairs; padding words decode to -inf
+        const float cl = P.tscale * kLog2e;
         float mx = -INFINITY;
-        for (int w = lane; w < n / 8; w += 32) {
-          const uint4 v = lds128(base + w * 16);
-          float f[8];
-          unpack_bf16x8(v, f);
-          mx = fmaxf(mx, max3(max3(f[0], f[1], f[2]), max3(f[3], f[4], f[5]), fmaxf(f[6], f[7])));
-        }
-        mx = warp_max(mx);
-        const float m = __fmul_rn(mx, P.tscale);
-        float sum = 0.0f;
-        if (m > -INFINITY) {
-          for (int w = lane; w < n / 8; w += 32) {
-            const uint4 v = lds128(base + w * 16);
-            float f[8];
-            unpack_bf16x8(v, f);
+        unsigned long long s2 = pack2(0.0f, 0.0f);
+        for (int w0 = lane; w0 < nw; w0 += 4 * 32) {
+          float xv[4][8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) sum += exp_shift(__fmul_rn(f[e], P.tscale), m);
+          for (int b = 0; b < 4; ++b) {
+            const int w = w0 + 32 * b;
+            const uint4 v = w < nw ? lds128(base + w * 16)
+                                   : make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
+            unpack_bf16x8(v, xv[b]);
+          }
+          float g = mx;
+#pragma unroll
+          for (int b = 0; b < 4; ++b)
+            g = fmaxf(g, max3(max3(xv[b][0], xv[b][1], xv[b][2]), max3(xv[b][3], xv[b][4], xv[b][5]),
+                              fmaxf(xv[b][6], xv[b][7])));
+          if (g > mx) {
+            if (mx > -INFINITY) {
+              const float f = fast_exp2((mx - g) * cl);
+              s2 = mul2(s2, pack2(f, f));
+            }
+            mx = g;
+          }
+          if (mx > -INFINITY) {
+            const unsigned long long nm = pack2(-mx, -mx), c2 = pack2(cl, cl);
+#pragma unroll
+            for (int b = 0; b < 4; ++b)
+#pragma unroll
+              for (int e = 0; e < 8; e += 2) {
+                float a0, a1;
+                unpack2(mul2(add2(pack2(xv[b][e], xv[b][e + 1]), nm), c2), a0, a1);
+                s2 = add2(s2, pack2(fast_exp2(a0), fast_exp2(a1)));
+              }
           }
         }
-        sum = warp_sum(sum);
+        float sa, sb;
+        unpack2(s2, sa, sb);
+        // merge the lanes in the scaled domain: (m = max * scale, s)
+        const StatsAcc acc = warp_merge(
+            StatsAcc{mx > -INFINITY ? __fmul_rn(mx, P.tscale) : -INFINITY, sa + sb, 0});
+        const float m = acc.m, sum = acc.s;
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(&st.empty[x]);  // the stage may be refilled
@@ -646,10 +685,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           p = 0;
         }
         ri.prev = p;
-        select_two_level<ARGMAX>(P, ri, r, s, tid, tbar, ss.sel[team], ss.w1s[team]);
+        select_two_level<ARGMAX>(P, ri, r, s, tid, tbar, ss.sel[team], ss.w1s[team], &drawn[s]);
         tbar();
-        // the outputs (written by thread 0) are visible before the count
-        if (tid == 0) red_release_add(&drawn[s], 1u);
       }
     }
     if (!ok) *abort = 1;
