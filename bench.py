@@ -363,14 +363,12 @@ def other_configs(spec, workloads, dev, peak):
     res = [torch.empty(R, dtype=torch.int32, device=dev),
            torch.empty(R, g + 1, dtype=torch.int32, device=dev),
            torch.empty(R, dtype=torch.int32, device=dev)]
-    for op in range(6):
+    for op in range(7):
         ws.for_op(op, R, g, V, 0, stream)
 
     def mtp():
-        spec.spec_markov_propose(wl.U, None, None, None, None, 0.0, draft_tokens=toks,
-                                 want_stats=False, workspace=ws, stream=stream)
-        spec.spec_verify_greedy(wl.target, toks, accept_len=res[0], out_tokens=res[1],
-                                next_anchor=res[2], workspace=ws, stream=stream)
+        spec.spec_mtp_greedy(wl.U, wl.target, draft_tokens=toks, accept_len=res[0],
+                             out_tokens=res[1], next_anchor=res[2], workspace=ws, stream=stream)
     ms = graph_ms(mtp, stream)
     entry("mtp_greedy_R64_g3_V129280", ms, R * (2 * g + 1),
           (wl.U.numel() + wl.target.numel()) * 2,

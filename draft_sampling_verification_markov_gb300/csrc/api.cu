@@ -107,6 +107,14 @@ size_t partial_entries(int op, int R, int gamma, int V, int rank) {
       }
       break;
     case SPEC_OP_VERIFY_GREEDY: e = tr; break;
+    case SPEC_OP_MTP_GREEDY: {
+      // one partial per streamed item, or the two-call form's proposal and verification
+      const size_t fe = (size_t)R * (2 * (size_t)gamma + 1) * cdiv(V, kMtpChunk);
+      const size_t pe = dr * stream_nseg(V);
+      e = fe > pe ? fe : pe;
+      e = e > tr ? e : tr;
+      break;
+    }
     case SPEC_OP_TARGET_STATS: e = tgt; break;
     case SPEC_OP_VERIFY_REJECTION: e = tgt > (size_t)R * seg_draft ? tgt : (size_t)R * seg_draft; break;
     case SPEC_OP_TV_CONFIDENCE: e = tgt > dr * seg_draft ? tgt : dr * seg_draft; break;
@@ -377,9 +385,15 @@ static int markov_propose_impl(const void* U, int u_dtype, const void* W1, const
     o.w1 = aligned16(W1) && (rank * (int)esize(wdt)) % 16 == 0 ? W1 : nullptr;
     o.w1_row_bytes = rank * (int)esize(wdt);
     uint32_t* sync = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + kSyncOffset);
+    // The target rows ride along only while the proposal's serial chain leaves SMs idle: with
+    // at most two 128-request groups. With more groups the streaming CTAs are busy and the
+    // normalisers are cheaper as a pass of their own.
+    const bool along = target && R <= 256;
     if (launch_markov_propose_tc(j, o, w.pm, w.ps, greedy ? w.pi : nullptr, greedy, sync, s,
-                                 target, target_stats, 1.0f / temperature) != cudaSuccess)
+                                 along ? target : nullptr, target_stats,
+                                 1.0f / temperature) != cudaSuccess)
       return SPEC_ERR_CUDA;
+    if (target && !along) return target_after(target, target_stats, u_dtype, temperature, R, gamma, V, w, s);
     return finish();
   }
   // every launch after the first is chained to the one before it
@@ -718,6 +732,35 @@ int spec_markov_propose(const void* U, int u_dtype, const void* W1, const void* 
   return markov_propose_impl(U, u_dtype, W1, W2, w_dtype, rank, anchors, u_draft, temperature, R,
                              gamma, V, draft_tokens, draft_logp, draft_stats, ws, ws_bytes,
                              stream, nullptr);
+}
+
+int spec_mtp_greedy(const void* D, const void* target, int dtype, const int32_t* lengths, int R,
+                    int gamma, int V, int32_t* draft_tokens, int32_t* accept_len,
+                    int32_t* out_tokens, int32_t* next_anchor, void* ws, size_t ws_bytes,
+                    void* stream) {
+  if (!sizes_ok(R, gamma, V)) return SPEC_ERR_INVALID_ARG;
+  if (!dtype_ok(dtype)) return SPEC_ERR_UNSUPPORTED_DTYPE;
+  Layout L;
+  int rc = check_ws(ws, ws_bytes, SPEC_OP_MTP_GREEDY, R, gamma, V, 0, &L);
+  if (rc != SPEC_OK) return rc;
+  if (R == 0) return SPEC_OK;
+  if (!target || !accept_len || (gamma > 0 && (!D || !draft_tokens))) return SPEC_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (mtp_greedy_supported(dtype, R, gamma, V, D, target)) {
+    const Ws w = carve(ws, L);
+    if (launch_mtp_greedy(dtype, D, target, R, gamma, V, lengths, draft_tokens, accept_len,
+                          out_tokens, next_anchor, w.pm, w.pi, w.status, s) != cudaSuccess)
+      return SPEC_ERR_CUDA;
+    return finish();
+  }
+  if (gamma > 0) {
+    rc = markov_propose_impl(D, dtype, nullptr, nullptr, dtype, 0, nullptr, nullptr, 0.0f, R,
+                             gamma, V, draft_tokens, nullptr, nullptr, ws, ws_bytes, stream,
+                             nullptr);
+    if (rc != SPEC_OK) return rc;
+  }
+  return verify_greedy_impl(target, dtype, draft_tokens, lengths, nullptr, R, gamma, V,
+                            accept_len, out_tokens, next_anchor, ws, ws_bytes, stream);
 }
 
 int spec_markov_propose_masked(const void* U, int u_dtype, const void* W1, const void* W2,

@@ -103,6 +103,17 @@ bool make_tensor_map_bf16(CUtensorMap* m, const void* base, int rank, const cuui
 int take_stall_request();
 // Vocabulary columns per partial written by the tcgen05 producer in pass mode `mode`.
 int markov_tc_seg(int mode);
+// MTP/NextN greedy proposal + greedy verification (mtp.cu): one streaming launch takes the
+// argmax of every draft and target row in kMtpChunk-element items (pm / pi: one partial per
+// item, R * (2 gamma + 1) * cdiv(V, kMtpChunk) of them), a chained launch merges them per
+// request and runs the scan.
+constexpr int kMtpChunk = 4096;
+constexpr int kMtpMaxGamma = 1024;
+bool mtp_greedy_supported(int dtype, int R, int gamma, int V, const void* D, const void* T);
+cudaError_t launch_mtp_greedy(int dtype, const void* D, const void* T, int R, int gamma, int V,
+                              const int32_t* lengths, int32_t* draft_tokens, int32_t* accept_len,
+                              int32_t* out_tokens, int32_t* next_anchor, float* pm, int* pi,
+                              uint32_t* status, cudaStream_t s);
 // Smallest partial segment any Markov producer writes (sizes the workspace).
 constexpr int kMarkovMinSeg = 32;
 

@@ -17,7 +17,7 @@ from . import build as _build
 SPEC_OK = 0
 SPEC_F32, SPEC_BF16 = 0, 1
 (SPEC_OP_PROPOSE, SPEC_OP_VERIFY_GREEDY, SPEC_OP_VERIFY_REJECTION, SPEC_OP_TV_CONFIDENCE,
- SPEC_OP_SCHEDULE, SPEC_OP_TARGET_STATS, SPEC_OP_ALL) = range(7)
+ SPEC_OP_SCHEDULE, SPEC_OP_TARGET_STATS, SPEC_OP_MTP_GREEDY, SPEC_OP_ALL) = range(8)
 (SPEC_DEV_BAD_TOKEN, SPEC_DEV_NONFINITE, SPEC_DEV_EMPTY_RESIDUAL, SPEC_DEV_BAD_LENGTH,
  SPEC_DEV_TIMEOUT) = 1, 2, 4, 8, 16
 SPEC_SCHEDULE_MAX_CANDIDATES = 16384
@@ -58,6 +58,7 @@ def lib():
         L.spec_markov_propose.argtypes = [vp, i, vp, vp, i, i, vp, vp, f, i, i, i, vp, vp, vp, vp,
                                           sz, vp]
         L.spec_verify_greedy.argtypes = [vp, i, vp, vp, i, i, i, vp, vp, vp, vp, sz, vp]
+        L.spec_mtp_greedy.argtypes = [vp, vp, i, vp, i, i, i, vp, vp, vp, vp, vp, sz, vp]
         L.spec_target_stats.argtypes = [vp, i, f, i, i, vp, vp, sz, vp]
         L.spec_verify_rejection.argtypes = [vp, vp, i, vp, vp, i, i, vp, vp, vp, vp, vp, vp, vp,
                                             f, vp, i, i, i, vp, vp, vp, vp, sz, vp]
@@ -91,7 +92,7 @@ def lib():
                      "spec_tv_confidence", "spec_schedule_prefix", "spec_schedule_topk",
                      "spec_verify_greedy_noalloc", "spec_markov_propose_masked",
                      "spec_verify_rejection_masked", "spec_tv_confidence_masked",
-                     "spec_markov_propose_target_stats",
+                     "spec_markov_propose_target_stats", "spec_mtp_greedy",
                      "spec_flat_layout", "spec_target_stats_flat", "spec_verify_greedy_flat",
                      "spec_verify_rejection_flat"):
             getattr(L, name).restype = i
@@ -256,6 +257,34 @@ def spec_markov_propose_target_stats(U, W1, W2, anchors, u_draft, temperature, t
         _ptr(target), _ptr(target_stats), wp, wn, _stream(stream))
     _check("spec_markov_propose_target_stats", rc)
     return draft_tokens, draft_logp, draft_stats, target_stats
+
+
+def spec_mtp_greedy(D, target, lengths=None, *, draft_tokens=None, accept_len=None,
+                    out_tokens=None, next_anchor=None, workspace=None, stream=None):
+    """MTP/NextN greedy proposal (draft argmax per position) and greedy verification in one
+    call. D [R, gamma, V] and target [R, gamma+1, V] of one dtype. Returns (draft_tokens [R,g],
+    accept_len [R], out_tokens [R, g+1], next_anchor [R]), all int32."""
+    R, rows, V = target.shape
+    gamma = rows - 1
+    dev = target.device
+    if gamma > 0 and (D is None or tuple(D.shape) != (R, gamma, V) or D.dtype != target.dtype):
+        raise ValueError("D must be [R, gamma, V] with the target's dtype")
+    i32 = dict(dtype=torch.int32, device=dev)
+    if draft_tokens is None:
+        draft_tokens = torch.empty(R, gamma, **i32)
+    if accept_len is None:
+        accept_len = torch.empty(R, **i32)
+    if out_tokens is None:
+        out_tokens = torch.empty(R, gamma + 1, **i32)
+    if next_anchor is None:
+        next_anchor = torch.empty(R, **i32)
+    ws = workspace or default_workspace(dev)
+    wp, wn = ws.for_op(SPEC_OP_MTP_GREEDY, R, gamma, V, 0, stream)
+    rc = lib().spec_mtp_greedy(_ptr(D), _ptr(target), _dt(target), _ptr(lengths), R, gamma, V,
+                               _ptr(draft_tokens), _ptr(accept_len), _ptr(out_tokens),
+                               _ptr(next_anchor), wp, wn, _stream(stream))
+    _check("spec_mtp_greedy", rc)
+    return draft_tokens, accept_len, out_tokens, next_anchor
 
 
 def spec_verify_greedy(target, draft_tokens, lengths=None, *, accept_len=None, out_tokens=None,

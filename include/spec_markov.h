@@ -66,7 +66,8 @@ extern "C" {
 #define SPEC_OP_TV_CONFIDENCE 3
 #define SPEC_OP_SCHEDULE 4
 #define SPEC_OP_TARGET_STATS 5
-#define SPEC_OP_ALL 6 /* a workspace large enough for every op at this size */
+#define SPEC_OP_MTP_GREEDY 6
+#define SPEC_OP_ALL 7 /* a workspace large enough for every op at this size */
 
 /* device status bits (spec_device_status) */
 #define SPEC_DEV_BAD_TOKEN 0x1u      /* an anchor or draft token outside [0, V) was read */
@@ -137,9 +138,9 @@ int spec_markov_propose(const void* U, int u_dtype, const void* W1, const void* 
  *   R * (gamma + 1), V, target_stats): the proposal of "[DeepSeek-6] DSpark", sections 3-4, and
  *   the p_t normalisers that its rejection verification (section 9) needs.
  * The target normalisers do not depend on the proposal. With bf16 weights on the tensor cores
- * the proposal runs as one persistent launch whose positions leave HBM partly idle; a share of
- * its CTAs streams the target rows meanwhile, so the two cost about as much time as the
- * proposal alone. Other shapes run the two operations one after the other.
+ * and R <= 256 the proposal runs as one persistent launch whose serial positions leave SMs
+ * partly idle, and a share of its CTAs streams the target rows meanwhile. Other shapes run the
+ * two operations one after the other.
  * Arguments: as spec_markov_propose (U of dtype l_dtype), plus
  *   target       [R, gamma+1, V] target logits, dtype l_dtype (required).
  *   target_stats [R*(gamma+1), 2] fp32 output (m, log Z) of softmax(target[row,:] / T), for
@@ -153,6 +154,37 @@ int spec_markov_propose_target_stats(const void* U, int l_dtype, const void* W1,
                                      int V, int32_t* draft_tokens, float* draft_logp,
                                      float* draft_stats, const void* target, float* target_stats,
                                      void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * MTP/NextN greedy proposal and greedy verification of the same window in one call.
+ * Defines: "Module deepseek_v4_mtp", Forward (without a Markov head the draft token of
+ *   position k is the argmax of the draft logits of position k-1, so the positions are
+ *   independent) and "DeepSeek-V4 MTP/NextN 怎样逐步生成候选", sections 三-四 (the verify
+ *   window [bonus, d1..d_gamma]: accept the longest prefix of drafts equal to the target
+ *   argmax of the row before them, then emit the target argmax of the row after it).
+ * Equal to spec_markov_propose(D, dtype, NULL, NULL, 0, 0, NULL, NULL, 0, ...) followed by
+ * spec_verify_greedy(target, dtype, draft_tokens, lengths, ...), bit for bit. With 16-byte
+ * aligned logits, V a multiple of 8 (bf16) or 4 (fp32), gamma <= 1024 and R <= 2048 it is one
+ * streaming launch over both tensors; other shapes run the two operations.
+ * Arguments:
+ *   D            [R, gamma, V] draft logits (bf16 or fp32, `dtype`); may be NULL if gamma = 0.
+ *   target       [R, gamma+1, V] target logits of the same dtype.
+ *   lengths      [R] int32 verified lengths l_r in [0, gamma], or NULL for gamma. Target rows
+ *                past l_r are not read; all gamma draft tokens are always proposed.
+ *   draft_tokens [R, gamma] int32 output: the draft argmax per position (ties: lowest id).
+ *   accept_len, out_tokens, next_anchor: as spec_verify_greedy (out_tokens, next_anchor
+ *                optional).
+ * Workspace: spec_workspace_bytes(SPEC_OP_MTP_GREEDY, R, gamma, V, 0), initialised once with
+ * spec_workspace_init (the launch uses per-request counters that it leaves at zero).
+ * Errors: SPEC_ERR_INVALID_ARG for bad sizes or NULL required pointers,
+ * SPEC_ERR_UNSUPPORTED_DTYPE, SPEC_ERR_WORKSPACE_TOO_SMALL. A row without a finite maximum sets
+ * SPEC_DEV_NONFINITE (its argmax is then 0); a length outside [0, gamma] sets
+ * SPEC_DEV_BAD_LENGTH and is clamped.
+ */
+int spec_mtp_greedy(const void* D, const void* target, int dtype, const int32_t* lengths, int R,
+                    int gamma, int V, int32_t* draft_tokens, int32_t* accept_len,
+                    int32_t* out_tokens, int32_t* next_anchor, void* ws, size_t ws_bytes,
+                    void* stream);
 
 /*
  * Greedy verification with a bonus token.
@@ -385,7 +417,9 @@ int spec_verify_rejection_flat(const void* target, const void* U, int l_dtype, c
  *     process exits; R * (gamma + 1) above SPEC_NOALLOC_MAX_ROWS returns SPEC_ERR_TOO_LARGE
  *     before any launch;
  *   - the first call on a device looks up that array's device address (once per device, with
- *     that device current); make that first call before any stream capture;
+ *     that device current); make that first call before any stream capture. The address is
+ *     kept for the life of the process: after a cudaDeviceReset of that device it is stale, and
+ *     this entry point must not be called on that device again;
  *   - every call on a device shares the one array, so calls whose work overlaps on the GPU
  *     (other streams, other host threads) race and give undefined results: order them;
  *   - the device status bits of this call (SPEC_DEV_*, cleared at the start of every call) are
@@ -398,6 +432,8 @@ int spec_verify_greedy_noalloc(const void* target, int t_dtype, const int32_t* d
                                uint32_t* device_status, void* stream);
 
 /*
+ * TEST-ONLY: never call this outside a test of the timeout path; the next tensor-core pass it
+ * stalls produces no result.
  * Test support for the bounded waits (no counterpart on the pages). The next tensor-core
  * Markov pass launched by this process never receives its first W2 tile, so its MMA thread's
  * wait expires (after about 2 s of SM clock): the kernel sets SPEC_DEV_TIMEOUT in the device

@@ -50,7 +50,7 @@ def test_host_only_entry_points(cuda_lib):
     f.argtypes = [ctypes.c_int] * 5
     a = f(0, 256, 7, 129280, 256)
     assert a > 256 and a % 256 == 0
-    assert f(6, 256, 7, 129280, 256) >= max(f(op, 256, 7, 129280, 256) for op in range(6))
+    assert f(7, 256, 7, 129280, 256) >= max(f(op, 256, 7, 129280, 256) for op in range(7))
     assert f(0, -1, 7, 10, 0) == 0          # invalid sizes report 0
     assert f(99, 1, 1, 1, 0) == 0
 
