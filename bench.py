@@ -419,6 +419,26 @@ def other_configs(spec, workloads, dev, peak):
           (wl.U.numel() + wl.target.numel() + wl.W2.numel()) * 2,
           {"mean_emitted_per_request": float(lp.emitted_tokens().float().mean())})
     assert ws.status() == 0 and lp.ws.status() == 0, "device status word set"
+    padded_out = lp.out_tokens.clone()
+    del lp
+    torch.cuda.empty_cache()
+
+    # the same iterations verifying the flattened batch (packed rows, per-request offsets); the
+    # packing copy of the B scheduled rows stands in for a target model that writes only them
+    lp = SpecLoop(wl.U, wl.target, wl.W1, wl.W2, wl.anchors, wl.u_draft, wl.u_accept,
+                  wl.u_resid, wl.temperature, wl.sps.to(dev), iterations=2, flat=True)
+    ms_flat = graph_ms(lambda: lp.run(), stream, reps=3) / 2
+    B = float(lp.batch.float().mean())
+    row_bytes = wl.V * wl.target.element_size()
+    entry("full_loop_flat_R1024_g16_V129280_per_iteration", ms_flat, R * (2 * g + 1),
+          (wl.U.numel() + wl.target.numel() + wl.W2.numel()) * 2,
+          {"scheduled_B": B, "padded_rows": R * (g + 1),
+           "packed_bytes_per_iteration": 2 * B * row_bytes,
+           "padded_ms_per_iteration": ms,
+           "same_outputs_as_padded": bool(torch.equal(padded_out, lp.out_tokens)),
+           "note": "packing copies only the B scheduled target rows (read + write); "
+                   "verification then reads the packed rows"})
+    assert lp.ws.status() == 0, "device status word set"
     del wl, lp
     torch.cuda.empty_cache()
     return out

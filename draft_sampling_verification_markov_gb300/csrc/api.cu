@@ -483,6 +483,23 @@ int spec_flat_layout(const int32_t* lengths, int R, int gamma, int32_t* offsets,
   return finish();
 }
 
+int spec_flat_pack(const void* src, int row_bytes, const int32_t* lengths,
+                   const int32_t* offsets, int R, int gamma, void* dst, void* ws, size_t ws_bytes,
+                   void* stream) {
+  if (R < 0 || gamma < 0 || (long long)R * (gamma + 1) > (1LL << 30)) return SPEC_ERR_INVALID_ARG;
+  if (row_bytes < 4 || row_bytes % 4 != 0) return SPEC_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < kHeader || (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0)
+    return SPEC_ERR_INVALID_ARG;
+  if (R == 0) return SPEC_OK;
+  if (!src || !dst || !lengths || !offsets) return SPEC_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(src) & 3) != 0 || (reinterpret_cast<uintptr_t>(dst) & 3) != 0)
+    return SPEC_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  TraceScope ts(SPEC_KCLASS_OTHER, s);
+  launch_flat_pack(src, row_bytes, lengths, offsets, R, gamma, dst, static_cast<uint32_t*>(ws), s);
+  return finish();
+}
+
 int spec_target_stats_flat(const void* target, int t_dtype, float temperature, int R, int gamma,
                            int V, const int32_t* offsets, float* stats, void* ws,
                            size_t ws_bytes, void* stream) {

@@ -71,6 +71,11 @@ size_t schedule_smem_bytes(int R, int gamma);
 // Flattened verify batch layout from per-request lengths (offsets [R+1], optional row markers).
 void launch_flat_layout(const int32_t* lengths, int R, int gamma, int32_t* offsets,
                         int32_t* row_req, int32_t* row_pos, uint32_t* status, cudaStream_t s);
+// Rows (r, i <= l_r) of a padded [R, gamma+1] array of row_bytes-byte rows to packed rows
+// offsets[r] + i (row_bytes a multiple of 4).
+void launch_flat_pack(const void* src, int row_bytes, const int32_t* lengths,
+                      const int32_t* offsets, int R, int gamma, void* dst, uint32_t* status,
+                      cudaStream_t s);
 
 // tcgen05 Markov producer (markov_tc.cu). Returns false when the shape is not supported
 // (the caller then uses the CUDA-core producer).

@@ -282,6 +282,62 @@ __global__ void __launch_bounds__(kSchedThreads) flat_layout_kernel(const int32_
   }
 }
 
+// Copy of the verified rows of a padded [R, gamma+1, row] array into the flattened layout:
+// padded row (r, i), i <= l_r, to packed row offsets[r] + i. One block per padded row; rows past
+// a request's length are neither read nor written, so the bytes moved are those of the B rows.
+__global__ void __launch_bounds__(256) flat_pack_kernel(const char* src, int row_bytes,
+                                                        const int32_t* lengths,
+                                                        const int32_t* offsets, int R, int gamma,
+                                                        char* dst, uint32_t* status) {
+  const long long row = blockIdx.x;
+  const int r = (int)(row / (gamma + 1)), i = (int)(row % (gamma + 1));
+  int l = lengths[r];
+  if (l < 0 || l > gamma) {
+    if (threadIdx.x == 0) atomicOr(status, SPEC_DEV_BAD_LENGTH);
+    l = l < 0 ? 0 : gamma;
+  }
+  if (i > l) return;
+  const long long b = (long long)offsets[r] + i;
+  if (b < 0 || b >= (long long)R * (gamma + 1)) {
+    if (threadIdx.x == 0) atomicOr(status, SPEC_DEV_BAD_LENGTH);
+    return;
+  }
+  const char* from = src + row * row_bytes;
+  char* to = dst + b * row_bytes;
+  if (row_bytes % 16 == 0 && (reinterpret_cast<uintptr_t>(src) & 15) == 0 &&
+      (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+    const uint4* f = reinterpret_cast<const uint4*>(from);
+    uint4* t = reinterpret_cast<uint4*>(to);
+    const int n = row_bytes / 16;
+    for (int w = threadIdx.x; w < n; w += 4 * blockDim.x) {
+      uint4 v[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int x = w + k * blockDim.x;
+        if (x < n) v[k] = ld_stream16(f + x);
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int x = w + k * blockDim.x;
+        if (x < n) t[x] = v[k];
+      }
+    }
+  } else {  // row_bytes % 4 == 0
+    const uint32_t* f = reinterpret_cast<const uint32_t*>(from);
+    uint32_t* t = reinterpret_cast<uint32_t*>(to);
+    for (int w = threadIdx.x; w < row_bytes / 4; w += blockDim.x) t[w] = f[w];
+  }
+}
+
+void launch_flat_pack(const void* src, int row_bytes, const int32_t* lengths,
+                      const int32_t* offsets, int R, int gamma, void* dst, uint32_t* status,
+                      cudaStream_t s) {
+  const long long rows = (long long)R * (gamma + 1);
+  flat_pack_kernel<<<(unsigned)rows, 256, 0, s>>>(static_cast<const char*>(src), row_bytes,
+                                                  lengths, offsets, R, gamma,
+                                                  static_cast<char*>(dst), status);
+}
+
 void launch_flat_layout(const int32_t* lengths, int R, int gamma, int32_t* offsets,
                         int32_t* row_req, int32_t* row_pos, uint32_t* status, cudaStream_t s) {
   flat_layout_kernel<<<1, kSchedThreads, 0, s>>>(lengths, R, gamma, offsets, row_req, row_pos,

@@ -33,11 +33,17 @@ class SpecLoop:
     section 7): iteration t still ranks its own candidates by its own survival, but the batch
     size it fills is the Theta-optimal one of iteration t - 2 (dynamic top-K). The first two
     iterations have no such history and use their own Theta optimum. One scheduler launch per
-    iteration both selects and records the Theta optimum for iteration t + 2 (batch_opt)."""
+    iteration both selects and records the Theta optimum for iteration t + 2 (batch_opt).
+
+    flat=True (with a scheduler) verifies the flattened batch of section 7: the scheduled rows
+    are packed into B = sum_r (1 + l_r) consecutive rows with per-request offsets, the target
+    normalisers are packed alike, and rejection verification reads the packed rows. The
+    packing copy stands in for a target model that writes only the B scheduled rows; the
+    outputs equal the padded loop's bit for bit."""
 
     def __init__(self, U, target, W1, W2, anchors0, u_draft, u_accept, u_resid, temperature,
                  sps=None, *, iterations=None, schedule=True, allowed=None,
-                 async_schedule=False):
+                 async_schedule=False, flat=False):
         R, gamma, V = U.shape
         self.R, self.gamma, self.V = R, gamma, V
         self.iters = int(iterations if iterations is not None else u_draft.shape[0])
@@ -48,6 +54,7 @@ class SpecLoop:
         self.allowed = allowed
         self.schedule = bool(schedule) and sps is not None
         self.async_schedule = self.schedule and bool(async_schedule)
+        self.flat = self.schedule and bool(flat)
         self.rank = 0 if W1 is None else int(W1.shape[1])
         dev = U.device
         i32 = dict(dtype=torch.int32, device=dev)
@@ -68,6 +75,10 @@ class SpecLoop:
         self.theta = torch.empty(n, dtype=torch.float64, device=dev)
         self.accept_len = torch.empty(n, R, **i32)
         self.out_tokens = torch.empty(n, R, gamma + 1, **i32)
+        if self.flat:
+            self.offsets = torch.empty(R + 1, **i32)
+            self.packed_target = torch.empty(R * (gamma + 1), V, dtype=target.dtype, device=dev)
+            self.packed_stats = torch.empty(R * (gamma + 1), 2, **f32)
         # one workspace large enough for every step, reserved before any capture
         self.ws = S.Workspace(device=dev)
         self.ws.reserve(int(S.lib().spec_workspace_bytes(S.SPEC_OP_ALL, R, gamma, V, self.rank)))
@@ -99,6 +110,24 @@ class SpecLoop:
             else:
                 S.spec_schedule_prefix(self.survival[t], self.sps, **out)
             lengths = self.lengths[t]
+        if self.flat:
+            # the flattened verify batch: B packed target rows and their normalisers
+            S.spec_flat_layout(lengths, self.gamma, offsets=self.offsets, markers=False,
+                               workspace=ws, stream=stream)
+            tv = self.target.view(self.R, self.gamma + 1, self.V)
+            S.spec_flat_pack(tv, lengths, self.offsets, out=self.packed_target, workspace=ws,
+                             stream=stream)
+            S.spec_flat_pack(self.target_stats.view(self.R, self.gamma + 1, 2), lengths,
+                             self.offsets, out=self.packed_stats, workspace=ws, stream=stream)
+            S.spec_verify_rejection_flat(self.packed_target, self.U, self.W1, self.W2, a_t,
+                                         self.draft_tokens[t], self.draft_logp, self.draft_stats,
+                                         self.u_accept[t], self.u_resid[t], T, lengths,
+                                         self.offsets, target_stats=self.packed_stats,
+                                         accept_len=self.accept_len[t],
+                                         out_tokens=self.out_tokens[t],
+                                         next_anchor=self.anchors[t + 1], workspace=ws,
+                                         stream=stream, allowed=self.allowed)
+            return
         S.spec_verify_rejection(self.target, self.U, self.W1, self.W2, a_t, self.draft_tokens[t],
                                 self.draft_logp, self.draft_stats, self.u_accept[t],
                                 self.u_resid[t], T, lengths, target_stats=self.target_stats,

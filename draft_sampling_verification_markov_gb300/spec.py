@@ -77,6 +77,7 @@ def lib():
         L.spec_tv_confidence_masked.argtypes = [vp, vp, i, vp, vp, i, i, vp, vp, vp, vp, f, i, i,
                                                 i, vp, vp, vp, vp, sz, vp]
         L.spec_flat_layout.argtypes = [vp, i, i, vp, vp, vp, vp, sz, vp]
+        L.spec_flat_pack.argtypes = [vp, i, vp, vp, i, i, vp, vp, sz, vp]
         L.spec_target_stats_flat.argtypes = [vp, i, f, i, i, i, vp, vp, vp, sz, vp]
         L.spec_verify_greedy_flat.argtypes = [vp, i, vp, vp, vp, i, i, i, vp, vp, vp, vp, sz, vp]
         L.spec_verify_rejection_flat.argtypes = [vp, vp, i, vp, vp, i, i, vp, vp, vp, vp, vp, vp,
@@ -93,7 +94,8 @@ def lib():
                      "spec_verify_greedy_noalloc", "spec_markov_propose_masked",
                      "spec_verify_rejection_masked", "spec_tv_confidence_masked",
                      "spec_markov_propose_target_stats", "spec_mtp_greedy",
-                     "spec_flat_layout", "spec_target_stats_flat", "spec_verify_greedy_flat",
+                     "spec_flat_layout", "spec_flat_pack", "spec_target_stats_flat",
+                     "spec_verify_greedy_flat",
                      "spec_verify_rejection_flat"):
             getattr(L, name).restype = i
         _lib = L
@@ -462,6 +464,26 @@ def spec_flat_layout(lengths, gamma, *, offsets=None, row_req=None, row_pos=None
                                 _ptr(row_pos), ws.ptr, ws.nbytes, _stream(stream))
     _check("spec_flat_layout", rc)
     return offsets, row_req, row_pos
+
+
+def spec_flat_pack(src, lengths, offsets, *, out=None, workspace=None, stream=None):
+    """Rows (r, i <= l_r) of a padded src [R, gamma+1, ...] to packed rows offsets[r] + i of
+    out [R*(gamma+1), ...] (allocated when None; rows past B are left as they were)."""
+    R, g1 = src.shape[0], src.shape[1]
+    dev = src.device
+    _i32_on(lengths, dev, "lengths")
+    _i32_on(offsets, dev, "offsets")
+    row_bytes = src[0, 0].numel() * src.element_size() if src.numel() else 4
+    if out is None:
+        out = torch.empty((R * g1,) + tuple(src.shape[2:]), dtype=src.dtype, device=dev)
+    if out.numel() != src.numel() or out.dtype != src.dtype:
+        raise ValueError("out holds R*(gamma+1) rows of src's row shape and dtype")
+    ws = workspace or default_workspace(dev)
+    ws.reserve(256, stream)
+    rc = lib().spec_flat_pack(_ptr(src), int(row_bytes), _ptr(lengths), _ptr(offsets), R,
+                              g1 - 1, _ptr(out), ws.ptr, ws.nbytes, _stream(stream))
+    _check("spec_flat_pack", rc)
+    return out
 
 
 def spec_target_stats_flat(target, temperature, offsets, gamma, *, stats=None, workspace=None,

@@ -367,6 +367,22 @@ int spec_flat_layout(const int32_t* lengths, int R, int gamma, int32_t* offsets,
                      void* stream);
 
 /*
+ * Packing of padded rows into the flattened layout: for every request r and position
+ * i <= l_r, row (r, i) of src [R, gamma+1, row_bytes] is copied to packed row offsets[r] + i of
+ * dst [R*(gamma+1), row_bytes]. Rows past a request's length are neither read nor written, so
+ * the bytes moved are those of the B scheduled rows. It stands in for a target model that
+ * writes its logits (or a caller's per-row statistics) straight into the packed layout.
+ *   row_bytes  bytes per row, a multiple of 4 (16-byte rows and pointers copy 16 bytes at a
+ *              time); lengths and offsets as for spec_flat_layout (device).
+ * A length outside [0, gamma] is clamped and sets SPEC_DEV_BAD_LENGTH; so does an offset that
+ * would put a row outside the R*(gamma+1) packed rows (that row is not written). The
+ * workspace is used for its status word only (ws_bytes >= 256).
+ */
+int spec_flat_pack(const void* src, int row_bytes, const int32_t* lengths,
+                   const int32_t* offsets, int R, int gamma, void* dst, void* ws, size_t ws_bytes,
+                   void* stream);
+
+/*
  * Target normalisers of a flattened batch: stats[b] = (m, log Z) of softmax(target[b,:] / T)
  * for the packed rows b < offsets[R]; rows past the batch are neither read nor written.
  * target [R*(gamma+1), V] packed, stats [R*(gamma+1), 2] fp32 (packed like target).

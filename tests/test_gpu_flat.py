@@ -184,3 +184,23 @@ def test_scheduler_to_flat_verify(spec, ws):
                                                   offsets, workspace=ws)
     dn, dout, dnxt = spec.spec_verify_rejection(g["target"], *args, lengths, workspace=ws)
     assert torch.equal(n, dn) and torch.equal(out, dout) and torch.equal(nxt, dnxt)
+
+
+@pytest.mark.parametrize("dtype,width", [(torch.bfloat16, 1000), (torch.float32, 2), (torch.float32, 7)])
+def test_flat_pack_copies_only_the_scheduled_rows(spec, ws, dtype, width):
+    """spec_flat_pack: padded row (r, i <= l_r) lands on packed row offsets[r] + i; rows past
+    B keep what they held (NaN here), whatever the row width (16-byte or 4-byte copies)."""
+    R, gamma = 37, 5
+    g = torch.Generator().manual_seed(width)
+    src = torch.randn(R, gamma + 1, width, generator=g).to(dtype).cuda()
+    lengths = torch.randint(0, gamma + 1, (R,), generator=g, dtype=torch.int32).cuda()
+    offsets, _, _ = spec.spec_flat_layout(lengths, gamma, markers=False, workspace=ws)
+    out = torch.full((R * (gamma + 1), width), float("nan"), dtype=dtype, device="cuda")
+    spec.spec_flat_pack(src, lengths, offsets, out=out, workspace=ws)
+    torch.cuda.synchronize()
+    ln = lengths.cpu().tolist()
+    want = torch.cat([src[r, :ln[r] + 1] for r in range(R)])
+    B = want.shape[0]
+    assert int(offsets[-1]) == B
+    assert torch.equal(out[:B], want)
+    assert torch.isnan(out[B:].float()).all()

@@ -25,12 +25,12 @@ def spec():
     return s
 
 
-def _loop(spec, wl, schedule=True, async_schedule=False):
+def _loop(spec, wl, schedule=True, async_schedule=False, flat=False):
     from draft_sampling_verification_markov_gb300.loop import SpecLoop
     g = {k: v.cuda() for k, v in wl.tensors().items()}
     return SpecLoop(g["U"], g["target"], g["W1"], g["W2"], g["anchors"], g["u_draft"],
                     g["u_accept"], g["u_resid"], wl.temperature, g.get("sps"),
-                    schedule=schedule, async_schedule=async_schedule)
+                    schedule=schedule, async_schedule=async_schedule, flat=flat)
 
 
 def check_iteration(lp, wl, t, sample=None, report=None):
@@ -105,6 +105,32 @@ def test_loop_graph_replay_equals_eager(spec):
     torch.cuda.synchronize()
     assert torch.equal(first, graph.out_tokens)
     assert eager.ws.status() == 0 and graph.ws.status() == 0
+
+
+@pytest.mark.parametrize("async_schedule", [False, True])
+def test_flat_loop_equals_padded_loop(spec, async_schedule):
+    """Verification of the flattened batch (packed target rows and normalisers, per-request
+    offsets) gives the padded loop's outputs bit for bit, eager and as one replayed graph."""
+    wl = W.full_loop("cpu", R=70, gamma=5, V=2048, rank=128, iterations=4, seed=36)
+    padded = _loop(spec, wl, async_schedule=async_schedule)
+    padded.run()
+    flat = _loop(spec, wl, async_schedule=async_schedule, flat=True)
+    flat.run()
+    graph = _loop(spec, wl, async_schedule=async_schedule, flat=True)
+    graph.capture()
+    graph.replay()
+    torch.cuda.synchronize()
+    for name in ("anchors", "draft_tokens", "lengths", "batch", "accept_len", "out_tokens"):
+        assert torch.equal(getattr(padded, name), getattr(flat, name)), name
+        assert torch.equal(getattr(padded, name), getattr(graph, name)), name
+    # the packed rows of the last iteration are the scheduled rows, in request order
+    B = int(flat.batch[-1])
+    assert int(flat.offsets[-1]) == B
+    ln = flat.lengths[-1].cpu()
+    rows = [r * (wl.gamma + 1) + i for r in range(wl.R) for i in range(int(ln[r]) + 1)]
+    want = flat.target.view(-1, wl.V)[torch.tensor(rows, device="cuda")]
+    assert torch.equal(flat.packed_target[:B], want)
+    assert padded.ws.status() == 0 and flat.ws.status() == 0 and graph.ws.status() == 0
 
 
 def test_async_loop_graph_replay_equals_eager(spec):

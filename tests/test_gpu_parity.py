@@ -179,7 +179,8 @@ def test_target_stats_match_oracle(spec, ws):
             assert abs((st[row, 0] + st[row, 1]) - (m + lz)) <= LOG_TOL * max(1, abs(m + lz))
 
 
-@pytest.mark.parametrize("R,gamma,V,rank", [(70, 4, 1000, 256), (5, 3, 2048, 0), (4, 2, 777, 40)])
+@pytest.mark.parametrize("R,gamma,V,rank", [(70, 4, 1000, 256), (5, 3, 2048, 0), (4, 2, 777, 40),
+                                           (96, 16, 129280, 256)])
 def test_tv_confidence_and_survival(spec, ws, R, gamma, V, rank):
     wl = _wl(R, gamma, V, rank, "bf16", seed=200 + V, T=0.9)
     g = to_dev(wl, "cuda")
