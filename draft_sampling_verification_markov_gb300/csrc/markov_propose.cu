@@ -1077,10 +1077,11 @@ cudaError_t launch_markov_propose_tc(const RowJob& j, const SelectOut& o, float*
   const int grid = num_sms();
   p.nsel = grid / 4 < 32 ? grid / 4 : 32;
   if (p.nsel < 1) p.nsel = 1;
-  // with a target, 5/16 of the SMs stream its rows for the normalisers meanwhile (at R = 256,
-  // gamma = 7 the step is shortest near that share: a statistics CTA reduces about 40 GB/s, and
-  // fewer streaming CTAs lengthen the proposal only once they drop below about 70)
-  p.nstat = target ? grid * 5 / 16 : 0;
+  // with a target, 29 % of the SMs stream its rows for the normalisers meanwhile: a statistics
+  // CTA reduces about 40 GB/s, and every CTA taken from the streaming ones lengthens the
+  // proposal. At R = 256, gamma = 7 on 152 SMs the launch is shortest with 43-44 (305 us;
+  // 310 us at 42 or 45, 321 us at 47, 354 us at 36 or 58)
+  p.nstat = target ? grid * 29 / 100 : 0;
   if (target && p.nstat < 1) p.nstat = 1;
   p.ns = grid - p.nsel - p.nstat;
   if (p.ns < 1) return cudaErrorInvalidConfiguration;
