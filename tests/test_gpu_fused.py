@@ -2,8 +2,9 @@
 against the oracle: the proposals follow the same comparison rules as spec_markov_propose, the
 target normalisers are checked against a float64 log-sum-exp of every row, and rejection
 verification with those normalisers against the oracle's. Shapes cover the persistent
-tensor-core launch (one and several request groups, a ragged last group) and the fallback of
-two separate passes (fp32 weights, no Markov head, no draft positions)."""
+tensor-core launch (one and two request groups, a ragged last group), the persistent proposal
+followed by a separate normaliser pass (more than two groups), and the fallback of two separate
+passes (fp32 weights, no Markov head, no draft positions)."""
 import numpy as np
 import pytest
 import torch
@@ -31,6 +32,7 @@ def _target_norms(target, T):
 
 
 @pytest.mark.parametrize("R,gamma,V,rank,wdt", [
+    (300, 2, 4104, 128, "bf16"),   # persistent proposal, three groups: normalisers after it
     (130, 3, 4104, 128, "bf16"),   # persistent: two groups, the second of two rows
     (9, 4, 2048, 256, "bf16"),     # persistent: one group
     (7, 3, 1000, 48, "f32"),       # two passes: fp32 weights on CUDA cores
