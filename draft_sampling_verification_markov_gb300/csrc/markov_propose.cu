@@ -15,8 +15,9 @@
 // Sweep s (s = 0 .. gamma*G - 1) is position k = s / G + 1 of group g = s % G: one pass over
 // all 128-column W2 tiles against the group's 128-row block.
 // CTAs (one per SM, all resident; a launch that cannot hold them all times out, it cannot hang):
-//   streaming CTAs (all but a quarter, at most 32, of the SMs) each take a contiguous range of
-//   tiles per sweep (rotated by one CTA per sweep, so that the longer ranges move around):
+//   streaming CTAs (the SMs left after the select CTAs and, with a target, the statistics
+//   CTAs) each take a contiguous range of tiles per sweep (rotated by one CTA per sweep, so
+//   that the longer ranges move around):
 //     warp 0      W2 (B operand) TMA producer, two 64 KB stages, evict-last (W2 stays in L2);
 //     warp 1      tensor-memory allocator and single-thread tcgen05.mma issuer (A from tensor
 //                 memory: two slots, one per sweep parity);
@@ -30,8 +31,11 @@
 //   released a sweep, a team draws its row's token with a two-level search (the row's coarse
 //   partials, in vocabulary order, give the normaliser and the crossing tile range; that range's
 //   64-column partials give the crossing segment, rebuilt element by element). The selects run
-//   on SMs of their own: on the streaming SMs they shared issue slots with the epilogue warps
-//   and took several times longer.
+//   on SMs of their own (a quarter of the SMs, at most 32): on the streaming SMs they shared
+//   issue slots with the epilogue warps and took several times longer.
+//   target-statistics CTAs (only with a target rows pointer: 29 % of the SMs) stream the target
+//   rows in 16 KB chunks through twelve bulk-copy stages into their softmax normalisers; they
+//   share nothing with the proposal but the launch, and fill the time its serial chain leaves.
 // Inter-CTA counters live at a fixed place of the caller's workspace; they are zero before a
 // launch (workspace initialisation) and the last CTA to finish puts them back to zero. Every
 // wait is bounded: on expiry the CTA sets SPEC_DEV_TIMEOUT and a workspace abort word, and
