@@ -108,6 +108,27 @@ def test_validation_rejects_before_launch(cuda_lib):
         ctypes.c_size_t, vp]
     assert gf(bogus, 1, bogus, bogus, None, 4, 3, 8, bogus, None, None, bogus, 1 << 20,
               None) == -1
+    # packing rows into the flattened layout: a row width that is not a multiple of 4 bytes,
+    # missing lengths, a misaligned destination
+    fp = cuda_lib.spec_flat_pack
+    fp.restype = ctypes.c_int
+    fp.argtypes = [vp, ctypes.c_int, vp, vp, ctypes.c_int, ctypes.c_int, vp, vp,
+                   ctypes.c_size_t, vp]
+    assert fp(bogus, 6, bogus, bogus, 4, 3, bogus, bogus, 1024, None) == -1
+    assert fp(bogus, 8, None, bogus, 4, 3, bogus, bogus, 1024, None) == -1
+    assert fp(bogus, 8, bogus, bogus, 4, 3, vp(0x1002), bogus, 1024, None) == -1
+    # the MTP greedy step: a bad dtype, no target, a workspace too small, no draft logits
+    mg = cuda_lib.spec_mtp_greedy
+    mg.restype = ctypes.c_int
+    mg.argtypes = [vp, vp, ctypes.c_int, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp,
+                   vp, vp, vp, ctypes.c_size_t, vp]
+    assert mg(bogus, bogus, 5, None, 4, 3, 64, bogus, bogus, None, None, bogus, 1 << 20,
+              None) == -2
+    assert mg(bogus, None, 1, None, 4, 3, 64, bogus, bogus, None, None, bogus, 1 << 20,
+              None) == -1
+    assert mg(bogus, bogus, 1, None, 4, 3, 64, bogus, bogus, None, None, bogus, 16, None) == -3
+    assert mg(None, bogus, 1, None, 4, 3, 64, bogus, bogus, None, None, bogus, 1 << 20,
+              None) == -1
     # the no-allocation greedy verify: beyond its fixed scratch, then a bad dtype
     na = cuda_lib.spec_verify_greedy_noalloc
     na.restype = ctypes.c_int
