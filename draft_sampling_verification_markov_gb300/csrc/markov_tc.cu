@@ -634,13 +634,24 @@ __global__ void __launch_bounds__(kThreads, 1)
               unpack_bf16x8(uw[c], uv);
 #pragma unroll
               for (int e = 0; e < 8; ++e) {
-                const float pt = prob_of(tv[e] * j.scale, tn);
-                float pd = prob_of((uv[e] + __uint_as_float(braw[c * 8 + e])) * j.scale, dn);
                 const int be = c * 8 + e;  // column of the warp's half tile
-                if (!(((be < 32 ? mlo : mhi) >> (be & 31)) & 1u)) pd = 0.0f;  // disallowed
+                const bool allowed = ((be < 32 ? mlo : mhi) >> (be & 31)) & 1u;
                 float x;
-                if constexpr (MODE == MODE_TV) x = fminf(pt, pd);
-                else x = fmaxf(pt - (resid ? pd : 0.0f), 0.0f);  // bonus rows: p_t
+                if constexpr (MODE == MODE_TV) {
+                  // min(p_t, p_d) = 2^min(a_t, a_d) for the exponents a of prob_of: exp is
+                  // increasing, so one exponential per element instead of two
+                  const float at = ((tv[e] * j.scale - tn.m) - tn.lz) * kLog2e;
+                  const float ad =
+                      allowed ? (((uv[e] + __uint_as_float(braw[c * 8 + e])) * j.scale - dn.m) -
+                                 dn.lz) * kLog2e
+                              : -INFINITY;  // a disallowed token has p_d = 0
+                  x = fast_exp2(fminf(at, ad));
+                } else {
+                  const float pt = prob_of(tv[e] * j.scale, tn);
+                  float pd = prob_of((uv[e] + __uint_as_float(braw[c * 8 + e])) * j.scale, dn);
+                  if (!allowed) pd = 0.0f;
+                  x = fmaxf(pt - (resid ? pd : 0.0f), 0.0f);  // bonus rows: p_t
+                }
                 acc[e & 3] += (!tail || vb + c * 8 + e < j.V) ? x : 0.0f;
               }
             }
