@@ -48,3 +48,34 @@ def test_expired_wait_reports_timeout_and_context_survives(spec):
     assert ws.status() == 0
     for a, b in zip(again, ref):
         assert torch.equal(a, b)
+
+
+def test_expired_wait_in_the_fused_launch(spec):
+    """The same with the target normalisers in the launch (statistics CTAs beside the
+    proposal): the stalled launch reports SPEC_DEV_TIMEOUT and returns, and the next call gives
+    the proposal and the normalisers of an unstalled run."""
+    wl = W.markov_rejection("cuda", R=130, gamma=2, V=4096, rank=128, seed=42)
+    run = lambda ws: spec.spec_markov_propose_target_stats(wl.U, wl.W1, wl.W2, wl.anchors, None,
+                                                           1.0, wl.target, workspace=ws)
+    ref_ws = spec.Workspace(device="cuda")
+    ref = [x.clone() for x in run(ref_ws)]
+    torch.cuda.synchronize()
+    assert ref_ws.status() == 0
+
+    ws = spec.Workspace(device="cuda")
+    run(ws)
+    torch.cuda.synchronize()
+    assert spec.lib().spec_test_stall_next_markov() == 0
+    t0 = time.time()
+    run(ws)
+    torch.cuda.synchronize()
+    waited = time.time() - t0
+    status = ws.status(clear=True)
+    assert status & SPEC_DEV_TIMEOUT, f"status {status:#x}"
+    assert 0.5 < waited < 30.0
+
+    again = run(ws)
+    torch.cuda.synchronize()
+    assert ws.status() == 0
+    for a, b in zip(again, ref):
+        assert torch.equal(a, b)
