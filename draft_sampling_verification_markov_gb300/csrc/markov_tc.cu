@@ -20,15 +20,15 @@
 //   U / T tiles: the base-logit (and target) rows of each (unit, row block), by TMA with an
 //      evict-first policy (read once), 64-column boxes in the 128-byte-swizzled layout; rows
 //      that are not equally spaced (the final rows of rejection verification) are copied by
-//      the producer warp with 16-byte cp.async into the same layout, each row's piece read
+//      six copier warps with 16-byte cp.async into the same layout, each row's piece read
 //      whole by neighbouring lanes.
 // The W1 rows of the A gather are prefetched into L2 by the kernel that drew the tokens, so
 // the logit stream starts at once.
-// Warp roles (384 threads, one CTA per SM, persistent over a contiguous range of units):
+// Warp roles (one CTA per SM, persistent over a contiguous range of units; struct Roles):
 //   warp 0  W2 (B operand) TMA producer;  warp 1  TMEM allocator + single-thread MMA issuer;
-//   warp 2  U / T tile producer (T rows only when rows are gathered);  warps 3..10  epilogue:
-//   warp w reads TMEM lanes 32*(w%4).. and column half (w-3)/4 of the tile;  warp 11  the
-//   gathered U rows (idle otherwise).
+//   tiles by TMA (384 threads): warp 2  U / T tile producer, warps 3..10  epilogue, warp 11
+//   idle; gathered rows (512 threads): warps 2, 3 and 12..15  row copiers, warps 4..11
+//   epilogue. An epilogue warp w reads TMEM lanes 32*(w%4).. and one column half of the tile.
 // Epilogues (per row, per N/2-column half tile, one partial each):
 //   MODE_STATS  z = (U + bias) * scale -> (max z, sum exp(z - max), first argmax);
 //   MODE_TV     sum min(p_d, p_t);    MODE_RESID  sum max(0, p_t - p_d) (p_t on bonus rows).
@@ -47,9 +47,23 @@ namespace tc {
 
 constexpr int kBM = 128;                            // rows per tile (one MMA, 128 TMEM lanes)
 constexpr int kEpiWarps = 8;
-constexpr int kFirstEpi = 3;                       // warps 0..2: B producer, MMA, U/T producer
-constexpr int kRowWarp = kFirstEpi + kEpiWarps;     // second producer of gathered rows
-constexpr int kThreads = (kRowWarp + 1) * 32;
+
+// Warp roles. Tiles by TMA (12 warps): 0 W2 producer, 1 MMA issuer, 2 U / T producer, 3..10
+// epilogue, 11 idle. Gathered rows (16 warps): 0 W2 producer, 1 MMA issuer, 2, 3 and 12..15
+// row copiers, 4..11 epilogue. A copier warp moves about 10 GB/s of 256-byte row pieces with
+// cp.async, so the gathered rows need several; the copiers and producers (warpgroups 0 and 3)
+// run on 80 registers and hand the rest to the epilogue warpgroups (1 and 2), which get 176:
+// 4 x 128 threads x 128 registers at launch = 2 x 128 x 80 + 2 x 128 x 176.
+template <bool GATHER>
+struct Roles {
+  static constexpr int kWarps = GATHER ? 16 : 12;
+  static constexpr int kThreads = kWarps * 32;
+  static constexpr int kFirstEpi = GATHER ? 4 : 3;
+  static constexpr int kCopiers = GATHER ? 6 : 1;
+  static constexpr int kRegsLow = 80, kRegsHigh = 176;
+  static_assert(!GATHER || 2 * kRegsLow + 2 * kRegsHigh == 4 * (65536 / kThreads),
+                "register split");
+};
 constexpr uint32_t kBoxBytes = kBM * 128;         // one TMA box: 128 rows x 64 columns (bf16)
 
 // Per pass mode. Shared memory (A lives in tensor memory):
@@ -142,11 +156,12 @@ __device__ __forceinline__ void row_norms_tc(const RowJob& j, const TileRow& tr,
 // of an odd count holds one block). The B tile is loaded once and feeds one MMA group per row
 // block, and both blocks' A operands stay in tensor memory while the CTA works on the pair.
 template <int MODE, bool ARGMAX, bool GATHER>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Roles<GATHER>::kThreads, 1)
     markov_tc_kernel(const __grid_constant__ CUtensorMap map_w2,
                      const __grid_constant__ CUtensorMap map_u,
                      const __grid_constant__ CUtensorMap map_t, const TcParams P) {
   using C = Cfg<MODE>;
+  using RL = Roles<GATHER>;
   constexpr int BN = C::kBN;
   constexpr int KB = C::kBStages, KU = C::kUStages, KA = C::kAccStages;
   constexpr bool kPair = MODE != MODE_STATS;  // needs target tiles
@@ -173,7 +188,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* scr_free = drain + 1;  // the first A gather is done with its scratch (B stage 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(scr_free + 1);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  // gathered modes: T and U row indices of the pair's two row blocks, [block][row]
+  // gathered rows: T and U row indices of the pair's two row blocks, [block][row]; each copier
+  // writes and reads only the entries of its own rows
   int* row_t = reinterpret_cast<int*>(tail + 256);
   // scratch of the CTA's first A gather (4 KB per epilogue warp): the second W2 stage, or with
   // a single W2 stage the second T stage; whoever fills it first waits for scr_free
@@ -202,7 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&b_empty[s], 1);
     }
     for (int s = 0; s < KU; ++s) {
-      mbar_init(&u_full[s], GATHER ? 64 : 1);  // gathered rows: one arrival per producer lane
+      mbar_init(&u_full[s], GATHER ? 32 * RL::kCopiers : 1);  // gathered: one per copier lane
       mbar_init(&u_empty[s], kEpiWarps);
     }
     for (int s = 0; s < KA; ++s) {
@@ -232,171 +248,186 @@ __global__ void __launch_bounds__(kThreads, 1)
   // tiles (inputs that no kernel writes) start loading before that kernel's completion; the
   // warps that read its tokens or write the partials it reads pass grid_dep_wait first.
 
-  if (warp == 0) {
-    // ---------------------------------------------------------------- W2 (B) producer
-    const uint64_t pol_keep = policy_evict_last();
-    int bs = 0;
-    uint32_t bph = 0;
-    bool ok = true;
-    int nt = nt_first;
-    for (long long u = u_begin; u < u_end && ok; ++u) {
-      const int n0 = nt * BN;
-      if (++nt == n_nt) nt = 0;
-      ok = mbar_wait(&b_empty[bs], bph ^ 1, abort, status);
-      if (ok && kScrInB && u == u_begin + 1) ok = mbar_wait(scr_free, 0, abort, status);
-      if (ok && lane == 0 && !(P.stall && u == u_begin)) {
-        mbar_arrive_expect_tx(&b_full[bs], ka_n * C::kBAtomBytes);
-        for (int ka = 0; ka < ka_n; ++ka)
-          tma_load_2d(sB + bs * C::kBStageBytes + ka * C::kBAtomBytes, &map_w2, ka * 64, n0,
-                      &b_full[bs], pol_keep);
-      }
-      if (++bs == KB) { bs = 0; bph ^= 1; }
-    }
-    // drain: every issued copy lands before the CTA moves on
-    if (lane == 0)
-      for (int s = 0; s < KB; ++s) mbar_drain(&b_full[s], (s < bs) ? bph : (bph ^ 1));
-  } else if (warp == 2 || (GATHER && warp == kRowWarp)) {
-    // ---------------------------------------------------------------- U / T producer
-    const uint64_t pol_stream = policy_evict_first();
-    int us = 0;
-    uint32_t uph = 0;
-    bool ok = true;
-    int mp = mp_first, nt = nt_first, rows_mp = -1;
-    const bool tside = warp == 2;
-    if constexpr (GATHER) grid_dep_wait();  // the final rows come from the acceptance scan
-    // gathered row indices of the pair's two row blocks, loaded once per pair into a table
-    // (rows past R and the U rows of bonus rows point at row 0 and are ignored)
-    for (long long u = u_begin; u < u_end && ok; ++u) {
-      const int n0 = nt * BN;
-      const int nb = 2 * mp + 1 < n_mt ? 2 : 1;
-      if constexpr (GATHER) {
-        // warp 2 gathers the T rows and the second producer warp the U rows; each builds its
-        // own table, with every load of a lane in flight at once
-        if (mp != rows_mp) {
-          rows_mp = mp;
-          constexpr int kPer = 2 * kBM / 32;
-          int nn[kPer], kind[kPer];
-#pragma unroll
-          for (int t = 0; t < kPer; ++t) {
-            const int q = lane + 32 * t, r = 2 * mp * kBM + q;  // q / kBM: block of the pair
-            const bool in = r < j.R && q / kBM < nb;
-            nn[t] = in ? j.final_n[r] : -1;
-            kind[t] = in && !tside ? j.final_kind[r] : 0;
-          }
-#pragma unroll
-          for (int t = 0; t < kPer; ++t) {
-            const int q = lane + 32 * t, r = 2 * mp * kBM + q;
-            if (tside) row_t[q] = nn[t] >= 0 ? (int)target_row(j, r, nn[t]) : 0;
-            else row_u[q] = kind[t] ? r * j.gamma + nn[t] : 0;
-          }
-          __syncwarp();
-        }
-      }
-      for (int sb = 0; sb < nb && ok; ++sb) {
-        const int mt = 2 * mp + sb;
-        ok = mbar_wait(&u_empty[us], uph ^ 1, abort, status);
-        if (ok && !kScrInB && us == 1 && uph == 0) ok = mbar_wait(scr_free, 0, abort, status);
-        if (!ok) break;
-        unsigned char* du = sU + us * C::kTileBytes;
-        unsigned char* dt = sT + us * C::kTileBytes;
-        if constexpr (!GATHER) {
-          if (lane == 0) {
-            const TileRow tr = tile_row(j, P.t, mt, 0);
-            const int r0 = tr.r, kk = tr.k - 1;
-            mbar_arrive_expect_tx(&u_full[us], (kPair ? 2u : 1u) * C::kTileBytes);
-            for (int b = 0; b < C::kBoxes; ++b) {
-              tma_load_3d(du + b * kBoxBytes, &map_u, n0 + b * 64, kk, r0, &u_full[us],
-                          pol_stream);
-              if constexpr (kPair)
-                tma_load_3d(dt + b * kBoxBytes, &map_t, n0 + b * 64, kk, r0, &u_full[us],
-                            pol_stream);
-            }
-          }
-        } else {
-          // final rows of rejection verification: per instruction, 8 lanes per 64-column box
-          // copy one row's piece (16 bytes each) of this warp's tensor (T or U), so a warp
-          // moves 4 / kBoxes whole row pieces; pieces land in the 128-byte swizzled box layout,
-          // and columns past V are zero-filled without a read
-          constexpr int kLanesPerRow = 8 * C::kBoxes, kRowsPerInstr = 32 / kLanesPerRow;
-          const unsigned short* Tb = static_cast<const unsigned short*>(j.T);
-          const unsigned short* Ub = static_cast<const unsigned short*>(j.U);
-          const uint32_t st_base = smem_u32(dt), su_base = smem_u32(du);
-          const int c = lane % kLanesPerRow;          // 16-byte chunk of the row piece
-          const int bx = c >> 3, cc = c & 7;          // box and chunk within the box
-          const uint32_t nb16 = n0 + 8 * c < j.V ? 16u : 0u;
-#pragma unroll 4
-          for (int k = 0; k < kBM / kRowsPerInstr; ++k) {
-            const int i = kRowsPerInstr * k + lane / kLanesPerRow;  // row within the block
-            const int* tab = tside ? row_t : row_u;
-            const long long ro = (long long)tab[sb * kBM + i] * j.V + n0 + 8 * c;
-            const uint32_t so = bx * kBoxBytes + i * 128 + ((cc ^ (i & 7)) << 4);
-            cp_async16((tside ? st_base : su_base) + so, (tside ? Tb : Ub) + (nb16 ? ro : 0),
-                       nb16, pol_stream);
-          }
-          cp_async_arrive(&u_full[us]);
-        }
-        if (++us == KU) { us = 0; uph ^= 1; }
-      }
-      if (++nt == n_nt) { nt = 0; ++mp; }
-    }
-    if (lane == 0)
-      for (int s = 0; s < KU; ++s) mbar_drain(&u_full[s], (s < us) ? uph : (uph ^ 1));
-  } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA issuer
-    constexpr uint32_t idesc = idesc_bf16(kBM, BN);
-    if (lane == 0) {
-      bool ok = true;
-      int bs = 0, as = 0;
+  const bool epi_warp = warp >= RL::kFirstEpi && warp < RL::kFirstEpi + kEpiWarps;
+  if (!epi_warp) {
+    if constexpr (GATHER) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(RL::kRegsLow));
+    if (warp == 0) {
+      // ---------------------------------------------------------------- W2 (B) producer
+      const uint64_t pol_keep = policy_evict_last();
+      int bs = 0;
       uint32_t bph = 0;
-      uint32_t accph[KA] = {};
-      int mp = mp_first, nt = nt_first, cur_mp = -1, pair_i = -1;
+      bool ok = true;
+      int nt = nt_first;
       for (long long u = u_begin; u < u_end && ok; ++u) {
-        const int nb = 2 * mp + 1 < n_mt ? 2 : 1;
-        const bool first = mp != cur_mp;
-        if (first) {
-          cur_mp = mp;
-          ++pair_i;
+        const int n0 = nt * BN;
+        if (++nt == n_nt) nt = 0;
+        ok = mbar_wait(&b_empty[bs], bph ^ 1, abort, status);
+        if (ok && kScrInB && u == u_begin + 1) ok = mbar_wait(scr_free, 0, abort, status);
+        if (ok && lane == 0 && !(P.stall && u == u_begin)) {
+          mbar_arrive_expect_tx(&b_full[bs], ka_n * C::kBAtomBytes);
+          for (int ka = 0; ka < ka_n; ++ka)
+            tma_load_2d(sB + bs * C::kBStageBytes + ka * C::kBAtomBytes, &map_w2, ka * 64, n0,
+                        &b_full[bs], pol_keep);
         }
-        ok = mbar_wait(&b_full[bs], bph, abort, status);
-        if (!ok) break;
-        tc_fence_after();
-        for (int sb = 0; sb < nb && ok; ++sb) {
-          if (first) {
-            ok = mbar_wait(&a_full[sb], pair_i & 1, abort, status);
-            if (!ok) break;
+        if (++bs == KB) { bs = 0; bph ^= 1; }
+      }
+      // drain: every issued copy lands before the CTA moves on
+      if (lane == 0)
+        for (int s = 0; s < KB; ++s) mbar_drain(&b_full[s], (s < bs) ? bph : (bph ^ 1));
+    } else if (warp == 2 || (GATHER && (warp == 3 || warp >= 12))) {
+      // ---------------------------------------------------------------- U / T producer
+      const uint64_t pol_stream = policy_evict_first();
+      int us = 0;
+      uint32_t uph = 0;
+      bool ok = true;
+      int mp = mp_first, nt = nt_first, rows_mp = -1;
+      // gathered rows: copiers 0..2 take the T rows and 3..5 the U rows of every block, each
+      // the rows [r_lo, r_hi) (42, 42 and 44 of 128)
+      const int cw = warp <= 3 ? warp - 2 : warp - 10;
+      const bool tside = cw < 3;
+      const int sub = cw % 3;
+      const int r_lo = (sub * kBM / 3) & ~1, r_hi = sub == 2 ? kBM : ((sub + 1) * kBM / 3) & ~1;
+      if constexpr (GATHER) grid_dep_wait();  // the final rows come from the acceptance scan
+      // gathered row indices of the pair's two row blocks, loaded once per pair into a table
+      // (rows past R and the U rows of bonus rows point at row 0 and are ignored)
+      for (long long u = u_begin; u < u_end && ok; ++u) {
+        const int n0 = nt * BN;
+        const int nb = 2 * mp + 1 < n_mt ? 2 : 1;
+        if constexpr (GATHER) {
+          // each copier builds the table entries of its own rows in both blocks (2 x 44 at
+          // most), with every load of a lane in flight at once
+          if (mp != rows_mp) {
+            rows_mp = mp;
+            const int nr = r_hi - r_lo;
+            int nn[3], kind[3];
+#pragma unroll
+            for (int t = 0; t < 3; ++t) {
+              const int e = lane + 32 * t, sbx = e >= nr ? 1 : 0, ii = r_lo + e - sbx * nr;
+              const int r = (2 * mp + sbx) * kBM + ii;
+              const bool in = e < 2 * nr && sbx < nb && r < j.R;
+              nn[t] = in ? j.final_n[r] : -1;
+              kind[t] = in && !tside ? j.final_kind[r] : 0;
+            }
+#pragma unroll
+            for (int t = 0; t < 3; ++t) {
+              const int e = lane + 32 * t, sbx = e >= nr ? 1 : 0, ii = r_lo + e - sbx * nr;
+              const int r = (2 * mp + sbx) * kBM + ii;
+              if (e < 2 * nr) {
+                if (tside) row_t[sbx * kBM + ii] = nn[t] >= 0 ? (int)target_row(j, r, nn[t]) : 0;
+                else row_u[sbx * kBM + ii] = kind[t] ? r * j.gamma + nn[t] : 0;
+              }
+            }
+            __syncwarp();
           }
-          ok = mbar_wait(&acc_empty[as], accph[as] ^ 1, abort, status);
+        }
+        for (int sb = 0; sb < nb && ok; ++sb) {
+          const int mt = 2 * mp + sb;
+          ok = mbar_wait(&u_empty[us], uph ^ 1, abort, status);
+          // the first fill of T stage 1 waits until the first A gather is done with it
+          if (ok && !kScrInB && us == 1 && uph == 0 && (!GATHER || tside))
+            ok = mbar_wait(scr_free, 0, abort, status);
+          if (!ok) break;
+          unsigned char* du = sU + us * C::kTileBytes;
+          unsigned char* dt = sT + us * C::kTileBytes;
+          if constexpr (!GATHER) {
+            if (lane == 0) {
+              const TileRow tr = tile_row(j, P.t, mt, 0);
+              const int r0 = tr.r, kk = tr.k - 1;
+              mbar_arrive_expect_tx(&u_full[us], (kPair ? 2u : 1u) * C::kTileBytes);
+              for (int b = 0; b < C::kBoxes; ++b) {
+                tma_load_3d(du + b * kBoxBytes, &map_u, n0 + b * 64, kk, r0, &u_full[us],
+                            pol_stream);
+                if constexpr (kPair)
+                  tma_load_3d(dt + b * kBoxBytes, &map_t, n0 + b * 64, kk, r0, &u_full[us],
+                              pol_stream);
+              }
+            }
+          } else {
+            // final rows of rejection verification: per instruction, 8 lanes per 64-column box
+            // copy one row's piece (16 bytes each) of this copier's tensor (T or U), so a warp
+            // moves 4 / kBoxes whole row pieces; pieces land in the 128-byte swizzled box layout,
+            // and columns past V are zero-filled without a read
+            constexpr int kLanesPerRow = 8 * C::kBoxes, kRowsPerInstr = 32 / kLanesPerRow;
+            static_assert(kRowsPerInstr == 2, "copier row ranges are even");
+            const unsigned short* src = static_cast<const unsigned short*>(tside ? j.T : j.U);
+            const int* tab = tside ? row_t : row_u;
+            const uint32_t dst = smem_u32(tside ? dt : du);
+            const int c = lane % kLanesPerRow;          // 16-byte chunk of the row piece
+            const int bx = c >> 3, cc = c & 7;          // box and chunk within the box
+            const uint32_t nb16 = n0 + 8 * c < j.V ? 16u : 0u;
+#pragma unroll 4
+            for (int k = 0; k < (r_hi - r_lo) / kRowsPerInstr; ++k) {
+              const int i = r_lo + kRowsPerInstr * k + lane / kLanesPerRow;  // row of the block
+              const long long ro = (long long)tab[sb * kBM + i] * j.V + n0 + 8 * c;
+              const uint32_t so = bx * kBoxBytes + i * 128 + ((cc ^ (i & 7)) << 4);
+              cp_async16(dst + so, src + (nb16 ? ro : 0), nb16, pol_stream);
+            }
+            cp_async_arrive(&u_full[us]);
+          }
+          if (++us == KU) { us = 0; uph ^= 1; }
+        }
+        if (++nt == n_nt) { nt = 0; ++mp; }
+      }
+      if (lane == 0)
+        for (int s = 0; s < KU; ++s) mbar_drain(&u_full[s], (s < us) ? uph : (uph ^ 1));
+    } else if (warp == 1) {
+      // ---------------------------------------------------------------- MMA issuer
+      constexpr uint32_t idesc = idesc_bf16(kBM, BN);
+      if (lane == 0) {
+        bool ok = true;
+        int bs = 0, as = 0;
+        uint32_t bph = 0;
+        uint32_t accph[KA] = {};
+        int mp = mp_first, nt = nt_first, cur_mp = -1, pair_i = -1;
+        for (long long u = u_begin; u < u_end && ok; ++u) {
+          const int nb = 2 * mp + 1 < n_mt ? 2 : 1;
+          const bool first = mp != cur_mp;
+          if (first) {
+            cur_mp = mp;
+            ++pair_i;
+          }
+          ok = mbar_wait(&b_full[bs], bph, abort, status);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t d = tmem + as * BN;
-          const uint32_t a = tmem + C::kAccCols + sb * C::kACols;
-          for (int ka = 0; ka < ka_n; ++ka) {
-            const uint32_t b_base = smem_u32(sB + bs * C::kBStageBytes + ka * C::kBAtomBytes);
-            // K = 16 per instruction: 8 tensor-memory columns of A, 32 bytes of a B row
+          for (int sb = 0; sb < nb && ok; ++sb) {
+            if (first) {
+              ok = mbar_wait(&a_full[sb], pair_i & 1, abort, status);
+              if (!ok) break;
+            }
+            ok = mbar_wait(&acc_empty[as], accph[as] ^ 1, abort, status);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t d = tmem + as * BN;
+            const uint32_t a = tmem + C::kAccCols + sb * C::kACols;
+            for (int ka = 0; ka < ka_n; ++ka) {
+              const uint32_t b_base = smem_u32(sB + bs * C::kBStageBytes + ka * C::kBAtomBytes);
+              // K = 16 per instruction: 8 tensor-memory columns of A, 32 bytes of a B row
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-              mma_bf16_ta(d, a + ka * 32 + ks * 8, sw128_desc(b_base + ks * 32), idesc,
-                          (ka | ks) != 0);
+              for (int ks = 0; ks < 4; ++ks)
+                mma_bf16_ta(d, a + ka * 32 + ks * 8, sw128_desc(b_base + ks * 32), idesc,
+                            (ka | ks) != 0);
+            }
+            mma_commit(&acc_full[as]);
+            accph[as] ^= 1;
+            if (++as == KA) as = 0;
           }
-          mma_commit(&acc_full[as]);
-          accph[as] ^= 1;
-          if (++as == KA) as = 0;
+          if (!ok) break;
+          mma_commit(&b_empty[bs]);
+          if (++bs == KB) { bs = 0; bph ^= 1; }
+          if (++nt == n_nt) { nt = 0; ++mp; }
+          if (u + 1 == u_end || mp != cur_mp) mma_commit(a_empty);  // last unit of this pair
         }
-        if (!ok) break;
-        mma_commit(&b_empty[bs]);
-        if (++bs == KB) { bs = 0; bph ^= 1; }
-        if (++nt == n_nt) { nt = 0; ++mp; }
-        if (u + 1 == u_end || mp != cur_mp) mma_commit(a_empty);  // last unit of this pair
+        // all MMAs issued by this thread complete before tensor memory is released
+        mma_commit(drain);
+        mbar_drain(drain, 0);
       }
-      // all MMAs issued by this thread complete before tensor memory is released
-      mma_commit(drain);
-      mbar_drain(drain, 0);
+      __syncwarp();
     }
-    __syncwarp();
-  } else if (warp >= kFirstEpi && warp < kFirstEpi + kEpiWarps) {
+  } else {
+    if constexpr (GATHER) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(RL::kRegsHigh));
     // ---------------------------------------------------------------- epilogue
     grid_dep_wait();
-    const int ew = warp - kFirstEpi;
+    const int ew = warp - RL::kFirstEpi;
     const int q = warp & 3;          // TMEM lane quarter
     const int h = ew >> 2;           // column half
     const int i = q * 32 + lane;     // row within the tile (TMEM lane)
@@ -627,32 +658,45 @@ __global__ void __launch_bounds__(kThreads, 1)
             // that the exponentials of all columns overlap; four partial sums
             float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
             const int vb = n0 + col0;
+            const bool masked = j.mask != nullptr;
 #pragma unroll
             for (int c = 0; c < kHalf / 8; ++c) {
               float uv[8], tv[8];
               unpack_bf16x8(tw[c], tv);
               unpack_bf16x8(uw[c], uv);
+              // Outside the element loop, in the tiles that have them: a column past V gets both
+              // logits -inf (its term is 0 in both modes, even beside a non-finite normaliser)
+              // and a disallowed token the base logit -inf (p_d = 0).
+              if (tail) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                  if (vb + c * 8 + e >= j.V) tv[e] = uv[e] = -INFINITY;
+              }
+              if (masked) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                  const int be = c * 8 + e;  // column of the warp's half tile
+                  if (!(((be < 32 ? mlo : mhi) >> (be & 31)) & 1u)) uv[e] = -INFINITY;
+                }
+              }
 #pragma unroll
               for (int e = 0; e < 8; ++e) {
-                const int be = c * 8 + e;  // column of the warp's half tile
-                const bool allowed = ((be < 32 ? mlo : mhi) >> (be & 31)) & 1u;
                 float x;
                 if constexpr (MODE == MODE_TV) {
                   // min(p_t, p_d) = 2^min(a_t, a_d) for the exponents a of prob_of: exp is
                   // increasing, so one exponential per element instead of two
                   const float at = ((tv[e] * j.scale - tn.m) - tn.lz) * kLog2e;
                   const float ad =
-                      allowed ? (((uv[e] + __uint_as_float(braw[c * 8 + e])) * j.scale - dn.m) -
-                                 dn.lz) * kLog2e
-                              : -INFINITY;  // a disallowed token has p_d = 0
+                      (((uv[e] + __uint_as_float(braw[c * 8 + e])) * j.scale - dn.m) - dn.lz) *
+                      kLog2e;
                   x = fast_exp2(fminf(at, ad));
                 } else {
                   const float pt = prob_of(tv[e] * j.scale, tn);
-                  float pd = prob_of((uv[e] + __uint_as_float(braw[c * 8 + e])) * j.scale, dn);
-                  if (!allowed) pd = 0.0f;
+                  const float pd =
+                      prob_of((uv[e] + __uint_as_float(braw[c * 8 + e])) * j.scale, dn);
                   x = fmaxf(pt - (resid ? pd : 0.0f), 0.0f);  // bonus rows: p_t
                 }
-                acc[e & 3] += (!tail || vb + c * 8 + e < j.V) ? x : 0.0f;
+                acc[e & 3] += x;
               }
             }
             P.ps[o] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
@@ -725,7 +769,8 @@ cudaError_t launch_t(const TcParams& p, const CUtensorMap& w2, const CUtensorMap
   auto k = markov_tc_kernel<MODE, ARGMAX, GATHER>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  return launch_kernel(k, dim3(grid), dim3(kThreads), smem, s, p.j.pdl != 0, w2, u, t, p);
+  return launch_kernel(k, dim3(grid), dim3(Roles<GATHER>::kThreads), smem, s, p.j.pdl != 0, w2,
+                       u, t, p);
 }
 
 }  // namespace tc
@@ -802,15 +847,7 @@ cudaError_t launch_markov_tc(const RowJob& j, float* pm, float* ps, int* pi, boo
       const cuuint64_t st[2] = {(cuuint64_t)j.V * 2, (cuuint64_t)j.V * 2 * (j.gamma + 1)};
       if (!make_map(&t, j.T, 3, dt, st, box)) return cudaErrorInvalidValue;
     }
-  } else {
-    // rows gathered four at a time: 2-D maps over all rows, boxes one row high
-    const cuuint32_t box[2] = {64, 1};
-    const cuuint64_t du[2] = {(cuuint64_t)j.V, (cuuint64_t)j.R * j.gamma};
-    const cuuint64_t dt[2] = {(cuuint64_t)j.V, (cuuint64_t)j.R * (j.gamma + 1)};
-    const cuuint64_t sv[1] = {(cuuint64_t)j.V * 2};
-    if (!make_map(&u, j.U, 2, du, sv, box)) return cudaErrorInvalidValue;
-    if (!make_map(&t, j.T, 2, dt, sv, box)) return cudaErrorInvalidValue;
-  }
+  }  // gathered rows are copied with cp.async: their maps stay zero and unused
   if (j.mode == MODE_STATS) {
     if (argmax) return launch_t<MODE_STATS, true, false>(p, w2, u, t, grid, s);
     return launch_t<MODE_STATS, false, false>(p, w2, u, t, grid, s);

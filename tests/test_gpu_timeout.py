@@ -79,3 +79,35 @@ def test_expired_wait_in_the_fused_launch(spec):
     assert ws.status() == 0
     for a, b in zip(again, ref):
         assert torch.equal(a, b)
+
+
+def test_expired_wait_in_the_residual_pass(spec):
+    """The same on the residual pass of rejection verification (gathered final rows, six copier
+    warps and a register split between warpgroups): the stalled pass reports SPEC_DEV_TIMEOUT
+    and returns, and the next verify gives the results of an unstalled run."""
+    wl = W.markov_rejection("cuda", R=130, gamma=3, V=4096, rank=128, seed=43)
+    ws = spec.Workspace(device="cuda")
+    toks, logp, stats = spec.spec_markov_propose(wl.U, wl.W1, wl.W2, wl.anchors, wl.u_draft,
+                                                 1.0, workspace=ws)
+    tst = spec.spec_target_stats(wl.target, 1.0, workspace=ws)
+    ver = lambda: spec.spec_verify_rejection(wl.target, wl.U, wl.W1, wl.W2, wl.anchors, toks,
+                                             logp, stats, wl.u_accept, wl.u_resid, 1.0,
+                                             target_stats=tst, workspace=ws)
+    ref = [x.clone() for x in ver()]
+    torch.cuda.synchronize()
+    assert ws.status() == 0
+
+    assert spec.lib().spec_test_stall_next_markov() == 0
+    t0 = time.time()
+    ver()
+    torch.cuda.synchronize()
+    waited = time.time() - t0
+    status = ws.status(clear=True)
+    assert status & SPEC_DEV_TIMEOUT, f"status {status:#x}"
+    assert 0.5 < waited < 30.0
+
+    again = ver()
+    torch.cuda.synchronize()
+    assert ws.status() == 0
+    for a, b in zip(again, ref):
+        assert torch.equal(a, b)
