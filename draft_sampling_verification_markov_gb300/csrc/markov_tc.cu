@@ -613,34 +613,28 @@ __global__ void __launch_bounds__(Roles<GATHER>::kThreads, 1)
         tc_fence_after();
         ok = mbar_wait(&u_full[us], uph, abort, status);
         if (!ok) break;
-        // TMEM reads and shared-memory reads first, then release the stages
-        uint32_t braw[kHalf];
-        tmem_ld32_async(taddr, braw);
-        if constexpr (kHalf == 64) tmem_ld32_async(taddr + 32, braw + 32);
+        const size_t o = (size_t)tr.prow * P.nseg + (n0 + col0) / kHalf;
         const uint32_t u_base = smem_u32(sU + us * C::kTileBytes);
         const uint32_t t_base = smem_u32(sT + us * C::kTileBytes);
-        uint4 uw[kHalf / 8], tw[kHalf / 8];
-#pragma unroll
-        for (int c = 0; c < kHalf / 8; ++c) {
-          const int col = col0 + 8 * c;
-          const int b = col >> 6, cc = (col & 63) >> 3;
-          const uint32_t off = b * kBoxBytes + i * 128 + ((cc ^ (i & 7)) << 4);
-          uw[c] = lds128(u_base + off);
-          if constexpr (kPair) tw[c] = lds128(t_base + off);
-        }
-        tmem_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&acc_empty[as]);
-          mbar_arrive(&u_empty[us]);
-        }
-        if (++us == KU) { us = 0; uph ^= 1; }
-        accph[as] ^= 1;
-        if (++as == KA) as = 0;
-
-        const size_t o = (size_t)tr.prow * P.nseg + (n0 + col0) / kHalf;
         if constexpr (MODE == MODE_STATS) {
+          // TMEM reads and shared-memory reads first, then release the stages
+          uint32_t braw[kHalf];
+          tmem_ld32_async(taddr, braw);
+          if constexpr (kHalf == 64) tmem_ld32_async(taddr + 32, braw + 32);
+          uint4 uw[kHalf / 8];
+#pragma unroll
+          for (int c = 0; c < kHalf / 8; ++c) {
+            const int col = col0 + 8 * c;
+            const int b = col >> 6, cc = (col & 63) >> 3;
+            uw[c] = lds128(u_base + b * kBoxBytes + i * 128 + ((cc ^ (i & 7)) << 4));
+          }
+          tmem_wait_ld();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&acc_empty[as]);
+            mbar_arrive(&u_empty[us]);
+          }
           float m, sum;
           int idx;
           stats_partial64<ARGMAX>(braw, uw, j.scale, n0 + col0, j.V, tail, j.mask != nullptr, mlo,
@@ -653,14 +647,39 @@ __global__ void __launch_bounds__(Roles<GATHER>::kThreads, 1)
         } else {
           const Norm dn = sb ? dn1 : dn0, tn = sb ? tn1 : tn0;
           const bool resid = sb ? rs1 : rs0;
-          if (live) {
-            // branch-free: every column's two probabilities are computed, then selected, so
-            // that the exponentials of all columns overlap; four partial sums
-            float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            const int vb = n0 + col0;
-            const bool masked = j.mask != nullptr;
+          // 32 columns at a time (one rolled loop, so the code stays small): their accumulators
+          // and logits, then their terms; the stages are released after the last reads.
+          // Branch-free: every column's two probabilities are computed, then selected, so that
+          // the exponentials of all columns overlap; four partial sums, in column order.
+          float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+          const bool masked = j.mask != nullptr;
+#pragma unroll 1
+          for (int hh = 0; hh < kHalf / 32; ++hh) {
+            uint32_t braw[32];
+            tmem_ld32_async(taddr + 32 * hh, braw);
+            uint4 uw[4], tw[4];
 #pragma unroll
-            for (int c = 0; c < kHalf / 8; ++c) {
+            for (int c = 0; c < 4; ++c) {
+              const int col = col0 + 32 * hh + 8 * c;
+              const int b = col >> 6, cc = (col & 63) >> 3;
+              const uint32_t off = b * kBoxBytes + i * 128 + ((cc ^ (i & 7)) << 4);
+              uw[c] = lds128(u_base + off);
+              tw[c] = lds128(t_base + off);
+            }
+            tmem_wait_ld();
+            if (hh == kHalf / 32 - 1) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) {
+                mbar_arrive(&acc_empty[as]);
+                mbar_arrive(&u_empty[us]);
+              }
+            }
+            if (!live) continue;
+            const int vb = n0 + col0 + 32 * hh;   // first column of these 32
+            const uint32_t mbits = hh ? mhi : mlo;  // their allowed-token bits
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
               float uv[8], tv[8];
               unpack_bf16x8(tw[c], tv);
               unpack_bf16x8(uw[c], uv);
@@ -674,10 +693,8 @@ __global__ void __launch_bounds__(Roles<GATHER>::kThreads, 1)
               }
               if (masked) {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                  const int be = c * 8 + e;  // column of the warp's half tile
-                  if (!(((be < 32 ? mlo : mhi) >> (be & 31)) & 1u)) uv[e] = -INFINITY;
-                }
+                for (int e = 0; e < 8; ++e)
+                  if (!((mbits >> (c * 8 + e)) & 1u)) uv[e] = -INFINITY;
               }
 #pragma unroll
               for (int e = 0; e < 8; ++e) {
@@ -699,9 +716,12 @@ __global__ void __launch_bounds__(Roles<GATHER>::kThreads, 1)
                 acc[e & 3] += x;
               }
             }
-            P.ps[o] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
           }
+          if (live) P.ps[o] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
         }
+        if (++us == KU) { us = 0; uph ^= 1; }
+        accph[as] ^= 1;
+        if (++as == KA) as = 0;
       }
       if (++nt == n_nt) { nt = 0; ++mp; }
     }
